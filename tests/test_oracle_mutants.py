@@ -1,0 +1,113 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that a pin fails.
+
+Each case swaps one rule of the oracle for a wrong one -- an index off by one,
+a flipped half, a reversed pairing, a dropped term, a different tie rule -- and
+re-runs the pin that is meant to catch it. A mutant that survives would mean
+the pins cannot tell the pages' method from a near miss.
+"""
+
+import numpy as np
+import pytest
+
+from conftest import read_golden
+from oracle import numerics, schedules
+import test_oracle_pins as pins
+import test_oracle_properties as props
+
+
+def _plant_ring_rule(monkeypatch, phase, rule):
+    orig = schedules._ring_phase
+
+    def patched(w, rings, r, reduce, combine, name):
+        return orig(w, rings, rule if name == phase else r, reduce, combine, name)
+
+    monkeypatch.setattr(schedules, "_ring_phase", patched)
+
+
+def test_mutant_reduce_scatter_index(monkeypatch):
+    _plant_ring_rule(monkeypatch, "reduce-scatter", lambda p, s: p + s)
+    with pytest.raises(AssertionError):
+        pins.test_ring_send_table_fig_4_2(read_golden)
+
+
+def test_mutant_all_gather_index(monkeypatch):
+    _plant_ring_rule(monkeypatch, "all-gather", lambda p, s: p - s)
+    with pytest.raises(AssertionError):
+        pins.test_ring_trace_4gpu(read_golden)
+
+
+def test_mutant_intra_group_slice_rule(monkeypatch):
+    # "send slice (l - s)" in phase 1 leaves local rank l owning slice l+1 and
+    # breaks the hierarchical sum order
+    _plant_ring_rule(monkeypatch, "intra-group reduce-scatter", lambda p, s: p - s)
+    with pytest.raises(AssertionError):
+        props.test_scale_and_bf16_finish_applied_once()
+
+
+def test_mutant_receiver_overwrites_instead_of_adding(monkeypatch):
+    orig = schedules._ring_phase
+
+    def patched(w, rings, rule, reduce, combine, name):
+        return orig(w, rings, rule, reduce, (lambda a, b: a) if reduce else combine, name)
+
+    monkeypatch.setattr(schedules, "_ring_phase", patched)
+    with pytest.raises(AssertionError):
+        pins.test_ring_trace_4gpu(read_golden)
+
+
+def test_mutant_rabenseifner_keeps_other_half(monkeypatch):
+    src = schedules.rabenseifner_allreduce
+
+    def flipped(x, **kw):
+        # run with rank bits complemented: the kept half is the other one
+        N = x.shape[0]
+        out, st = src(x[::-1].copy(), **kw)
+        st.owned = {N - 1 - i: v for i, v in st.owned.items()}
+        return out[::-1], st
+
+    monkeypatch.setattr(schedules, "rabenseifner_allreduce", flipped)
+    with pytest.raises(AssertionError):
+        pins.test_rabenseifner_fig_4_5(read_golden)
+
+
+def test_mutant_tree_pairs_far_ranks_first(monkeypatch):
+    def far_first(values):
+        vals = list(values)
+        while len(vals) > 1:
+            h = len(vals) // 2
+            vals = [vals[m] + vals[m + h] for m in range(h)]
+        return vals[0]
+
+    monkeypatch.setattr(numerics, "_tree", far_first)
+    with pytest.raises(AssertionError):
+        props.test_brute_force_every_algorithm(8, 64)
+
+
+def test_mutant_ring_order_starts_one_rank_late(monkeypatch):
+    orig = numerics._left_fold
+
+    def late(x, ranks, cols=slice(None)):
+        return orig(x, ranks[1:] + ranks[:1], cols)
+
+    monkeypatch.setattr(numerics, "_left_fold", late)
+    with pytest.raises(AssertionError):
+        props.test_brute_force_every_algorithm(5, 31)
+
+
+def test_mutant_bf16_ties_away_from_zero(monkeypatch):
+    def away(x):
+        bits = np.ascontiguousarray(x, np.float32).view(np.uint32)
+        return ((bits + np.uint32(0x8000)) >> np.uint32(16)).astype(np.uint16)
+
+    monkeypatch.setattr(numerics, "f32_to_bf16_rne", away)
+    with pytest.raises(AssertionError):
+        props.test_bf16_rne_hand_built(0x3F808000, 0x3F80)
+
+
+def test_mutant_bf16_truncation(monkeypatch):
+    def trunc(x):
+        return (np.ascontiguousarray(x, np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+    monkeypatch.setattr(numerics, "f32_to_bf16_rne", trunc)
+    with pytest.raises(AssertionError):
+        props.test_bf16_rne_matches_torch_conversion()
