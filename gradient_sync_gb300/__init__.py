@@ -1,0 +1,195 @@
+"""GB300 gradient all-reduce over N virtual ranks held in one GPU's memory.
+
+A thin Python binding of libar_gb300.so: the functions below carry the C
+ABI's names (include/ar.h) and only marshal arguments -- torch tensors or raw
+integer device pointers in, status codes out as exceptions. Every step of the
+all-reduce runs in the library's CUDA kernels; there is no Python or CPU
+fallback, and importing a function whose library is missing raises.
+"""
+
+from __future__ import annotations
+
+from . import _lib
+
+# ---- enums of include/ar.h
+AR_OK, AR_EINVAL, AR_EUNSUPPORTED, AR_ENOMEM, AR_ECUDA, AR_ETIMEOUT = range(6)
+AR_F32, AR_BF16 = 0, 1
+AR_RING, AR_RABENSEIFNER, AR_HIER, AR_FUSED = 0, 1, 2, 3
+AR_ORDER_RING, AR_ORDER_RANK, AR_ORDER_TREE, AR_ORDER_HIER = 0, 1, 2, 3
+AR_MAX_RANKS = 64
+AR_MAX_BUCKET_TENSORS = 32
+
+ALGOS = {"ring": AR_RING, "rabenseifner": AR_RABENSEIFNER, "hier": AR_HIER, "fused": AR_FUSED}
+ORDERS = {"ring": AR_ORDER_RING, "rank": AR_ORDER_RANK, "tree": AR_ORDER_TREE, "hier": AR_ORDER_HIER}
+DTYPES = {"f32": AR_F32, "bf16": AR_BF16}
+
+
+class ArError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {ar_status_string(status)}" if what else ar_status_string(status))
+
+
+def _check(status: int, what: str):
+    if status != AR_OK:
+        raise ArError(status, what)
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _ptrs(xs):
+    return _lib.ptr_array([_ptr(x) for x in xs])
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+# ---------------------------------------------------------------- plans
+
+
+class Plan:
+    """An ar_plan_t*; destroyed with the object."""
+
+    def __init__(self, handle: int, desc: dict):
+        self.handle = handle
+        self.desc = desc
+
+    def __del__(self):
+        h, self.handle = getattr(self, "handle", None), None
+        if h:
+            try:
+                _lib.load().ar_plan_destroy(h)
+            except Exception:
+                pass
+
+    @property
+    def stats(self) -> dict:
+        return ar_plan_stats(self)
+
+
+def ar_plan(n_ranks: int, count: int, dtype="f32", algo="fused", group_size: int = 0, order="ring",
+            scale: float = 1.0) -> Plan:
+    """Validate the descriptor and build the schedule (host only)."""
+    d = _lib.ArDesc(int(n_ranks), int(count), DTYPES.get(dtype, dtype), ALGOS.get(algo, algo),
+                    int(group_size), ORDERS.get(order, order), float(scale))
+    h = _lib.c_void_p()
+    _check(_lib.load().ar_plan(d, h), "ar_plan")
+    return Plan(h.value, dict(n_ranks=n_ranks, count=count, dtype=dtype, algo=algo,
+                              group_size=group_size, order=order, scale=scale))
+
+
+def ar_plan_stats(plan: Plan) -> dict:
+    s = _lib.ArStats()
+    _check(_lib.load().ar_plan_stats(plan.handle, s), "ar_plan_stats")
+    return {f: getattr(s, f) for f, _ in _lib.ArStats._fields_}
+
+
+def ar_plan_transfers(plan: Plan, step: int):
+    """(op, [(src, dst, first, end), ...]) of one step of a step plan."""
+    import ctypes
+
+    lib = _lib.load()
+    op, n = _lib.c_int(), _lib.c_int()
+    _check(lib.ar_plan_transfers(plan.handle, step, op, n, None, 0), "ar_plan_transfers")
+    buf = (ctypes.c_int64 * max(1, 4 * n.value))()
+    _check(lib.ar_plan_transfers(plan.handle, step, op, n, buf, n.value), "ar_plan_transfers")
+    rows = [tuple(buf[4 * i: 4 * i + 4]) for i in range(n.value)]
+    return ("reduce" if op.value == 0 else "copy"), rows
+
+
+def ar_execute(plan: Plan, bufs, outs=None, workspace=None, stream=None):
+    """Enqueue the all-reduce of the N device buffers ``bufs`` (in place unless ``outs``)."""
+    o = _ptrs(outs) if outs is not None else None
+    _check(_lib.load().ar_execute(plan.handle, _ptrs(bufs), o, _ptr(workspace), _stream(stream)),
+           "ar_execute")
+
+
+def ar_execute_host(plan: Plan, host_in, host_out, dev_bufs, workspace=None, stream=None):
+    """All-reduce host buffers through device staging buffers; returns when done."""
+    _check(_lib.load().ar_execute_host(plan.handle, _ptrs(host_in), _ptrs(host_out), _ptrs(dev_bufs),
+                                       _ptr(workspace), _stream(stream)), "ar_execute_host")
+
+
+# ---------------------------------------------------------------- buckets
+
+
+def _counts(counts):
+    return (_lib.c_size_t * len(counts))(*[int(c) for c in counts])
+
+
+def ar_bucket_plan(counts, elem_bytes: int, cap_bytes: int):
+    """Returns (bucket_of_tensor list, n_buckets)."""
+    n = len(counts)
+    out = (_lib.c_int * n)()
+    nb = _lib.c_int()
+    _check(_lib.load().ar_bucket_plan(_counts(counts), n, int(elem_bytes), int(cap_bytes), out, nb),
+           "ar_bucket_plan")
+    return list(out), nb.value
+
+
+def _table(tensors):
+    """tensors[r][t] -> flat pointer array [r * n_tensors + t]."""
+    return _lib.ptr_array([_ptr(t) for row in tensors for t in row])
+
+
+def ar_bucket_pack(tensors, counts, t_begin: int, t_end: int, in_dtype, bucket, stream=None):
+    n = len(tensors)
+    _check(_lib.load().ar_bucket_pack(n, _table(tensors), _counts(counts), len(counts), t_begin, t_end,
+                                      DTYPES.get(in_dtype, in_dtype), _ptrs(bucket), _stream(stream)),
+           "ar_bucket_pack")
+
+
+def ar_bucket_unpack(bucket, scale: float, out_dtype, tensors, counts, t_begin: int, t_end: int,
+                     stream=None):
+    n = len(tensors)
+    _check(_lib.load().ar_bucket_unpack(n, _ptrs(bucket), float(scale), DTYPES.get(out_dtype, out_dtype),
+                                        _table(tensors), _counts(counts), len(counts), t_begin, t_end,
+                                        _stream(stream)), "ar_bucket_unpack")
+
+
+def ar_bucket_allreduce(tensors, counts, t_begin: int, t_end: int, dtype, scale: float, stream=None):
+    n = len(tensors)
+    _check(_lib.load().ar_bucket_allreduce(n, _table(tensors), _counts(counts), len(counts), t_begin, t_end,
+                                           DTYPES.get(dtype, dtype), float(scale), _stream(stream)),
+           "ar_bucket_allreduce")
+
+
+# ---------------------------------------------------------------- status
+
+
+def ar_device_status(clear: bool = True) -> int:
+    return _lib.load().ar_device_status(1 if clear else 0)
+
+
+def ar_status_string(status: int) -> str:
+    return _lib.load().ar_status_string(int(status)).decode()
+
+
+def ar_version() -> int:
+    return _lib.load().ar_version()
+
+
+# ---------------------------------------------------------------- convenience
+
+
+def workspace_for(plan: Plan, device=None):
+    """A torch byte tensor of the plan's workspace size (None when it needs none)."""
+    nbytes = plan.stats["workspace_bytes"]
+    if nbytes == 0:
+        return None
+    import torch
+
+    return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")

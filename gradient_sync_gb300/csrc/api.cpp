@@ -1,0 +1,709 @@
+// C ABI of the all-reduce library: descriptor validation, the schedules' step
+// tables (built on the host from the pages' index rules), execution, the
+// bucket calls and the host-memory variant.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "internal.h"
+
+using namespace ar;
+
+namespace {
+
+constexpr int kVersion = 1;
+
+bool is_pow2(int n) { return n > 0 && (n & (n - 1)) == 0; }
+int64_t imod(int64_t a, int64_t n) { return ((a % n) + n) % n; }
+size_t esize(ar_dtype d) { return d == AR_BF16 ? 2 : 4; }
+int64_t rup(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+int64_t rdown(int64_t x, int64_t a) { return x / a * a; }
+
+// Cut [lo, hi) into n parts: part p is [lo + p*len/n, lo + (p+1)*len/n).
+std::vector<int64_t> cuts(int64_t lo, int64_t hi, int n) {
+  std::vector<int64_t> b(n + 1);
+  for (int p = 0; p <= n; ++p) b[p] = lo + (int64_t(p) * (hi - lo)) / n;
+  return b;
+}
+
+void add_xfer(Step& st, int src, int dst, int64_t lo, int64_t hi, Space xs, Space ys, Space ds,
+              bool fin) {
+  if (hi <= lo) return;  // L < N leaves some chunks empty
+  Transfer t;
+  t.src = int16_t(src);
+  t.dst = int16_t(dst);
+  t.xs = xs;
+  t.ys = ys;
+  t.ds = ds;
+  t.fin = fin ? 1 : 0;
+  t.lo = lo;
+  t.hi = hi;
+  st.xfers.push_back(t);
+}
+
+// Ring all-reduce (primer ch. 4, "Collective communication: algorithms, cost
+// and the library that runs them", §4.2 "The ring, one step at a time").
+// Reduce-scatter step s = 0..N-2: rank i sends chunk (i - s) mod N to rank
+// i + 1, which adds its own copy; after N-1 steps rank i owns chunk
+// (i + 1) mod N. All-gather step s: rank i sends complete chunk
+// (i + 1 - s) mod N, which the receiver overwrites.
+void build_ring(ar_plan_t* p) {
+  const int N = p->desc.n_ranks;
+  const int64_t L = int64_t(p->desc.count);
+  const auto b = cuts(0, L, N);
+  for (int s = 0; s <= N - 2; ++s) {
+    Step st{OP_ADD, {}};
+    const bool last = s == N - 2;
+    for (int i = 0; i < N; ++i) {
+      const int c = int(imod(i - s, N));
+      add_xfer(st, i, (i + 1) % N, b[c], b[c + 1], s == 0 ? RAW : PART, RAW, last ? RES : PART, last);
+    }
+    p->steps.push_back(st);
+  }
+  for (int s = 0; s <= N - 2; ++s) {
+    Step st{OP_COPY, {}};
+    for (int i = 0; i < N; ++i) {
+      const int c = int(imod(i + 1 - s, N));
+      add_xfer(st, i, (i + 1) % N, b[c], b[c + 1], RES, RES, RES, false);
+    }
+    p->steps.push_back(st);
+  }
+}
+
+// Rabenseifner: recursive halving reduce-scatter, recursive doubling
+// all-gather (primer §4.3, Fig. 4.5 and Animation 4.2). Step k = 1..log2 N:
+// rank i pairs with i xor 2^(k-1), keeps the lower half of its chunk range if
+// bit k-1 of i is 0 (else the upper half), sends the other half and adds
+// what arrives; the all-gather runs the pairs in reverse order and copies.
+void build_rabenseifner(ar_plan_t* p) {
+  const int N = p->desc.n_ranks;
+  const int64_t L = int64_t(p->desc.count);
+  const auto b = cuts(0, L, N);
+  int K = 0;
+  while ((1 << K) < N) ++K;
+  std::vector<std::pair<int, int>> rng(N, {0, N});
+  for (int k = 1; k <= K; ++k) {
+    const int d = 1 << (k - 1);
+    Step st{OP_ADD, {}};
+    std::vector<std::pair<int, int>> next(rng);
+    for (int i = 0; i < N; ++i) {
+      const int lo = rng[i].first, hi = rng[i].second, mid = (lo + hi) / 2;
+      const bool lower = ((i >> (k - 1)) & 1) == 0;
+      const std::pair<int, int> keep = lower ? std::make_pair(lo, mid) : std::make_pair(mid, hi);
+      const std::pair<int, int> send = lower ? std::make_pair(mid, hi) : std::make_pair(lo, mid);
+      next[i] = keep;
+      // partner i^d keeps exactly the half that i sends
+      add_xfer(st, i, i ^ d, b[send.first], b[send.second], k == 1 ? RAW : PART, k == 1 ? RAW : PART,
+               k == K ? RES : PART, k == K);
+    }
+    rng = next;
+    p->steps.push_back(st);
+  }
+  for (int k = K; k >= 1; --k) {
+    const int d = 1 << (k - 1);
+    Step st{OP_COPY, {}};
+    for (int i = 0; i < N; ++i) add_xfer(st, i, i ^ d, b[rng[i].first], b[rng[i].second], RES, RES, RES, false);
+    std::vector<std::pair<int, int>> next(rng);
+    for (int i = 0; i < N; ++i)
+      next[i] = {std::min(rng[i].first, rng[i ^ d].first), std::max(rng[i].second, rng[i ^ d].second)};
+    rng = next;
+    p->steps.push_back(st);
+  }
+}
+
+// Hierarchical all-reduce over M = N/G groups of G consecutive ranks (primer
+// §4.4, Fig. 4.8 and Animation 4.3; AI Infra Book ch. 7, §7.2.1):
+// (1) ring reduce-scatter inside each group, local rank l sending slice
+//     (l - 1 - s) mod G, so that local rank k owns slice k;
+// (2) for each slice k, a ring all-reduce among local rank k of every group,
+//     over slice k cut into M sub-chunks;
+// (3) ring all-gather inside each group, local rank l sending slice (l - s).
+void build_hier(ar_plan_t* p) {
+  const int N = p->desc.n_ranks, G = p->desc.group_size, M = N / G;
+  const int64_t L = int64_t(p->desc.count);
+  const auto sb = cuts(0, L, G);
+  for (int s = 0; s <= G - 2; ++s) {  // phase 1
+    Step st{OP_ADD, {}};
+    const bool fin = (M == 1) && s == G - 2;
+    for (int g = 0; g < M; ++g)
+      for (int l = 0; l < G; ++l) {
+        const int c = int(imod(l - 1 - s, G));
+        add_xfer(st, g * G + l, g * G + (l + 1) % G, sb[c], sb[c + 1], s == 0 ? RAW : PART, RAW,
+                 fin ? RES : PART, fin);
+      }
+    p->steps.push_back(st);
+  }
+  if (M > 1) {  // phase 2
+    const Space own = G > 1 ? PART : RAW;
+    for (int s = 0; s <= M - 2; ++s) {
+      Step st{OP_ADD, {}};
+      const bool fin = s == M - 2;
+      for (int k = 0; k < G; ++k) {
+        const auto sub = cuts(sb[k], sb[k + 1], M);
+        for (int m = 0; m < M; ++m) {
+          const int j = int(imod(m - s, M));
+          add_xfer(st, m * G + k, ((m + 1) % M) * G + k, sub[j], sub[j + 1], s == 0 ? own : PART, own,
+                   fin ? RES : PART, fin);
+        }
+      }
+      p->steps.push_back(st);
+    }
+    for (int s = 0; s <= M - 2; ++s) {
+      Step st{OP_COPY, {}};
+      for (int k = 0; k < G; ++k) {
+        const auto sub = cuts(sb[k], sb[k + 1], M);
+        for (int m = 0; m < M; ++m) {
+          const int j = int(imod(m + 1 - s, M));
+          add_xfer(st, m * G + k, ((m + 1) % M) * G + k, sub[j], sub[j + 1], RES, RES, RES, false);
+        }
+      }
+      p->steps.push_back(st);
+    }
+  }
+  for (int s = 0; s <= G - 2; ++s) {  // phase 3
+    Step st{OP_COPY, {}};
+    for (int g = 0; g < M; ++g)
+      for (int l = 0; l < G; ++l) {
+        const int c = int(imod(l - s, G));
+        add_xfer(st, g * G + l, g * G + (l + 1) % G, sb[c], sb[c + 1], RES, RES, RES, false);
+      }
+    p->steps.push_back(st);
+  }
+}
+
+size_t space_bytes(Space s, ar_dtype d) { return s == PART ? 4 : esize(d); }
+
+void compute_stats(ar_plan_t* p) {
+  const ar_desc& d = p->desc;
+  const int N = d.n_ranks;
+  const int64_t L = int64_t(d.count);
+  ar_stats& st = p->stats;
+  st = ar_stats{};
+  p->ws_stride = rup(std::max<int64_t>(L, 1), 64);
+  if (d.algo == AR_FUSED) {
+    st.steps = N > 1 ? 1 : 0;
+    st.launches = (L > 0 && N > 1) ? 1 : 0;
+    st.bytes_sent_per_rank = N > 1 ? size_t(L) * esize(d.dtype) : 0;
+    st.hbm_bytes = N > 1 ? 2 * size_t(N) * size_t(L) * esize(d.dtype) : 0;
+    st.workspace_bytes = 0;
+    return;
+  }
+  st.steps = int(p->steps.size());
+  std::vector<size_t> sent(N, 0);
+  for (const Step& s : p->steps) {
+    if (!s.xfers.empty()) st.launches += 1;
+    for (const Transfer& t : s.xfers) {
+      const size_t len = size_t(t.hi - t.lo);
+      if (s.op == OP_ADD) {
+        sent[t.src] += len * space_bytes(Space(t.xs), d.dtype);
+        st.hbm_bytes += len * (space_bytes(Space(t.xs), d.dtype) + space_bytes(Space(t.ys), d.dtype) +
+                               space_bytes(Space(t.ds), d.dtype));
+      } else {
+        sent[t.src] += len * esize(d.dtype);
+        st.hbm_bytes += len * 2 * esize(d.dtype);
+      }
+    }
+  }
+  st.bytes_sent_per_rank = N > 0 ? *std::max_element(sent.begin(), sent.end()) : 0;
+  const bool uses_ws = d.dtype == AR_BF16 && N > 1;
+  st.workspace_bytes = uses_ws ? size_t(N) * size_t(p->ws_stride) * 4 : 0;
+}
+
+ar_status check_ptr(const void* ptr) {
+  if (ptr == nullptr) return AR_EINVAL;
+  if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return AR_EINVAL;
+  return AR_OK;
+}
+
+// Every [start, start + bytes) must be disjoint from the others.
+bool disjoint(std::vector<std::pair<uintptr_t, uintptr_t>> iv) {
+  std::sort(iv.begin(), iv.end());
+  for (size_t i = 1; i < iv.size(); ++i)
+    if (iv[i].first < iv[i - 1].second) return false;
+  return true;
+}
+
+ar_status check_buffers(const ar_plan_t* p, void* const* bufs, void* const* outs, void* workspace) {
+  if (bufs == nullptr) return AR_EINVAL;
+  const int N = p->desc.n_ranks;
+  const size_t bytes = p->desc.count * esize(p->desc.dtype);
+  std::vector<std::pair<uintptr_t, uintptr_t>> iv;
+  for (int r = 0; r < N; ++r) {
+    if (check_ptr(bufs[r]) != AR_OK) return AR_EINVAL;
+    iv.push_back({uintptr_t(bufs[r]), uintptr_t(bufs[r]) + bytes});
+    if (outs != nullptr) {
+      if (check_ptr(outs[r]) != AR_OK) return AR_EINVAL;
+      if (outs[r] != bufs[r]) iv.push_back({uintptr_t(outs[r]), uintptr_t(outs[r]) + bytes});
+    }
+  }
+  if (p->stats.workspace_bytes > 0) {
+    if (check_ptr(workspace) != AR_OK) return AR_EINVAL;
+    iv.push_back({uintptr_t(workspace), uintptr_t(workspace) + p->stats.workspace_bytes});
+  }
+  if (bytes > 0 && !disjoint(iv)) return AR_EINVAL;
+  return AR_OK;
+}
+
+ar_status from_cuda(cudaError_t e) { return e == cudaSuccess ? AR_OK : AR_ECUDA; }
+
+// Segment count and tiles per segment of a fused launch over [e_lo, e_hi).
+void fused_tiling(const ar_desc& d, FusedParams& fp) {
+  const int N = d.n_ranks;
+  const int64_t L = int64_t(d.count);
+  std::vector<std::pair<int64_t, int64_t>> segs;
+  if (d.order == AR_ORDER_RING) {
+    const auto b = cuts(0, L, N);
+    for (int c = 0; c < N; ++c) segs.push_back({b[c], b[c + 1]});
+  } else if (d.order == AR_ORDER_HIER) {
+    const int G = d.group_size, M = N / G;
+    const auto sb = cuts(0, L, G);
+    for (int k = 0; k < G; ++k) {
+      const auto sub = cuts(sb[k], sb[k + 1], M);
+      for (int j = 0; j < M; ++j) segs.push_back({sub[j], sub[j + 1]});
+    }
+  } else {
+    segs.push_back({0, L});
+  }
+  const int64_t W = d.dtype == AR_BF16 ? 8 : 4;
+  const int64_t tile = fused_tile_elems(d.dtype);
+  int64_t tps = 1;
+  for (auto& s : segs) {
+    const int64_t lo = std::max(s.first, fp.e_lo), hi = std::min(s.second, fp.e_hi);
+    if (hi <= lo) continue;
+    const int64_t body = std::max<int64_t>(rdown(hi, W) - rup(lo, W), 0);
+    tps = std::max(tps, (body + tile - 1) / tile);
+  }
+  fp.n_seg = int(segs.size());
+  fp.tiles_per_seg = tps;
+}
+
+ar_status execute_fused(const ar_plan_t* p, void* const* bufs, void* const* outs, int64_t e_lo,
+                        int64_t e_hi, cudaStream_t stream) {
+  const ar_desc& d = p->desc;
+  FusedParams fp;
+  std::memset(&fp, 0, sizeof(fp));
+  for (int r = 0; r < d.n_ranks; ++r) {
+    fp.in[r] = bufs[r];
+    fp.out[r] = outs ? outs[r] : bufs[r];
+  }
+  fp.n = d.n_ranks;
+  fp.order = d.n_ranks == 1 ? AR_ORDER_RANK : d.order;
+  fp.g = d.order == AR_ORDER_HIER ? d.group_size : d.n_ranks;
+  fp.m = d.order == AR_ORDER_HIER ? d.n_ranks / d.group_size : 1;
+  fp.count = int64_t(d.count);
+  fp.e_lo = e_lo;
+  fp.e_hi = e_hi;
+  fp.scale = d.scale;
+  fused_tiling(d, fp);
+  return from_cuda(launch_fused(fp, d.dtype, stream));
+}
+
+ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs, void* workspace,
+                        cudaStream_t stream) {
+  const ar_desc& d = p->desc;
+  const int N = d.n_ranks;
+  static thread_local StepParams sp;  // ~3 KB, reused between calls
+  std::memset(&sp, 0, sizeof(sp));
+  for (int r = 0; r < N; ++r) {
+    sp.raw[r] = bufs[r];
+    sp.res[r] = outs ? outs[r] : bufs[r];
+  }
+  sp.ws = static_cast<float*>(workspace);
+  sp.ws_stride = p->ws_stride;
+  sp.scale = d.scale;
+  if (N == 1) {
+    const bool in_place = outs == nullptr || outs[0] == bufs[0];
+    if (in_place && d.scale == 1.0f) return AR_OK;
+    sp.n_xfer = 1;
+    sp.x[0] = Transfer{0, 0, RAW, RAW, RES, 1, 0, int64_t(d.count)};
+    sp.tile_start[0] = 0;
+    const int64_t body = std::max<int64_t>(rdown(d.count, kStepVec), 0);
+    sp.tile_start[1] = int32_t(std::max<int64_t>(1, (body + kStepTile - 1) / kStepTile));
+    return from_cuda(launch_step(sp, d.dtype, OP_FINISH, sp.tile_start[1], false, stream));
+  }
+  bool first = true;
+  for (const Step& st : p->steps) {
+    if (st.xfers.empty()) continue;
+    sp.n_xfer = int(st.xfers.size());
+    int tiles = 0;
+    for (int x = 0; x < sp.n_xfer; ++x) {
+      const Transfer& t = st.xfers[x];
+      sp.x[x] = t;
+      sp.tile_start[x] = tiles;
+      const int64_t body = std::max<int64_t>(rdown(t.hi, kStepVec) - rup(t.lo, kStepVec), 0);
+      tiles += int(std::max<int64_t>(1, (body + kStepTile - 1) / kStepTile));
+    }
+    sp.tile_start[sp.n_xfer] = tiles;
+    const ar_status s = from_cuda(launch_step(sp, d.dtype, st.op, tiles, !first, stream));
+    if (s != AR_OK) return s;
+    first = false;
+  }
+  return AR_OK;
+}
+
+// Internal streams and events of ar_execute_host, one set per device.
+struct HostPipe {
+  int device = -1;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  std::vector<cudaEvent_t> ev;
+};
+std::mutex g_host_mu;
+std::vector<HostPipe> g_pipes;
+
+ar_status host_pipe(HostPipe** out, size_t n_events) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return AR_ECUDA;
+  HostPipe* hp = nullptr;
+  for (auto& x : g_pipes)
+    if (x.device == dev) hp = &x;
+  if (hp == nullptr) {
+    g_pipes.push_back(HostPipe{});
+    hp = &g_pipes.back();
+    hp->device = dev;
+    if (cudaStreamCreateWithFlags(&hp->h2d, cudaStreamNonBlocking) != cudaSuccess) return AR_ECUDA;
+    if (cudaStreamCreateWithFlags(&hp->d2h, cudaStreamNonBlocking) != cudaSuccess) return AR_ECUDA;
+  }
+  while (hp->ev.size() < n_events) {
+    cudaEvent_t e;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return AR_ECUDA;
+    hp->ev.push_back(e);
+  }
+  *out = hp;
+  return AR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ar_status ar_plan(const ar_desc* desc, ar_plan_t** out) {
+  if (desc == nullptr || out == nullptr) return AR_EINVAL;
+  *out = nullptr;
+  const ar_desc& d = *desc;
+  const int N = d.n_ranks;
+  if (N < 1 || N > AR_MAX_RANKS) return AR_EINVAL;
+  if (d.dtype != AR_F32 && d.dtype != AR_BF16) return AR_EINVAL;
+  if (d.algo < AR_RING || d.algo > AR_FUSED) return AR_EINVAL;
+  if (!std::isfinite(d.scale)) return AR_EINVAL;
+  if (d.count > (size_t(1) << 40)) return AR_EINVAL;
+  if (d.algo == AR_RABENSEIFNER && !is_pow2(N)) return AR_EINVAL;
+  if (d.algo == AR_HIER && (d.group_size < 1 || N % d.group_size != 0)) return AR_EINVAL;
+  if (d.algo == AR_FUSED) {
+    if (d.order < AR_ORDER_RING || d.order > AR_ORDER_HIER) return AR_EINVAL;
+    if (d.order == AR_ORDER_TREE && !is_pow2(N)) return AR_EINVAL;
+    if (d.order == AR_ORDER_HIER && (d.group_size < 1 || N % d.group_size != 0)) return AR_EINVAL;
+  }
+  ar_plan_t* p = new (std::nothrow) ar_plan_t;
+  if (p == nullptr) return AR_ENOMEM;
+  try {
+    p->desc = d;
+    if (d.algo != AR_HIER && !(d.algo == AR_FUSED && d.order == AR_ORDER_HIER)) p->desc.group_size = 0;
+    if (N > 1) {
+      if (d.algo == AR_RING) build_ring(p);
+      if (d.algo == AR_RABENSEIFNER) build_rabenseifner(p);
+      if (d.algo == AR_HIER) build_hier(p);
+    }
+    compute_stats(p);
+  } catch (const std::bad_alloc&) {
+    delete p;
+    return AR_ENOMEM;
+  }
+  *out = p;
+  return AR_OK;
+}
+
+ar_status ar_plan_stats(const ar_plan_t* plan, ar_stats* stats) {
+  if (plan == nullptr || stats == nullptr) return AR_EINVAL;
+  *stats = plan->stats;
+  return AR_OK;
+}
+
+ar_status ar_plan_desc(const ar_plan_t* plan, ar_desc* desc) {
+  if (plan == nullptr || desc == nullptr) return AR_EINVAL;
+  *desc = plan->desc;
+  return AR_OK;
+}
+
+void ar_plan_destroy(ar_plan_t* plan) { delete plan; }
+
+ar_status ar_plan_transfers(const ar_plan_t* plan, int step, int* op, int* n_xfers, int64_t* xfers,
+                            int max_xfers) {
+  if (plan == nullptr || op == nullptr || n_xfers == nullptr) return AR_EINVAL;
+  if (plan->desc.algo == AR_FUSED || step < 0 || step >= int(plan->steps.size())) return AR_EINVAL;
+  const Step& st = plan->steps[size_t(step)];
+  *op = st.op == OP_ADD ? 0 : 1;
+  *n_xfers = int(st.xfers.size());
+  if (xfers != nullptr)
+    for (int i = 0; i < *n_xfers && i < max_xfers; ++i) {
+      const Transfer& t = st.xfers[size_t(i)];
+      xfers[4 * i + 0] = t.src;
+      xfers[4 * i + 1] = t.dst;
+      xfers[4 * i + 2] = t.lo;
+      xfers[4 * i + 3] = t.hi;
+    }
+  return AR_OK;
+}
+
+ar_status ar_execute(const ar_plan_t* plan, void* const* bufs, void* const* outs, void* workspace,
+                     void* stream) {
+  if (plan == nullptr) return AR_EINVAL;
+  const ar_status s = check_buffers(plan, bufs, outs, workspace);
+  if (s != AR_OK) return s;
+  if (plan->desc.count == 0) return AR_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (plan->desc.algo == AR_FUSED)
+    return execute_fused(plan, bufs, outs, 0, int64_t(plan->desc.count), st);
+  return execute_steps(plan, bufs, outs, workspace, st);
+}
+
+ar_status ar_execute_host(const ar_plan_t* plan, const void* const* host_in, void* const* host_out,
+                          void* const* dev_bufs, void* workspace, void* stream) {
+  if (plan == nullptr || host_in == nullptr || host_out == nullptr) return AR_EINVAL;
+  const ar_status s = check_buffers(plan, dev_bufs, nullptr, workspace);
+  if (s != AR_OK) return s;
+  const int N = plan->desc.n_ranks;
+  for (int r = 0; r < N; ++r)
+    if (host_in[r] == nullptr || host_out[r] == nullptr) return AR_EINVAL;
+  const int64_t L = int64_t(plan->desc.count);
+  if (L == 0) return AR_OK;
+  const size_t es = esize(plan->desc.dtype);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_host_mu);
+
+  if (plan->desc.algo != AR_FUSED) {  // the schedule spans the whole buffer: copy, run, copy
+    for (int r = 0; r < N; ++r)
+      if (cudaMemcpyAsync(dev_bufs[r], host_in[r], size_t(L) * es, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return AR_ECUDA;
+    const ar_status e = ar_execute(plan, dev_bufs, nullptr, workspace, stream);
+    if (e != AR_OK) return e;
+    for (int r = 0; r < N; ++r)
+      if (cudaMemcpyAsync(host_out[r], dev_bufs[r], size_t(L) * es, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return AR_ECUDA;
+    return from_cuda(cudaStreamSynchronize(st));
+  }
+
+  // Fused: elements are independent, so the buffers are cut into slabs of
+  // whole 16-byte vectors; slab k's host-to-device copies, its reduction and
+  // its device-to-host copies run on three streams, overlapping the copies of
+  // neighbouring slabs in both directions with the reduction.
+  const int64_t target = std::max<int64_t>(int64_t(64) << 20, 0) / int64_t(es) / N;  // ~64 MiB per slab
+  const int64_t slab = std::max<int64_t>(rup(std::min<int64_t>(target, L), 64), 64);
+  const int64_t n_slabs = (L + slab - 1) / slab;
+  HostPipe* hp = nullptr;
+  ar_status e = host_pipe(&hp, size_t(2 * n_slabs + 1));
+  if (e != AR_OK) return e;
+  // copies must not start before earlier work on the caller's stream
+  cudaEvent_t start = hp->ev[2 * n_slabs];
+  if (cudaEventRecord(start, st) != cudaSuccess) return AR_ECUDA;
+  if (cudaStreamWaitEvent(hp->h2d, start, 0) != cudaSuccess) return AR_ECUDA;
+  for (int64_t k = 0; k < n_slabs; ++k) {
+    const int64_t lo = k * slab, hi = std::min(L, lo + slab);
+    for (int r = 0; r < N; ++r)
+      if (cudaMemcpyAsync(static_cast<char*>(dev_bufs[r]) + lo * es,
+                          static_cast<const char*>(host_in[r]) + lo * es, size_t(hi - lo) * es,
+                          cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess)
+        return AR_ECUDA;
+    cudaEvent_t copied = hp->ev[2 * k], reduced = hp->ev[2 * k + 1];
+    if (cudaEventRecord(copied, hp->h2d) != cudaSuccess) return AR_ECUDA;
+    if (cudaStreamWaitEvent(st, copied, 0) != cudaSuccess) return AR_ECUDA;
+    e = execute_fused(plan, dev_bufs, nullptr, lo, hi, st);
+    if (e != AR_OK) return e;
+    if (cudaEventRecord(reduced, st) != cudaSuccess) return AR_ECUDA;
+    if (cudaStreamWaitEvent(hp->d2h, reduced, 0) != cudaSuccess) return AR_ECUDA;
+    for (int r = 0; r < N; ++r)
+      if (cudaMemcpyAsync(static_cast<char*>(host_out[r]) + lo * es,
+                          static_cast<const char*>(dev_bufs[r]) + lo * es, size_t(hi - lo) * es,
+                          cudaMemcpyDeviceToHost, hp->d2h) != cudaSuccess)
+        return AR_ECUDA;
+  }
+  return from_cuda(cudaStreamSynchronize(hp->d2h));
+}
+
+// ---------------------------------------------------------------- buckets
+
+ar_status ar_bucket_plan(const size_t* counts, int n_tensors, size_t elem_bytes, size_t cap_bytes,
+                         int* bucket_of_tensor, int* n_buckets) {
+  if (counts == nullptr || bucket_of_tensor == nullptr || n_buckets == nullptr) return AR_EINVAL;
+  if (n_tensors < 1 || elem_bytes == 0) return AR_EINVAL;
+  int b = 0;
+  size_t cur = 0;
+  bool open = false;
+  for (int t = n_tensors - 1; t >= 0; --t) {  // backward produces the last tensor first
+    const size_t bytes = counts[t] * elem_bytes;
+    if (open && cur + bytes > cap_bytes) {
+      ++b;
+      cur = 0;
+    }
+    bucket_of_tensor[t] = b;
+    cur += bytes;
+    open = true;
+  }
+  *n_buckets = b + 1;
+  return AR_OK;
+}
+
+namespace {
+
+ar_status check_bucket_args(int n_ranks, const void* const* tensors, const size_t* counts, int n_tensors,
+                            int t_begin, int t_end) {
+  if (n_ranks < 1 || n_ranks > AR_MAX_RANKS) return AR_EINVAL;
+  if (tensors == nullptr || counts == nullptr) return AR_EINVAL;
+  if (n_tensors < 1 || t_begin < 0 || t_end > n_tensors || t_begin >= t_end) return AR_EINVAL;
+  for (int t = t_begin; t < t_end; ++t)
+    for (int r = 0; r < n_ranks; ++r)
+      if (check_ptr(tensors[size_t(r) * n_tensors + t]) != AR_OK) return AR_EINVAL;
+  return AR_OK;
+}
+
+// Packed offset of each tensor of bucket [t_begin, t_end): descending ids.
+std::vector<int64_t> packed_offsets(const size_t* counts, int t_begin, int t_end) {
+  std::vector<int64_t> off(t_end - t_begin);
+  int64_t o = 0;
+  for (int t = t_end - 1; t >= t_begin; --t) {
+    off[t - t_begin] = o;
+    o += int64_t(counts[t]);
+  }
+  return off;
+}
+
+ar_status run_pack(int n_ranks, const void* const* tensors, const size_t* counts, int n_tensors,
+                   int t_begin, int t_end, ar_dtype dtype, void* const* bucket, float scale, bool unpack,
+                   cudaStream_t stream) {
+  const auto off = packed_offsets(counts, t_begin, t_end);
+  const int max_group = std::min(AR_MAX_BUCKET_TENSORS, kMaxBucketPtrs / n_ranks);
+  static thread_local PackParams pp;
+  for (int g0 = t_end - 1; g0 >= t_begin; g0 -= max_group) {  // groups of tensors, packing order
+    std::memset(&pp, 0, sizeof(pp));
+    pp.n = n_ranks;
+    pp.scale = scale;
+    int nt = 0, tiles = 0;
+    for (int t = g0; t >= t_begin && nt < max_group; --t, ++nt) {
+      for (int r = 0; r < n_ranks; ++r) pp.tptr[nt * n_ranks + r] = const_cast<void*>(tensors[size_t(r) * n_tensors + t]);
+      pp.off[nt] = off[t - t_begin];
+      pp.cnt[nt] = int64_t(counts[t]);
+      pp.tile_start[nt] = tiles;
+      tiles += int((int64_t(counts[t]) + kPackTile - 1) / kPackTile);
+    }
+    pp.n_t = nt;
+    pp.tile_start[nt] = tiles;
+    for (int r = 0; r < n_ranks; ++r) pp.bucket[r] = bucket[r];
+    if (launch_pack(pp, dtype, unpack, stream) != cudaSuccess) return AR_ECUDA;
+  }
+  return AR_OK;
+}
+
+}  // namespace
+
+ar_status ar_bucket_pack(int n_ranks, const void* const* tensors, const size_t* counts, int n_tensors,
+                         int t_begin, int t_end, ar_dtype in_dtype, void* const* bucket, void* stream) {
+  ar_status s = check_bucket_args(n_ranks, tensors, counts, n_tensors, t_begin, t_end);
+  if (s != AR_OK) return s;
+  if (in_dtype != AR_F32 && in_dtype != AR_BF16) return AR_EINVAL;
+  if (bucket == nullptr) return AR_EINVAL;
+  for (int r = 0; r < n_ranks; ++r)
+    if (check_ptr(bucket[r]) != AR_OK) return AR_EINVAL;
+  return run_pack(n_ranks, tensors, counts, n_tensors, t_begin, t_end, in_dtype, bucket, 1.0f, false,
+                  static_cast<cudaStream_t>(stream));
+}
+
+ar_status ar_bucket_unpack(int n_ranks, const void* const* bucket, float scale, ar_dtype out_dtype,
+                           void* const* tensors, const size_t* counts, int n_tensors, int t_begin, int t_end,
+                           void* stream) {
+  ar_status s = check_bucket_args(n_ranks, tensors, counts, n_tensors, t_begin, t_end);
+  if (s != AR_OK) return s;
+  if (out_dtype != AR_F32 && out_dtype != AR_BF16) return AR_EINVAL;
+  if (bucket == nullptr || !std::isfinite(scale)) return AR_EINVAL;
+  for (int r = 0; r < n_ranks; ++r)
+    if (check_ptr(bucket[r]) != AR_OK) return AR_EINVAL;
+  return run_pack(n_ranks, tensors, counts, n_tensors, t_begin, t_end, out_dtype,
+                  const_cast<void* const*>(bucket), scale, true, static_cast<cudaStream_t>(stream));
+}
+
+ar_status ar_bucket_allreduce(int n_ranks, void* const* tensors, const size_t* counts, int n_tensors,
+                              int t_begin, int t_end, ar_dtype dtype, float scale, void* stream) {
+  ar_status s = check_bucket_args(n_ranks, tensors, counts, n_tensors, t_begin, t_end);
+  if (s != AR_OK) return s;
+  if (dtype != AR_F32 && dtype != AR_BF16) return AR_EINVAL;
+  if (!std::isfinite(scale)) return AR_EINVAL;
+  const int N = n_ranks;
+  const auto off = packed_offsets(counts, t_begin, t_end);
+  int64_t Lb = 0;
+  for (int t = t_begin; t < t_end; ++t) Lb += int64_t(counts[t]);
+  if (Lb == 0) return AR_OK;
+  const auto b = cuts(0, Lb, N);
+  const int64_t W = dtype == AR_BF16 ? 8 : 4;
+  const int64_t tile = fused_tile_elems(dtype);
+  const int max_group = std::min(AR_MAX_BUCKET_TENSORS, kMaxBucketPtrs / N);
+  static thread_local BucketFusedParams bp;
+  std::memset(&bp, 0, sizeof(bp));
+  int nt = 0, tiles = 0;
+  auto flush = [&]() -> ar_status {
+    if (bp.n_seg == 0) {
+      nt = 0;
+      return AR_OK;
+    }
+    bp.n = N;
+    bp.scale = scale;
+    bp.tile_start[bp.n_seg] = tiles;
+    const cudaError_t e = launch_bucket_fused(bp, dtype, static_cast<cudaStream_t>(stream));
+    std::memset(&bp, 0, sizeof(bp));
+    nt = 0;
+    tiles = 0;
+    return from_cuda(e);
+  };
+  for (int t = t_end - 1; t >= t_begin; --t) {  // packing order
+    const int64_t o = off[t - t_begin], n_el = int64_t(counts[t]);
+    if (n_el == 0) continue;
+    // the ring's chunks that overlap this tensor's packed range
+    int n_pieces = 0;
+    for (int c = 0; c < N; ++c)
+      if (std::max(b[c], o) < std::min(b[c + 1], o + n_el)) ++n_pieces;
+    if (nt == max_group || bp.n_seg + n_pieces > kMaxBucketSegs) {
+      s = flush();
+      if (s != AR_OK) return s;
+    }
+    for (int r = 0; r < N; ++r) bp.ptr[nt * N + r] = tensors[size_t(r) * n_tensors + t];
+    for (int c = 0; c < N; ++c) {
+      const int64_t lo = std::max(b[c], o), hi = std::min(b[c + 1], o + n_el);
+      if (lo >= hi) continue;
+      BucketSeg& sg = bp.seg[bp.n_seg];
+      sg.t = nt;
+      sg.rot = c;
+      sg.lo = lo - o;
+      sg.hi = hi - o;
+      bp.tile_start[bp.n_seg] = tiles;
+      const int64_t body = std::max<int64_t>(rdown(sg.hi, W) - rup(sg.lo, W), 0);
+      tiles += int(std::max<int64_t>(1, (body + tile - 1) / tile));
+      ++bp.n_seg;
+    }
+    ++nt;
+  }
+  return flush();
+}
+
+// ---------------------------------------------------------------- status
+
+ar_status ar_device_status(int clear) {
+  unsigned int v = 0;
+  if (read_device_status(&v, clear != 0) != cudaSuccess) return AR_ECUDA;
+  return v != 0 ? AR_ETIMEOUT : AR_OK;
+}
+
+const char* ar_status_string(ar_status status) {
+  switch (status) {
+    case AR_OK: return "AR_OK: success";
+    case AR_EINVAL: return "AR_EINVAL: invalid argument";
+    case AR_EUNSUPPORTED: return "AR_EUNSUPPORTED: not supported by this build";
+    case AR_ENOMEM: return "AR_ENOMEM: host allocation failed";
+    case AR_ECUDA: return "AR_ECUDA: CUDA runtime error";
+    case AR_ETIMEOUT: return "AR_ETIMEOUT: a device-side wait ran out of time";
+  }
+  return "unknown ar_status";
+}
+
+int ar_version(void) { return kVersion; }
+
+}  // extern "C"

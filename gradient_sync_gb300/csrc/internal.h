@@ -1,0 +1,121 @@
+// Internal declarations shared by the host planner (api.cpp) and the CUDA
+// launchers (*.cu). Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "../../include/ar.h"
+
+namespace ar {
+
+// Where a step operand lives. RAW: the rank's input buffer (input dtype).
+// PART: the rank's fp32 partial sums (fp32 runs: the output buffer itself;
+// bf16 runs: the workspace). RES: the rank's output buffer (output dtype).
+enum Space : uint8_t { RAW = 0, PART = 1, RES = 2 };
+
+enum StepOp : int { OP_ADD = 0, OP_COPY = 1, OP_FINISH = 2 };
+
+// One send/receive of a step: rank `dst` receives elements [lo, hi) from
+// rank `src`. ADD: dst_space[dst] = X[src] + Y[dst] (final: times scale,
+// rounded to the output type, written to RES). COPY: RES[dst] = RES[src].
+// FINISH (one rank): RES[dst] = scale * X[src], rounded to the output type.
+struct Transfer {
+  int16_t src, dst;
+  uint8_t xs, ys, ds, fin;
+  int64_t lo, hi;
+};
+
+struct Step {
+  StepOp op;
+  std::vector<Transfer> xfers;
+};
+
+}  // namespace ar
+
+struct ar_plan {
+  ar_desc desc;
+  std::vector<ar::Step> steps;  // empty for AR_FUSED
+  ar_stats stats;
+  int64_t ws_stride;  // fp32 elements per rank in the workspace (multiple of 64)
+};
+
+namespace ar {
+
+constexpr int kMaxXfers = AR_MAX_RANKS;
+
+// ---- kernel launch parameter blocks (passed by value, < 4 KB each) ----
+
+struct StepParams {
+  void* raw[AR_MAX_RANKS];
+  void* res[AR_MAX_RANKS];
+  float* ws;
+  int64_t ws_stride;
+  float scale;
+  int n_xfer;
+  Transfer x[kMaxXfers];
+  int32_t tile_start[kMaxXfers + 1];  // prefix sums of tiles per transfer
+};
+
+struct FusedParams {
+  const void* in[AR_MAX_RANKS];
+  void* out[AR_MAX_RANKS];
+  int n;            // ranks
+  int order;        // ar_order
+  int g, m;         // hierarchical group size and group count
+  int n_seg;        // segments of constant summation order
+  int64_t count;    // elements per rank
+  int64_t e_lo, e_hi;  // element range processed by this launch
+  int64_t tiles_per_seg;
+  float scale;
+};
+
+constexpr int kMaxBucketPtrs = 256;  // n_ranks * tensors per launch
+constexpr int kMaxBucketSegs = 96;
+
+struct BucketSeg {
+  int32_t t;      // tensor slot in the launch's pointer table
+  int32_t rot;    // ring order: first rank of the fold (the chunk index)
+  int64_t lo, hi; // element range inside the tensor
+};
+
+struct BucketFusedParams {
+  void* ptr[kMaxBucketPtrs];  // ptr[t * n + r]: rank r's tensor t
+  int n;
+  int n_seg;
+  float scale;
+  BucketSeg seg[kMaxBucketSegs];
+  int32_t tile_start[kMaxBucketSegs + 1];
+};
+
+struct PackParams {
+  void* tptr[kMaxBucketPtrs];  // tptr[t * n + r]
+  void* bucket[AR_MAX_RANKS];
+  int n;
+  int n_t;
+  float scale;
+  int64_t off[AR_MAX_BUCKET_TENSORS];   // packed offset of each tensor
+  int64_t cnt[AR_MAX_BUCKET_TENSORS];
+  int32_t tile_start[AR_MAX_BUCKET_TENSORS + 1];  // tiles per tensor (one rank)
+};
+
+// ---- launchers (defined in the .cu files) ----
+// Tile sizes the launchers and the host planner agree on (elements).
+constexpr int kThreads = 256;
+constexpr int kStepVec = 8;                               // elements per vector in step kernels
+constexpr int kStepUnroll = 2;
+constexpr int64_t kStepTile = kThreads * kStepVec * kStepUnroll;  // 4096
+constexpr int kPackTile = kThreads * 8;                   // 2048 elements
+
+cudaError_t launch_step(const StepParams& p, ar_dtype dtype, StepOp op, int total_tiles, bool pdl,
+                        cudaStream_t stream);
+cudaError_t launch_fused(const FusedParams& p, ar_dtype dtype, cudaStream_t stream);
+int64_t fused_tile_elems(ar_dtype dtype);
+cudaError_t launch_bucket_fused(const BucketFusedParams& p, ar_dtype dtype, cudaStream_t stream);
+cudaError_t launch_pack(const PackParams& p, ar_dtype dtype, bool unpack, cudaStream_t stream);
+cudaError_t read_device_status(unsigned int* value, bool clear);
+
+}  // namespace ar

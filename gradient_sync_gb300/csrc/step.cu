@@ -1,0 +1,204 @@
+// One dependent step of a schedule (ring, Rabenseifner or hierarchical), run
+// as one kernel over all of the step's transfers at once.
+//
+// In a step every rank sends one piece to one peer and receives one piece
+// (primer ch. 4, "Collective communication: algorithms, cost and the library
+// that runs them", §4.2: in each of the 2(N-1) ring steps all N links carry
+// one chunk at the same time; a step cannot start before the previous chunk
+// has arrived and been added). With virtual ranks in one HBM, "rank dst
+// receives [lo, hi) from rank src" is dst's kernel thread reading src's buffer
+// directly: reduce-scatter adds its own copy (2 reads + 1 write per element),
+// all-gather overwrites (1 read + 1 write). The kernel boundary is the step
+// boundary; consecutive steps are chained with programmatic dependent launch
+// so that the next step's CTAs are already resident when this one drains.
+//
+// Within a step no transfer writes a range another transfer reads (every
+// rank receives a different piece than the one it sends), so a step is safe
+// in place.
+#include "common.cuh"
+
+namespace ar {
+
+namespace {
+
+struct Operand {
+  char* base;
+  bool f32;
+};
+
+template <bool BF16>
+__device__ __forceinline__ Operand operand(const StepParams& p, int space, int rank) {
+  if (space == RAW) return {static_cast<char*>(p.raw[rank]), !BF16};
+  if (space == RES) return {static_cast<char*>(p.res[rank]), !BF16};
+  // PART: fp32 partial sums -- the output buffer itself for fp32 runs, the
+  // rank's slice of the workspace for bf16 runs
+  if (BF16) return {reinterpret_cast<char*>(p.ws + int64_t(rank) * p.ws_stride), true};
+  return {static_cast<char*>(p.res[rank]), true};
+}
+
+// 8 elements = 32 bytes of fp32 (two 16-byte words) or 16 bytes of bf16.
+struct Raw8 {
+  uint4 a, b;
+};
+
+__device__ __forceinline__ Raw8 load8(const Operand& o, int64_t e) {
+  Raw8 r;
+  if (o.f32) {
+    const uint4* q = reinterpret_cast<const uint4*>(o.base + e * 4);
+    r.a = __ldcs(q);
+    r.b = __ldcs(q + 1);
+  } else {
+    r.a = __ldcs(reinterpret_cast<const uint4*>(o.base + e * 2));
+    r.b = make_uint4(0, 0, 0, 0);
+  }
+  return r;
+}
+
+__device__ __forceinline__ void widen8(const Raw8& r, bool f32, float (&f)[8]) {
+  if (f32) {
+    f[0] = __uint_as_float(r.a.x); f[1] = __uint_as_float(r.a.y);
+    f[2] = __uint_as_float(r.a.z); f[3] = __uint_as_float(r.a.w);
+    f[4] = __uint_as_float(r.b.x); f[5] = __uint_as_float(r.b.y);
+    f[6] = __uint_as_float(r.b.z); f[7] = __uint_as_float(r.b.w);
+  } else {
+    f[0] = bf16lo(r.a.x); f[1] = bf16hi(r.a.x); f[2] = bf16lo(r.a.y); f[3] = bf16hi(r.a.y);
+    f[4] = bf16lo(r.a.z); f[5] = bf16hi(r.a.z); f[6] = bf16lo(r.a.w); f[7] = bf16hi(r.a.w);
+  }
+}
+
+__device__ __forceinline__ void store8(const Operand& o, int64_t e, const float (&f)[8]) {
+  if (o.f32) {
+    uint4* q = reinterpret_cast<uint4*>(o.base + e * 4);
+    __stcs(q, make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                         __float_as_uint(f[3])));
+    __stcs(q + 1, make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]), __float_as_uint(f[6]),
+                             __float_as_uint(f[7])));
+  } else {
+    __stcs(reinterpret_cast<uint4*>(o.base + e * 2),
+           make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7])));
+  }
+}
+
+__device__ __forceinline__ float load1(const Operand& o, int64_t e) {
+  if (o.f32) return reinterpret_cast<const float*>(o.base)[e];
+  return bf16_to_f32(reinterpret_cast<const uint16_t*>(o.base)[e]);
+}
+
+__device__ __forceinline__ void store1(const Operand& o, int64_t e, float v) {
+  if (o.f32)
+    reinterpret_cast<float*>(o.base)[e] = v;
+  else
+    reinterpret_cast<uint16_t*>(o.base)[e] = f32_to_bf16(v);
+}
+
+template <bool BF16, int OP>
+__global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ StepParams p) {
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int total = p.tile_start[p.n_xfer];
+  for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    int lo_i = 0, hi_i = p.n_xfer;  // find x with tile_start[x] <= t < tile_start[x+1]
+    while (hi_i - lo_i > 1) {
+      const int mid = (lo_i + hi_i) >> 1;
+      if (p.tile_start[mid] <= t)
+        lo_i = mid;
+      else
+        hi_i = mid;
+    }
+    const Transfer tr = p.x[lo_i];
+    const int64_t tt = t - p.tile_start[lo_i];
+    const Operand X = operand<BF16>(p, OP == OP_COPY ? RES : tr.xs, tr.src);
+    const Operand Y = operand<BF16>(p, tr.ys, tr.dst);
+    const Operand D = operand<BF16>(p, OP == OP_COPY ? RES : tr.ds, tr.dst);
+    const bool fin = tr.fin != 0;
+    const int64_t a0 = round_up(tr.lo, kStepVec);
+    int64_t a1 = round_down(tr.hi, kStepVec);
+    if (a1 < a0) a1 = a0;
+
+    int64_t e[kStepUnroll];
+    Raw8 rx[kStepUnroll], ry[kStepUnroll];
+#pragma unroll
+    for (int u = 0; u < kStepUnroll; ++u) {
+      e[u] = a0 + tt * kStepTile + (int64_t(u) * kThreads + threadIdx.x) * kStepVec;
+      if (e[u] < a1) {
+        rx[u] = load8(X, e[u]);
+        if (OP == OP_ADD) ry[u] = load8(Y, e[u]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kStepUnroll; ++u) {
+      if (e[u] < a1) {
+        if (OP == OP_COPY) {  // same type on both sides: move the bytes
+          if (X.f32) {
+            uint4* q = reinterpret_cast<uint4*>(D.base + e[u] * 4);
+            __stcs(q, rx[u].a);
+            __stcs(q + 1, rx[u].b);
+          } else {
+            __stcs(reinterpret_cast<uint4*>(D.base + e[u] * 2), rx[u].a);
+          }
+        } else {
+          float f[8];
+          widen8(rx[u], X.f32, f);
+          if (OP == OP_ADD) {
+            float g[8];
+            widen8(ry[u], Y.f32, g);
+#pragma unroll
+            for (int w = 0; w < 8; ++w) f[w] = fadd(f[w], g[w]);
+          }
+          if (fin) {
+#pragma unroll
+            for (int w = 0; w < 8; ++w) f[w] = fmul(f[w], p.scale);
+          }
+          store8(D, e[u], f);
+        }
+      }
+    }
+    if (tt == 0) {  // ragged head [lo, min(a0, hi)) and tail [a1, hi), element by element
+      int64_t es = -1;
+      const int64_t head_end = a0 < tr.hi ? a0 : tr.hi;
+      if (threadIdx.x < kStepVec - 1) {
+        es = tr.lo + threadIdx.x;
+        if (es >= head_end) es = -1;
+      } else if (threadIdx.x >= 32 && threadIdx.x < 32 + kStepVec - 1) {
+        es = a1 + (threadIdx.x - 32);
+        if (es >= tr.hi) es = -1;
+      }
+      if (es >= 0) {
+        float v = load1(X, es);
+        if (OP == OP_ADD) v = fadd(v, load1(Y, es));
+        if (OP != OP_COPY && fin) v = fmul(v, p.scale);
+        store1(D, es, v);
+      }
+    }
+  }
+}
+
+template <bool BF16>
+cudaError_t launch_op(const StepParams& p, StepOp op, int tiles, bool pdl, cudaStream_t stream) {
+  void (*k)(StepParams) = op == OP_ADD ? step_kernel<BF16, OP_ADD>
+                          : op == OP_COPY ? step_kernel<BF16, OP_COPY>
+                                          : step_kernel<BF16, OP_FINISH>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(persistent_grid(reinterpret_cast<const void*>(k), tiles));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, p);
+}
+
+}  // namespace
+
+cudaError_t launch_step(const StepParams& p, ar_dtype dtype, StepOp op, int total_tiles, bool pdl,
+                        cudaStream_t stream) {
+  if (total_tiles <= 0) return cudaSuccess;
+  return dtype == AR_BF16 ? launch_op<true>(p, op, total_tiles, pdl, stream)
+                          : launch_op<false>(p, op, total_tiles, pdl, stream);
+}
+
+}  // namespace ar

@@ -1,0 +1,222 @@
+/*
+ * ar.h -- C ABI of the GB300 gradient all-reduce library (libar_gb300.so).
+ *
+ * The operation (primer ch. 4, "Collective communication: algorithms, cost and
+ * the library that runs them", §4.1, table of collectives): N ranks each hold
+ * a buffer of `count` elements; after the all-reduce every rank holds the
+ * element-wise sum of all N buffers. Scaling ML Systems ("Collective
+ * communication", the ring all-reduce algorithm box) states the same input and
+ * output: rank i starts with G_i, every rank ends with G = G_0 + ... + G_{N-1}.
+ *
+ * Here the N ranks are virtual: their buffers all live in the memory of one
+ * GPU, and a "send" is the receiving rank's kernel reading the sender's
+ * buffer. There is no inter-GPU traffic and no communication library.
+ *
+ * Conventions for every call:
+ *  - Pointers named `bufs`, `outs`, `workspace`, `tensors`, `bucket` are
+ *    DEVICE pointers owned by the caller; arrays of them (`void* const*`) are
+ *    HOST arrays of length n_ranks (or n_ranks * n_tensors). Device buffers
+ *    must be 16-byte aligned and must not overlap one another, except that
+ *    outs[r] may equal bufs[r] (in place).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). Calls that take a stream only enqueue work and return without
+ *    synchronising; completion is observed by the caller through the stream
+ *    (Scaling ML Systems, "Collective communication": initiation of a
+ *    collective is non-blocking, returning does not mean completion).
+ *  - Errors are returned as ar_status, never printed and never fatal.
+ *    Argument checks happen before any work is enqueued; a call that returns
+ *    an error has enqueued nothing. AR_ECUDA reports a CUDA error at launch.
+ *  - No call allocates device memory, and no call synchronises the device,
+ *    except ar_execute_host (which waits for its own copies) and
+ *    ar_device_status (which reads a status word).
+ *  - The library never reads environment variables.
+ */
+#ifndef AR_GB300_H
+#define AR_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define AR_MAX_RANKS 64          /* largest N the kernels accept */
+#define AR_MAX_BUCKET_TENSORS 32 /* tensors in one bucket call */
+
+typedef enum {
+  AR_OK = 0,
+  AR_EINVAL = 1,        /* bad argument: see each call */
+  AR_EUNSUPPORTED = 2,  /* valid request this build does not implement */
+  AR_ENOMEM = 3,        /* host allocation failed */
+  AR_ECUDA = 4,         /* a CUDA runtime call failed */
+  AR_ETIMEOUT = 5       /* a device-side bounded wait ran out (sticky) */
+} ar_status;
+
+typedef enum { AR_F32 = 0, AR_BF16 = 1 } ar_dtype;
+
+/* Algorithms (primer §4.2 ring, §4.3 Rabenseifner, §4.4 hierarchical and
+ * in-network reduction). AR_RING, AR_RABENSEIFNER and AR_HIER run the
+ * schedule step by step: one kernel per dependent step, each step reading
+ * and writing the rank buffers as the schedule's sends and receives do.
+ * AR_FUSED computes the same result in a single pass over HBM: every element
+ * of every rank is read once and written once, the traffic of a rank that
+ * sends its buffer once and receives the sum once (primer §4.4, "In-network
+ * reduction"). */
+typedef enum { AR_RING = 0, AR_RABENSEIFNER = 1, AR_HIER = 2, AR_FUSED = 3 } ar_algo;
+
+/* Per-element summation order of AR_FUSED. Floating-point addition is not
+ * associative, so the order is part of the result (Scaling ML Systems,
+ * "Collective communication": bitwise identity across algorithms is not
+ * guaranteed). Each order reproduces one schedule bit for bit:
+ *  AR_ORDER_RING: element of chunk c: ((g_c + g_{c+1}) + ...) + g_{c-1}, the
+ *                 order of AR_RING (rank i sends chunk (i - s) mod N at
+ *                 reduce-scatter step s, primer §4.2).
+ *  AR_ORDER_RANK: ((g_0 + g_1) + ...) + g_{N-1}.
+ *  AR_ORDER_TREE: balanced binary tree over ranks in index order, the order
+ *                 of AR_RABENSEIFNER (N a power of two).
+ *  AR_ORDER_HIER: the order of AR_HIER with group_size G: inside each group
+ *                 a fold from local rank k+1 for slice k, then the group
+ *                 partials folded from group j for sub-chunk j.          */
+typedef enum { AR_ORDER_RING = 0, AR_ORDER_RANK = 1, AR_ORDER_TREE = 2, AR_ORDER_HIER = 3 } ar_order;
+
+typedef struct {
+  int n_ranks;     /* N, 1..AR_MAX_RANKS */
+  size_t count;    /* elements per rank buffer, >= 0 */
+  ar_dtype dtype;  /* element type of the rank buffers */
+  ar_algo algo;
+  int group_size;  /* AR_HIER, AR_ORDER_HIER: G >= 1 with N % G == 0; else ignored */
+  ar_order order;  /* AR_FUSED only */
+  float scale;     /* multiplies the complete fp32 sum once (1.0f = plain sum) */
+} ar_desc;
+
+/* Accounting of one ar_execute (primer §4.2 and §4.3 cost formulas). */
+typedef struct {
+  int steps;                   /* dependent steps: 2(N-1) ring, 2 log2 N
+                                  Rabenseifner, 2(G-1)+2(M-1) hierarchical,
+                                  1 fused */
+  int launches;                /* kernels one ar_execute launches */
+  size_t bytes_sent_per_rank;  /* largest per-rank send volume of the
+                                  schedule, in bytes of the payload type */
+  size_t hbm_bytes;            /* algorithmic HBM bytes of one ar_execute:
+                                  every element read or written counted once
+                                  per access, at its storage width */
+  size_t workspace_bytes;      /* device workspace ar_execute needs (0 = none) */
+} ar_stats;
+/* With one rank the schedule is empty (all fields 0 but workspace_bytes);
+ * ar_execute then only copies to `outs` and applies `scale`, if needed. */
+
+typedef struct ar_plan ar_plan_t;
+
+/* Validate `desc` and build the schedule's step tables on the host (no GPU
+ * call). Errors (AR_EINVAL): desc or out NULL; n_ranks outside
+ * 1..AR_MAX_RANKS; unknown dtype/algo/order; AR_RABENSEIFNER or
+ * AR_ORDER_TREE with N not a power of two (primer §4.3: "N must be a power of
+ * two"); AR_HIER or AR_ORDER_HIER with group_size < 1 or N % group_size != 0;
+ * scale not finite. AR_ENOMEM if the host tables cannot be allocated. On
+ * success *out owns the tables until ar_plan_destroy. */
+ar_status ar_plan(const ar_desc* desc, ar_plan_t** out);
+
+/* Fill *stats for the plan. AR_EINVAL if either pointer is NULL. */
+ar_status ar_plan_stats(const ar_plan_t* plan, ar_stats* stats);
+
+/* Copy the plan's descriptor into *desc. */
+ar_status ar_plan_desc(const ar_plan_t* plan, ar_desc* desc);
+
+/* Enqueue the all-reduce on `stream`.
+ *  bufs[r]:   rank r's input buffer (count elements of dtype), device.
+ *  outs:      NULL for in place (results overwrite bufs), or outs[r] = rank
+ *             r's output buffer (may equal bufs[r]).
+ *  workspace: device scratch of ar_stats.workspace_bytes bytes, 16-byte
+ *             aligned (fp32 partial sums of the bf16 step executors), or NULL
+ *             when that size is 0. Its contents on entry do not matter.
+ * Every rank ends with bitwise identical results. Errors (AR_EINVAL): NULL
+ * plan or bufs; a NULL or misaligned buffer; overlapping buffers; workspace
+ * NULL or misaligned when one is needed. count == 0 enqueues nothing. */
+ar_status ar_execute(const ar_plan_t* plan, void* const* bufs, void* const* outs, void* workspace,
+                     void* stream);
+
+/* The same all-reduce from and to HOST memory (pinned for full speed):
+ * copies host_in[r] to dev_bufs[r] for every rank, runs the plan in place on
+ * dev_bufs, copies dev_bufs[r] back to host_out[r] (host_out[r] may equal
+ * host_in[r]), and returns when the results are in host memory. AR_FUSED
+ * plans are split into slabs of elements so that copies in both directions
+ * overlap the reduction. dev_bufs and workspace are caller-owned device
+ * memory as in ar_execute. */
+ar_status ar_execute_host(const ar_plan_t* plan, const void* const* host_in, void* const* host_out,
+                          void* const* dev_bufs, void* workspace, void* stream);
+
+void ar_plan_destroy(ar_plan_t* plan);
+
+/* Introspection of a step plan's schedule (host only). For step `step`
+ * (0 <= step < ar_stats.steps), writes *op (0 = reduce: the receiver adds,
+ * 1 = copy: the receiver overwrites) and *n_xfers, and, if xfers is not NULL,
+ * up to max_xfers rows of 4 int64 values {src rank, dst rank, first element,
+ * end element}: rank dst receives elements [first, end) from rank src. Empty
+ * transfers (chunks with no elements) are omitted. AR_EINVAL for a NULL
+ * plan/op/n_xfers, an AR_FUSED plan, or step out of range. */
+ar_status ar_plan_transfers(const ar_plan_t* plan, int step, int* op, int* n_xfers, int64_t* xfers,
+                            int max_xfers);
+
+/* ---------------------------------------------------------------- buckets
+ * DDP bucket fusion (Scaling ML Systems, "Collective communication", section
+ * "Bucket fusion"): gradients are grouped into buckets of a capped byte size,
+ * filled in the reverse of the parameters' forward order, one all-reduce per
+ * bucket.
+ *
+ * Tensors are numbered 0..n_tensors-1 in FORWARD order. A bucket always holds
+ * a contiguous range of tensor ids [t_begin, t_end); inside the bucket they
+ * are packed in DESCENDING id order (the order backward produces them), so
+ * tensor t sits at packed offset sum(counts[u] for t < u < t_end).           */
+
+/* Assign tensors to buckets. counts[t] = elements of tensor t (forward
+ * order), elem_bytes = bytes per gradient element, cap_bytes = bucket cap.
+ * Filling starts at the last tensor; a bucket closes when the next tensor
+ * would take it over cap_bytes; a tensor larger than the cap gets its own
+ * bucket. Outputs: bucket_of_tensor[t] (bucket 0 fills first) and
+ * *n_buckets. Host only. AR_EINVAL: NULL pointers, n_tensors < 1,
+ * elem_bytes == 0. */
+ar_status ar_bucket_plan(const size_t* counts, int n_tensors, size_t elem_bytes, size_t cap_bytes,
+                         int* bucket_of_tensor, int* n_buckets);
+
+/* Pack bucket [t_begin, t_end): bucket[r][packed offset of t + e] =
+ * fp32(tensors[r * n_tensors + t][e]) for every rank r (bf16 widened
+ * exactly). bucket[r] has room for the bucket's element total. */
+ar_status ar_bucket_pack(int n_ranks, const void* const* tensors, const size_t* counts, int n_tensors,
+                         int t_begin, int t_end, ar_dtype in_dtype, void* const* bucket, void* stream);
+
+/* Unpack bucket [t_begin, t_end): tensors[r * n_tensors + t][e] =
+ * round(scale * bucket[r][packed offset of t + e]) in out_dtype (bf16:
+ * round to nearest even, once). */
+ar_status ar_bucket_unpack(int n_ranks, const void* const* bucket, float scale, ar_dtype out_dtype,
+                           void* const* tensors, const size_t* counts, int n_tensors, int t_begin,
+                           int t_end, void* stream);
+
+/* Pack + ring all-reduce + unpack of bucket [t_begin, t_end) in ONE pass with
+ * no pack buffer: every element of every rank's tensors is read once and the
+ * scaled, rounded result written once to every rank. The sum of packed
+ * element e runs in ring order over the packed bucket (chunk boundaries at
+ * floor(c * bucket_count / N)), so the result is bit-identical to
+ * ar_bucket_pack + AR_RING (fp32) + ar_bucket_unpack. dtype is the tensors'
+ * type. In place. */
+ar_status ar_bucket_allreduce(int n_ranks, void* const* tensors, const size_t* counts, int n_tensors,
+                              int t_begin, int t_end, ar_dtype dtype, float scale, void* stream);
+
+/* ---------------------------------------------------------------- status */
+
+/* Read (and clear, if clear != 0) the calling device's sticky status word,
+ * set by a kernel whose bounded device-side wait ran out. Synchronises the
+ * device. Returns AR_OK or AR_ETIMEOUT (or AR_ECUDA). */
+ar_status ar_device_status(int clear);
+
+/* Human-readable name of a status code (static string). */
+const char* ar_status_string(ar_status status);
+
+/* Library version, for the binding's load check. */
+int ar_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AR_GB300_H */

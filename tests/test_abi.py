@@ -1,0 +1,184 @@
+"""The C ABI without a GPU: the library loads, exports every call the header
+declares, rejects bad arguments before touching the device, and its host-side
+schedules are the oracle's schedules step for step.
+
+The oracle and the library share no code: the library builds its step tables
+in C++ from the index rules, the oracle simulates the sends in numpy.
+"""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import workloads
+from oracle import buckets as obuckets
+from oracle import schedules
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def g():
+    from gradient_sync_gb300 import build
+
+    build.build()
+    import gradient_sync_gb300 as g
+
+    return g
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "ar.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(ar_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(g):
+    names = header_functions()
+    assert len(names) >= 14, names
+    lib = ctypes.CDLL(g._lib.LIB_PATH)
+    for name in names:
+        assert hasattr(lib, name), name
+    # and the binding declares exactly those
+    assert sorted(g._lib.SIGNATURES) == names
+
+
+def test_version_and_status_strings(g):
+    assert g.ar_version() >= 1
+    for code in range(6):
+        assert g.ar_status_string(code).startswith("AR_")
+
+
+def _oracle_steps(fn, N, L, **kw):
+    """The oracle's sends grouped by step: {step: set of (src, dst, lo, hi)}."""
+    _, st = fn(np.zeros((N, 0), np.float32), idx=np.zeros(0, np.int64), L=L, **kw)
+    steps = {}
+    for step, src, dst, lo, hi in st.sends:
+        if hi > lo:
+            steps.setdefault(step, set()).add((src, dst, lo, hi))
+    return st, steps
+
+
+CASES = [(N, L) for N in (1, 2, 3, 4, 5, 8, 16) for L in (0, 1, 7, 16, 1000, 4099)] + [(64, 4096), (64, 50)]
+
+
+@pytest.mark.parametrize("N,L", CASES)
+def test_ring_table_matches_oracle(g, N, L):
+    plan = g.ar_plan(N, L, "f32", "ring")
+    st, steps = _oracle_steps(schedules.ring_allreduce, N, L)
+    stats = plan.stats
+    assert stats["steps"] == st.steps == 2 * (N - 1)
+    for s in range(stats["steps"]):
+        op, rows = g.ar_plan_transfers(plan, s)
+        assert op == ("reduce" if s < N - 1 else "copy")
+        assert set(rows) == steps.get(s, set()), s
+    assert stats["bytes_sent_per_rank"] == 4 * int(st.elements_sent.max())
+    assert stats["hbm_bytes"] == 4 * (st.element_reads + st.element_writes)
+
+
+@pytest.mark.parametrize("N,L", [(N, L) for N in (1, 2, 4, 8, 16, 64) for L in (0, 3, 64, 1001)])
+def test_rabenseifner_table_matches_oracle(g, N, L):
+    plan = g.ar_plan(N, L, "f32", "rabenseifner")
+    st, steps = _oracle_steps(schedules.rabenseifner_allreduce, N, L)
+    K = N.bit_length() - 1
+    stats = plan.stats
+    assert stats["steps"] == st.steps == 2 * K
+    for s in range(stats["steps"]):
+        op, rows = g.ar_plan_transfers(plan, s)
+        assert op == ("reduce" if s < K else "copy")
+        assert set(rows) == steps.get(s, set()), s
+    assert stats["hbm_bytes"] == 4 * (st.element_reads + st.element_writes)
+
+
+@pytest.mark.parametrize("N,G,L", [(16, 8, 1000), (16, 8, 4099), (8, 2, 333), (8, 4, 64), (6, 3, 100),
+                                   (8, 1, 77), (8, 8, 77), (4, 2, 3), (64, 8, 4096)])
+def test_hierarchical_table_matches_oracle(g, N, G, L):
+    plan = g.ar_plan(N, L, "f32", "hier", group_size=G)
+    st, steps = _oracle_steps(schedules.hierarchical_allreduce, N, L, group_size=G)
+    M = N // G
+    stats = plan.stats
+    assert stats["steps"] == st.steps == 2 * (G - 1) + 2 * (M - 1)
+    n_reduce = (G - 1) + (M - 1)
+    for s in range(stats["steps"]):
+        op, rows = g.ar_plan_transfers(plan, s)
+        assert op == ("reduce" if s < n_reduce else "copy")
+        assert set(rows) == steps.get(s, set()), s
+    assert stats["hbm_bytes"] == 4 * (st.element_reads + st.element_writes)
+
+
+def test_headline_accounting(g):
+    S = 192 << 20
+    ring = g.ar_plan(16, S // 4, "f32", "ring").stats
+    assert ring["bytes_sent_per_rank"] == 360 << 20
+    assert ring["hbm_bytes"] == 5 * 15 * S  # 5(N-1)*S: 3 per reduce, 2 per copy element
+    fused = g.ar_plan(16, S // 4, "f32", "fused").stats
+    assert fused["hbm_bytes"] == 2 * 16 * S and fused["launches"] == 1
+    hier = g.ar_plan(16, 96 << 20, "bf16", "hier", group_size=8).stats
+    assert hier["steps"] == 16
+    assert hier["workspace_bytes"] == 16 * (96 << 20) * 4
+    assert g.ar_plan(16, 96 << 20, "bf16", "fused", order="hier", group_size=8).stats["workspace_bytes"] == 0
+
+
+@pytest.mark.parametrize("kw", [
+    dict(n_ranks=0), dict(n_ranks=65), dict(dtype=7), dict(algo=9), dict(order=9),
+    dict(algo="rabenseifner", n_ranks=6), dict(order="tree", n_ranks=12),
+    dict(algo="hier", group_size=0), dict(algo="hier", group_size=3),
+    dict(order="hier", group_size=5), dict(scale=float("inf")), dict(scale=float("nan")),
+])
+def test_plan_rejects(g, kw):
+    args = dict(n_ranks=8, count=100, dtype="f32", algo="fused", group_size=2, order="ring", scale=1.0)
+    args.update(kw)
+    with pytest.raises(g.ArError) as e:
+        g.ar_plan(**args)
+    assert e.value.status == g.AR_EINVAL
+
+
+def test_execute_rejects_bad_pointers_without_touching_the_device(g):
+    plan = g.ar_plan(4, 1024, "f32", "fused")
+    good = [0x100000 * (r + 1) for r in range(4)]
+    for bufs in ([0] + good[1:], [good[0] + 4] + good[1:], [good[0]] * 4,
+                 [good[0], good[0] + 2048] + good[2:]):  # null, misaligned, same, overlapping
+        with pytest.raises(g.ArError) as e:
+            g.ar_execute(plan, bufs, stream=0)
+        assert e.value.status == g.AR_EINVAL
+    with pytest.raises(g.ArError):  # an output overlapping another rank's input
+        g.ar_execute(plan, good, outs=[good[1]] + good[1:], stream=0)
+    wplan = g.ar_plan(4, 1024, "bf16", "ring")
+    with pytest.raises(g.ArError) as e:  # bf16 step plans need a workspace
+        g.ar_execute(wplan, good, stream=0)
+    assert e.value.status == g.AR_EINVAL
+    empty = g.ar_plan(4, 0, "f32", "ring")
+    g.ar_execute(empty, good, stream=0)  # count 0: nothing to do, no device call
+
+
+def test_bucket_plan_matches_oracle(g):
+    counts = [c for _, c in workloads.transformer_tensors()]
+    of, nb = g.ar_bucket_plan(counts, 2, workloads.BUCKET_CAP_BYTES)
+    want = obuckets.bucket_plan(counts, 2, workloads.BUCKET_CAP_BYTES)
+    assert nb == len(want) == 81
+    for b, tensors in enumerate(want):
+        assert all(of[t] == b for t in tensors)
+    rng = np.random.default_rng(0)
+    for cap in (1, 9, 100, 10_000):
+        counts = rng.integers(0, 60, 50).tolist()
+        of, nb = g.ar_bucket_plan(counts, 4, cap)
+        want = obuckets.bucket_plan(counts, 4, cap)
+        assert nb == len(want)
+        assert [[t for t in reversed(range(50)) if of[t] == b] for b in range(nb)] == want
+
+
+def test_bucket_calls_reject(g):
+    ok = [[0x100000 * (r * 4 + t + 1) for t in range(3)] for r in range(2)]
+    with pytest.raises(g.ArError):
+        g.ar_bucket_allreduce(ok, [10, 10, 10], 2, 1, "bf16", 0.5, stream=0)  # empty range
+    with pytest.raises(g.ArError):
+        g.ar_bucket_allreduce(ok, [10, 10, 10], 0, 4, "bf16", 0.5, stream=0)  # past the end
+    bad = [row[:] for row in ok]
+    bad[1][2] += 2
+    with pytest.raises(g.ArError):
+        g.ar_bucket_allreduce(bad, [10, 10, 10], 0, 3, "bf16", 0.5, stream=0)  # misaligned
+    with pytest.raises(g.ArError):
+        g.ar_bucket_pack(ok, [10, 10, 10], 0, 3, "bf16", [0x9000000, 0], stream=0)  # null bucket

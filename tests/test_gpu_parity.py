@@ -1,0 +1,225 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle, element by
+element, bit for bit, at sizes the oracle finishes in seconds: several tiles,
+ragged chunk boundaries and tails, tiny and degenerate cases."""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from _gpu import assert_bits_equal, expected, to_device, to_host, widened
+from oracle import numerics
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def g():
+    from gradient_sync_gb300 import build
+
+    build.build()
+    import gradient_sync_gb300 as g
+
+    assert torch.cuda.is_available()
+    return g
+
+
+SIZES = [(1, 5), (2, 1), (2, 2), (3, 7), (4, 1000), (5, 4099), (8, 20003), (16, 100003), (7, 3),
+         (64, 4109), (64, 70), (16, 1 << 18)]
+
+
+def _group(N):
+    for G in (8, 4, 2, 3):
+        if N % G == 0 and G < N:
+            return G
+    return N
+
+
+def _run(g, x, dtype, algo, order="ring", group_size=0, scale=1.0, out_of_place=False):
+    N, L = x.shape
+    devs = [to_device(x[r], dtype) for r in range(N)]
+    outs = [torch.empty_like(d) for d in devs] if out_of_place else None
+    plan = g.ar_plan(N, L, dtype, algo, group_size=group_size, order=order, scale=scale)
+    ws = g.workspace_for(plan)
+    if ws is not None:
+        ws.fill_(0xFF)  # the workspace's contents on entry must not matter
+    g.ar_execute(plan, devs, outs=outs, workspace=ws)
+    torch.cuda.synchronize()
+    res = outs if out_of_place else devs
+    got = [to_host(t, dtype) for t in res]
+    if out_of_place:  # inputs untouched
+        for r in range(N):
+            np.testing.assert_array_equal(to_host(devs[r], dtype), x[r])
+    return got
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("order", ["ring", "rank", "tree", "hier"])
+@pytest.mark.parametrize("N,L", SIZES)
+def test_fused_matches_oracle(g, dtype, order, N, L):
+    if order == "tree" and N & (N - 1):
+        pytest.skip("tree order needs a power-of-two rank count")
+    G = _group(N) if order == "hier" else 0
+    scale = 0.125 if (N + L) % 2 else 1.0
+    x = workloads.all_ranks(workloads.small_spec(N, L, dtype, "normal", seed=N * 7 + L))
+    got = _run(g, x, dtype, "fused", order, G, scale, out_of_place=(L % 3 == 0))
+    want = expected("fused", order, x, dtype, G, scale)
+    for r in range(N):
+        assert_bits_equal(got[r], want, f"rank {r}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("algo", ["ring", "rabenseifner", "hier"])
+@pytest.mark.parametrize("N,L", SIZES)
+def test_step_executor_matches_oracle(g, dtype, algo, N, L):
+    if algo == "rabenseifner" and N & (N - 1):
+        pytest.skip("Rabenseifner needs a power-of-two rank count")
+    G = _group(N) if algo == "hier" else 0
+    scale = 0.5 if (N * L) % 3 == 1 else 1.0
+    x = workloads.all_ranks(workloads.small_spec(N, L, dtype, "uniform", seed=N * 11 + L))
+    got = _run(g, x, dtype, algo, group_size=G, scale=scale, out_of_place=(L % 2 == 1))
+    want = expected(algo, "ring", x, dtype, G, scale)
+    for r in range(N):
+        assert_bits_equal(got[r], want, f"rank {r}")
+
+
+@pytest.mark.parametrize("N,G", [(16, 8), (8, 2), (8, 1), (8, 8), (12, 3), (64, 8)])
+def test_hierarchical_shapes(g, N, G):
+    L = 30011
+    x = workloads.all_ranks(workloads.small_spec(N, L, "bf16", "normal", seed=G))
+    want = expected("hier", "ring", x, "bf16", G)
+    for algo, order in (("hier", "ring"), ("fused", "hier")):
+        got = _run(g, x, "bf16", algo, order, G)
+        for r in range(N):
+            assert_bits_equal(got[r], want, f"{algo} rank {r}")
+
+
+@pytest.mark.parametrize("algo,order", [("ring", "ring"), ("rabenseifner", "ring"), ("hier", "ring"),
+                                        ("fused", "ring"), ("fused", "rank"), ("fused", "tree"),
+                                        ("fused", "hier")])
+def test_integer_inputs_exact(g, algo, order):
+    """Integer inputs: every algorithm and order gives the exact sum."""
+    N, L = 8, 262_147
+    x = workloads.all_ranks(workloads.small_spec(N, L, "f32", "int"))
+    want = numerics.reference_sum_f64(x).astype(np.float32)
+    got = _run(g, x, "f32", algo, order, group_size=4)
+    for r in range(N):
+        assert_bits_equal(got[r], want, f"rank {r}")
+
+
+def test_fused_orders_reproduce_schedules_on_gpu(g):
+    """The fused single pass in a schedule's order equals that schedule run
+    step by step, bit for bit, on the GPU alone."""
+    N, L = 16, 1 << 20
+    x = workloads.all_ranks(workloads.small_spec(N, L, "f32", "normal", seed=3))
+    for algo, order, G in (("ring", "ring", 0), ("rabenseifner", "tree", 0), ("hier", "hier", 4)):
+        a = _run(g, x, "f32", algo, group_size=G)
+        b = _run(g, x, "f32", "fused", order, group_size=G)
+        assert_bits_equal(a[5], b[5], algo)
+
+
+def test_bf16_rounding_ties_on_gpu(g):
+    """bf16 sums that land exactly halfway between two bf16 values round to
+    even, as the format definition says: a bf16 value a plus half its ulp is
+    exact in fp32 and a tie for bf16."""
+    rng = np.random.default_rng(11)
+    K = 8192
+    a32 = (rng.uniform(1, 2, K) * 2.0 ** rng.integers(-30, 30, K) * rng.choice([-1, 1], K)).astype(np.float32)
+    a16 = numerics.f32_to_bf16_rne(a32)
+    a = numerics.bf16_to_f32(a16)
+    e = np.floor(np.log2(np.abs(a.astype(np.float64))))
+    half = (2.0 ** (e - 8) * rng.choice([-1, 1], K)).astype(np.float32)  # bf16 ulp is 2^(e-7)
+    b16 = numerics.f32_to_bf16_rne(half)
+    s = (a + numerics.bf16_to_f32(b16)).astype(np.float32)
+    tie = (s.view(np.uint32) & np.uint32(0xFFFF)) == 0x8000
+    assert tie.sum() > K // 3
+    odd = (s.view(np.uint32) >> np.uint32(16)) & np.uint32(1)
+    assert odd[tie].min() == 0 and odd[tie].max() == 1  # ties to both neighbours
+    x = np.stack([a16[tie], b16[tie]])
+    got = _run(g, x, "bf16", "fused", "rank")
+    want = numerics.f32_to_bf16_rne(s[tie])
+    assert_bits_equal(got[0], want, "ties")
+    assert_bits_equal(got[1], want, "ties")
+
+
+def test_buckets_pack_ring_unpack_and_fused(g):
+    """Bucketed sync: pack + ring + unpack, and the fused no-pack pass, both
+    against the oracle, with tensor sizes that leave ragged vectors and
+    packed offsets that are not 16-byte aligned."""
+    from oracle import buckets as ob
+
+    N = 8
+    counts = [5, 1000, 37, 4096, 9, 2051, 777, 64, 3, 10_000]
+    scale = 1.0 / N
+    rng = np.random.default_rng(7)
+    grads = [[numerics.f32_to_bf16_rne((rng.standard_normal(c) * 1e-3).astype(np.float32)) for c in counts]
+             for _ in range(N)]
+    plan = ob.bucket_plan(counts, 2, 2 * 3000)
+    of, nb = g.ar_bucket_plan(counts, 2, 2 * 3000)
+    assert nb == len(plan)
+    for b in plan:
+        lo, hi = min(b), max(b) + 1
+        assert sorted(b) == list(range(lo, hi))
+        want = ob.sync_bucket(grads, b, counts, scale)
+        Lb = sum(counts[t] for t in b)
+        # path 1: pack -> ring (fp32) -> unpack
+        dev = [[to_device(grads[r][t], "bf16") for t in range(len(counts))] for r in range(N)]
+        bucket = [torch.empty(Lb, dtype=torch.float32, device="cuda") for _ in range(N)]
+        g.ar_bucket_pack(dev, counts, lo, hi, "bf16", bucket)
+        ring = g.ar_plan(N, Lb, "f32", "ring")
+        g.ar_execute(ring, bucket)
+        g.ar_bucket_unpack(bucket, scale, "bf16", dev, counts, lo, hi)
+        torch.cuda.synchronize()
+        for t in b:
+            for r in range(N):
+                assert_bits_equal(to_host(dev[r][t], "bf16"), want[(t, 0)][r], f"pack path t={t} r={r}")
+        # path 2: fused, no pack buffer
+        dev = [[to_device(grads[r][t], "bf16") for t in range(len(counts))] for r in range(N)]
+        g.ar_bucket_allreduce(dev, counts, lo, hi, "bf16", scale)
+        torch.cuda.synchronize()
+        for t in b:
+            for r in range(N):
+                assert_bits_equal(to_host(dev[r][t], "bf16"), want[(t, 0)][r], f"fused t={t} r={r}")
+        # tensors outside the bucket are untouched
+        for t in range(len(counts)):
+            if t not in b:
+                assert_bits_equal(to_host(dev[0][t], "bf16"), grads[0][t], "outside bucket")
+
+
+def test_pack_unpack_f32_roundtrip(g):
+    N = 3
+    counts = [17, 8, 1]
+    rng = np.random.default_rng(1)
+    grads = [[rng.standard_normal(c).astype(np.float32) for c in counts] for _ in range(N)]
+    dev = [[to_device(grads[r][t], "f32") for t in range(3)] for r in range(N)]
+    bucket = [torch.empty(26, dtype=torch.float32, device="cuda") for _ in range(N)]
+    g.ar_bucket_pack(dev, counts, 0, 3, "f32", bucket)
+    torch.cuda.synchronize()
+    for r in range(N):  # descending tensor id inside the bucket
+        np.testing.assert_array_equal(to_host(bucket[r], "f32"),
+                                      np.concatenate([grads[r][2], grads[r][1], grads[r][0]]))
+    g.ar_bucket_unpack(bucket, 2.0, "f32", dev, counts, 0, 3)
+    torch.cuda.synchronize()
+    for r in range(N):
+        for t in range(3):
+            np.testing.assert_array_equal(to_host(dev[r][t], "f32"), grads[r][t] * np.float32(2.0))
+
+
+@pytest.mark.parametrize("algo", ["fused", "ring"])
+def test_execute_host_roundtrip(g, algo):
+    """Host buffers in and out (pinned), several slabs for the fused plan."""
+    N, L = 4, 9 * (1 << 20) + 5
+    x = workloads.all_ranks(workloads.small_spec(N, L, "f32", "normal", seed=9))
+    host_in = [torch.from_numpy(x[r].copy()).pin_memory() for r in range(N)]
+    host_out = [torch.empty(L, dtype=torch.float32).pin_memory() for _ in range(N)]
+    dev = [torch.empty(L, dtype=torch.float32, device="cuda") for _ in range(N)]
+    plan = g.ar_plan(N, L, "f32", algo, order="ring")
+    g.ar_execute_host(plan, host_in, host_out, dev)
+    want = expected(algo, "ring", x, "f32")
+    for r in range(N):
+        assert_bits_equal(host_out[r].numpy(), want, f"rank {r}")
+        np.testing.assert_array_equal(host_in[r].numpy(), x[r])
+
+
+def test_device_status_is_clear(g):
+    assert g.ar_device_status(clear=True) == g.AR_OK
