@@ -1,0 +1,114 @@
+"""Run and time one all-reduce case, or the size/algorithm sweep, on the GPU.
+
+    python -m gradient_sync_gb300.cases --algo fused --order ring --n 16 --count 8388608 --iters 3
+    python -m gradient_sync_gb300.cases --sweep > sweep.jsonl
+
+Each timed case prints one JSON line: time per call (median of CUDA-event
+timings on the launching stream, after warm-up), algbw = S/T, busbw =
+algbw * 2(N-1)/N, and the achieved algorithmic HBM bandwidth of the plan
+(ar_plan_stats.hbm_bytes / T). Inputs are random device data (timing does not
+depend on values); buffers are out of place so every call reduces the same
+data. Small cases run many calls per timing so that the per-call time is
+resolved; %HBM is only meaningful when N*S is well above the L2 size.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import sys
+
+import torch
+
+import gradient_sync_gb300 as g
+
+KiB, MiB, GiB = 1 << 10, 1 << 20, 1 << 30
+
+
+def hbm_peak():
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    try:
+        with open(os.path.join(root, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"])
+    except (OSError, KeyError, ValueError):
+        return 6800.0
+
+
+def time_case(n, count, dtype="f32", algo="fused", order="ring", group_size=0, iters=20, warmup=5,
+              reps=None):
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    esz = 4 if dtype == "f32" else 2
+    bufs = [torch.rand(count, device="cuda").to(tdt) for _ in range(n)]
+    outs = [torch.empty_like(b) for b in bufs]
+    plan = g.ar_plan(n, count, dtype, algo, group_size=group_size, order=order)
+    ws = g.workspace_for(plan)
+    st = plan.stats
+    nbytes = n * count * esz
+    if reps is None:  # calls per timing: enough work to resolve the time of small cases
+        reps = max(1, min(1000, (256 * MiB) // max(1, 2 * nbytes)))
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        g.ar_execute(plan, bufs, outs=outs, workspace=ws)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(iters):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            g.ar_execute(plan, bufs, outs=outs, workspace=ws)
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b) / reps)
+    times.sort()
+    ms = times[len(times) // 2]
+    S = count * esz
+    algbw = S / (ms * 1e-3) / 1e9
+    hbm = st["hbm_bytes"] / (ms * 1e-3) / 1e9
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    res = {"n": n, "bytes_per_rank": S, "dtype": dtype, "algo": algo, "order": order if algo == "fused" else None,
+           "group_size": group_size or None, "us": round(ms * 1e3, 2), "algbw": round(algbw, 2),
+           "busbw": round(algbw * 2 * (n - 1) / n, 2), "steps": st["steps"], "launches": st["launches"],
+           "hbm_bytes": st["hbm_bytes"], "hbm_gbs": round(hbm, 1),
+           "hbm_frac": round(hbm / hbm_peak(), 4) if nbytes > 4 * l2 else None}
+    del bufs, outs, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def sweep(out=sys.stdout, max_total=64 * GiB):
+    for n in (2, 4, 8, 16, 64):
+        for k in range(11):
+            S = KiB * 4 ** k
+            if n * S > max_total:
+                continue
+            for algo, order in (("fused", "ring"), ("fused", "rank"), ("ring", "ring"), ("rabenseifner", "ring")):
+                iters = 20 if n * S < GiB else 5
+                res = time_case(n, S // 4, "f32", algo, order, iters=iters, warmup=3)
+                print(json.dumps(res), file=out, flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--algo", default="fused")
+    ap.add_argument("--order", default="ring")
+    ap.add_argument("--n", type=int, default=16)
+    ap.add_argument("--count", type=int, default=8 * MiB)
+    ap.add_argument("--dtype", default="f32")
+    ap.add_argument("--group-size", type=int, default=0)
+    ap.add_argument("--iters", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--reps", type=int, default=None)
+    ap.add_argument("--sweep", action="store_true")
+    a = ap.parse_args(argv)
+    from gradient_sync_gb300 import build
+
+    build.build()
+    if a.sweep:
+        sweep()
+        return
+    print(json.dumps(time_case(a.n, a.count, a.dtype, a.algo, a.order, a.group_size, a.iters, a.warmup, a.reps)))
+
+
+if __name__ == "__main__":
+    main()
