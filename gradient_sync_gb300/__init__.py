@@ -123,6 +123,17 @@ def ar_execute_host(plan: Plan, host_in, host_out, dev_bufs, workspace=None, str
                                        _ptr(workspace), _stream(stream)), "ar_execute_host")
 
 
+AR_STATIC_WORKSPACE_BYTES = 64 << 20
+
+
+def ar_execute_noalloc(plan: Plan, bufs, outs=None, stream=None):
+    """ar_execute for callers that cannot allocate device memory: the workspace
+    comes from a fixed array inside the library (AR_STATIC_WORKSPACE_BYTES).
+    Calls share that array, so calls that overlap on the GPU race."""
+    o = _ptrs(outs) if outs is not None else None
+    _check(_lib.load().ar_execute_noalloc(plan.handle, _ptrs(bufs), o, _stream(stream)), "ar_execute_noalloc")
+
+
 # ---------------------------------------------------------------- buckets
 
 

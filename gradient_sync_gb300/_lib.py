@@ -30,6 +30,7 @@ SIGNATURES = {
     "ar_plan_desc": (c_int, [c_void_p, ctypes.POINTER(ArDesc)]),
     "ar_execute": (c_int, [c_void_p, VOIDPP, VOIDPP, c_void_p, c_void_p]),
     "ar_execute_host": (c_int, [c_void_p, VOIDPP, VOIDPP, VOIDPP, c_void_p, c_void_p]),
+    "ar_execute_noalloc": (c_int, [c_void_p, VOIDPP, VOIDPP, c_void_p]),
     "ar_plan_destroy": (None, [c_void_p]),
     "ar_plan_transfers": (c_int, [c_void_p, c_int, INTP, INTP, ctypes.POINTER(ctypes.c_int64), c_int]),
     "ar_bucket_plan": (c_int, [SIZEP, c_int, c_size_t, c_size_t, INTP, INTP]),

@@ -146,6 +146,44 @@ ar_status ar_execute(const ar_plan_t* plan, void* const* bufs, void* const* outs
 ar_status ar_execute_host(const ar_plan_t* plan, const void* const* host_in, void* const* host_out,
                           void* const* dev_bufs, void* workspace, void* stream);
 
+/* Size in bytes of the library's own device workspace used by
+ * ar_execute_noalloc. */
+#define AR_STATIC_WORKSPACE_BYTES (64u << 20)
+
+/* ar_execute for callers that cannot allocate device memory. The paper has no
+ * counterpart to this call.
+ *
+ * Who needs it: callers whose device memory is owned by another allocator (a
+ * framework's caching pool, or a fixed budget handed out by a host
+ * application) and who may not call cudaMalloc themselves, and callers on
+ * latency-sensitive paths where cudaMalloc could implicitly synchronise the
+ * device. Such callers cannot provide the workspace that ar_execute asks for
+ * (ar_stats.workspace_bytes; only the bf16 step-by-step plans need one).
+ *
+ * What it does: exactly what ar_execute(plan, bufs, outs, workspace, stream)
+ * does, with the workspace taken from a fixed array of
+ * AR_STATIC_WORKSPACE_BYTES bytes inside the library's device memory (every
+ * GPU that loads the library holds that array until the process exits). It
+ * calls no cudaMalloc, cudaFree or other allocating routine. The caller still
+ * passes the input and output buffers.
+ *
+ * Limits and rules:
+ *  - A plan whose ar_stats.workspace_bytes exceeds AR_STATIC_WORKSPACE_BYTES
+ *    is rejected with AR_EINVAL before anything is enqueued (use ar_execute
+ *    with your own workspace for it). Plans that need no workspace run as
+ *    with ar_execute.
+ *  - The first call on each device looks up the array's device address on
+ *    that device (a CUDA runtime query, not an allocation); make that first
+ *    call before any stream capture begins.
+ *  - All calls share the one array, and it keeps whatever the previous call
+ *    left in it. That is harmless: the kernels write every workspace word
+ *    before they read it within the same call, so nothing has to start at
+ *    zero. But two calls that overlap on the GPU (for example on two streams
+ *    at once) race on the array and give wrong results: order them on one
+ *    stream or with events.
+ * Other arguments and errors as ar_execute. */
+ar_status ar_execute_noalloc(const ar_plan_t* plan, void* const* bufs, void* const* outs, void* stream);
+
 void ar_plan_destroy(ar_plan_t* plan);
 
 /* Introspection of a step plan's schedule (host only). For step `step`
