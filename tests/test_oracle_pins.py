@@ -47,7 +47,7 @@ def test_ring_send_table_fig_4_2(golden):
         rs, ag = val.split("|")
         want = [int(t[1:]) for t in rs.split()] + [int(t[1:]) for t in ag.split()]
         assert table[(src, dst)] == want, key
-    # every step's sends carry every chunk exactly once ("each column holds every chunk once")
+    # in every step the N sends carry N different chunks (Fig. 4.2: no chunk twice in a column)
     for s in range(2 * (N - 1)):
         assert sorted(lo for step, _, _, lo, _ in st.sends if step == s) == list(range(N))
 
