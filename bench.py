@@ -333,7 +333,7 @@ def run_ours(args):
         "executors": executors,
         "e2e": {"value": round(S * world / (ms_e2e * 1e-3) / 1e9, 2), "unit": UNIT,
                 "h2d_bytes_per_step": N * S, "d2h_bytes_per_step": N * S, "ms_per_step": round(ms_e2e, 3),
-                "api": "ar_execute_host (pinned host buffers, slab-pipelined copies)"},
+                "api": "ar_execute_host: pinned host buffers read and written by the kernel over NVLink-C2C"},
         "gpu_launches": args.steps * st["launches"],
         "clocks": clocks.summary(),
     }

@@ -9,6 +9,8 @@ fallback, and importing a function whose library is missing raises.
 
 from __future__ import annotations
 
+import ctypes
+
 from . import _lib
 
 # ---- enums of include/ar.h
@@ -99,8 +101,6 @@ def ar_plan_stats(plan: Plan) -> dict:
 
 def ar_plan_transfers(plan: Plan, step: int):
     """(op, [(src, dst, first, end), ...]) of one step of a step plan."""
-    import ctypes
-
     lib = _lib.load()
     op, n = _lib.c_int(), _lib.c_int()
     _check(lib.ar_plan_transfers(plan.handle, step, op, n, None, 0), "ar_plan_transfers")
@@ -151,31 +151,50 @@ def ar_bucket_plan(counts, elem_bytes: int, cap_bytes: int):
     return list(out), nb.value
 
 
-def _table(tensors):
-    """tensors[r][t] -> flat pointer array [r * n_tensors + t]."""
-    return _lib.ptr_array([_ptr(t) for row in tensors for t in row])
+class TensorTable:
+    """The [rank][tensor] pointer table and element counts of the bucket calls,
+    marshalled once. Pass it in place of the nested tensor list when the same
+    gradients are synchronised again and again (as DDP does every step): the
+    per-call cost is then independent of the number of tensors."""
+
+    def __init__(self, tensors, counts=None):
+        self.n_ranks = len(tensors)
+        self.n_tensors = len(tensors[0])
+        if counts is None:
+            counts = [t.numel() for t in tensors[0]]
+        self.counts = list(counts)
+        self.c_ptrs = _lib.ptr_array([_ptr(t) for row in tensors for t in row])
+        self.c_counts = _counts(self.counts)
+
+
+def _marshal(tensors, counts):
+    if isinstance(tensors, TensorTable):
+        return tensors.n_ranks, tensors.c_ptrs, tensors.c_counts, tensors.n_tensors
+    return len(tensors), _lib.ptr_array([_ptr(t) for row in tensors for t in row]), _counts(counts), len(counts)
+
+
+def _buckets(bucket):
+    """Bucket buffers: a list of tensors/pointers, or an already marshalled pointer array."""
+    return bucket if isinstance(bucket, ctypes.Array) else _ptrs(bucket)
 
 
 def ar_bucket_pack(tensors, counts, t_begin: int, t_end: int, in_dtype, bucket, stream=None):
-    n = len(tensors)
-    _check(_lib.load().ar_bucket_pack(n, _table(tensors), _counts(counts), len(counts), t_begin, t_end,
-                                      DTYPES.get(in_dtype, in_dtype), _ptrs(bucket), _stream(stream)),
-           "ar_bucket_pack")
+    n, ptrs, cnt, nt = _marshal(tensors, counts)
+    _check(_lib.load().ar_bucket_pack(n, ptrs, cnt, nt, t_begin, t_end, DTYPES.get(in_dtype, in_dtype),
+                                      _buckets(bucket), _stream(stream)), "ar_bucket_pack")
 
 
 def ar_bucket_unpack(bucket, scale: float, out_dtype, tensors, counts, t_begin: int, t_end: int,
                      stream=None):
-    n = len(tensors)
-    _check(_lib.load().ar_bucket_unpack(n, _ptrs(bucket), float(scale), DTYPES.get(out_dtype, out_dtype),
-                                        _table(tensors), _counts(counts), len(counts), t_begin, t_end,
-                                        _stream(stream)), "ar_bucket_unpack")
+    n, ptrs, cnt, nt = _marshal(tensors, counts)
+    _check(_lib.load().ar_bucket_unpack(n, _buckets(bucket), float(scale), DTYPES.get(out_dtype, out_dtype),
+                                        ptrs, cnt, nt, t_begin, t_end, _stream(stream)), "ar_bucket_unpack")
 
 
 def ar_bucket_allreduce(tensors, counts, t_begin: int, t_end: int, dtype, scale: float, stream=None):
-    n = len(tensors)
-    _check(_lib.load().ar_bucket_allreduce(n, _table(tensors), _counts(counts), len(counts), t_begin, t_end,
-                                           DTYPES.get(dtype, dtype), float(scale), _stream(stream)),
-           "ar_bucket_allreduce")
+    n, ptrs, cnt, nt = _marshal(tensors, counts)
+    _check(_lib.load().ar_bucket_allreduce(n, ptrs, cnt, nt, t_begin, t_end, DTYPES.get(dtype, dtype),
+                                           float(scale), _stream(stream)), "ar_bucket_allreduce")
 
 
 # ---------------------------------------------------------------- status

@@ -62,18 +62,24 @@ def _run(cmd, verbose):
     return res.stdout + res.stderr
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile every source and link the library. Returns the library path."""
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, defines=(),
+          out: str | None = None, build_dir: str | None = None) -> str:
+    """Compile every source and link the library. Returns the library path.
+
+    ``defines`` (e.g. ["AR_FUSED_NB=8"]) set the compile-time tuning knobs;
+    ``out``/``build_dir`` place a variant build elsewhere."""
+    lib = out or LIB
+    bdir = build_dir or BUILD
+    if not force and out is None and up_to_date():
         return LIB
     cuda = cuda_home()
     nvcc = os.path.join(cuda, "bin", "nvcc")
-    os.makedirs(BUILD, exist_ok=True)
-    common = ["-O3", "-std=c++17", f"-I{INCLUDE}", f"-I{CSRC}"]
+    os.makedirs(bdir, exist_ok=True)
+    common = ["-O3", "-std=c++17", f"-I{INCLUDE}", f"-I{CSRC}"] + [f"-D{d}" for d in defines]
     jobs = []
     objs = []
     for src in CUDA_SOURCES:
-        obj = os.path.join(BUILD, src + ".o")
+        obj = os.path.join(bdir, src + ".o")
         cmd = [nvcc, *ARCH, "-lineinfo", *common, "-Xcompiler", "-fPIC", "-c",
                os.path.join(CSRC, src), "-o", obj]
         if ptxas_info:
@@ -81,20 +87,20 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         jobs.append(cmd)
         objs.append(obj)
     for src in CXX_SOURCES:
-        obj = os.path.join(BUILD, src + ".o")
+        obj = os.path.join(bdir, src + ".o")
         cmd = ["g++", *common, "-fPIC", "-Wall", f"-I{os.path.join(cuda, 'include')}", "-c",
                os.path.join(CSRC, src), "-o", obj]
         jobs.append(cmd)
         objs.append(obj)
     with ThreadPoolExecutor(len(jobs)) as ex:
         logs = list(ex.map(lambda c: _run(c, verbose), jobs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     _run([nvcc, *ARCH, "-shared", "-cudart", "static", "-Xcompiler", "-fPIC", *objs, "-o", tmp,
           "-lpthread", "-ldl", "-lrt"], verbose)
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     if ptxas_info:
         print("\n".join(logs))
-    return LIB
+    return lib
 
 
 def main(argv=None):

@@ -2,6 +2,7 @@
 
     python -m gradient_sync_gb300.cases --algo fused --order ring --n 16 --count 8388608 --iters 3
     python -m gradient_sync_gb300.cases --sweep > sweep.jsonl
+    python -m gradient_sync_gb300.cases --buckets fused|pack --iters 5
 
 Each timed case prints one JSON line: time per call (median of CUDA-event
 timings on the launching stream, after warm-up), algbw = S/T, busbw =
@@ -76,6 +77,70 @@ def time_case(n, count, dtype="f32", algo="fused", order="ring", group_size=0, i
     return res
 
 
+def time_buckets(n=8, path="fused", iters=5, warmup=2, cap_bytes=25 * MiB):
+    """Time one bucketed gradient sync of the 16-layer transformer (hidden 2048,
+    FFN 8192, vocab 32000; bf16 gradients; 25 MiB buckets in reverse layer
+    order; sum scaled by 1/n): every bucket either packed, ring all-reduced in
+    fp32 and unpacked ("pack"), or all-reduced in one fused pass over the
+    gradients in place ("fused")."""
+    import workloads
+
+    counts = [c for _, c in workloads.transformer_tensors()]
+    of, nb = g.ar_bucket_plan(counts, 2, cap_bytes)
+    ranges = []
+    for b in range(nb):
+        ts = [t for t in range(len(counts)) if of[t] == b]
+        ranges.append((min(ts), max(ts) + 1, sum(counts[t] for t in ts)))
+    grads = [[torch.randn(c, device="cuda").to(torch.bfloat16) for c in counts] for _ in range(n)]
+    table = g.TensorTable(grads, counts)  # marshalled once, as a DDP reducer builds its buckets once
+    stream = int(torch.cuda.current_stream().cuda_stream)
+    scale = 1.0 / n
+    total = sum(counts)
+    if path == "pack":
+        max_lb = max(lb for _, _, lb in ranges)
+        bucket_t = [torch.empty(max_lb, dtype=torch.float32, device="cuda") for _ in range(n)]
+        bucket = g._ptrs(bucket_t)
+        plans = {lb: g.ar_plan(n, lb, "f32", "ring") for _, _, lb in ranges}
+        hbm = sum(n * lb * (2 + 4) * 2 + plans[lb].stats["hbm_bytes"] for _, _, lb in ranges)
+        launches = sum(plans[lb].stats["launches"] + 2 for _, _, lb in ranges)
+
+        def sync():
+            for lo, hi, lb in ranges:
+                g.ar_bucket_pack(table, None, lo, hi, "bf16", bucket, stream=stream)
+                g.ar_execute(plans[lb], bucket_t, stream=stream)
+                g.ar_bucket_unpack(bucket, scale, "bf16", table, None, lo, hi, stream=stream)
+    else:
+        hbm = 2 * n * total * 2
+        launches = nb
+
+        def sync():
+            for lo, hi, _ in ranges:
+                g.ar_bucket_allreduce(table, None, lo, hi, "bf16", scale, stream=stream)
+    cur = torch.cuda.current_stream()
+    for _ in range(warmup):
+        sync()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(iters):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        sync()
+        b.record(cur)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    times.sort()
+    ms = times[len(times) // 2]
+    S = total * 2
+    res = {"workload": "bucketed 16-layer transformer", "n": n, "path": path, "buckets": nb,
+           "bytes_per_rank": S, "ms": round(ms, 4), "algbw": round(S / (ms * 1e-3) / 1e9, 2),
+           "busbw": round(S / (ms * 1e-3) / 1e9 * 2 * (n - 1) / n, 2), "launches": launches,
+           "hbm_bytes": hbm, "hbm_gbs": round(hbm / (ms * 1e-3) / 1e9, 1),
+           "hbm_frac": round(hbm / (ms * 1e-3) / 1e9 / hbm_peak(), 4)}
+    del grads, table
+    torch.cuda.empty_cache()
+    return res
+
+
 def sweep(out=sys.stdout, max_total=64 * GiB):
     for n in (2, 4, 8, 16, 64):
         for k in range(11):
@@ -100,12 +165,16 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--reps", type=int, default=None)
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--buckets", choices=["fused", "pack"], default=None)
     a = ap.parse_args(argv)
     from gradient_sync_gb300 import build
 
     build.build()
     if a.sweep:
         sweep()
+        return
+    if a.buckets:
+        print(json.dumps(time_buckets(path=a.buckets, iters=a.iters, warmup=min(a.warmup, 3))))
         return
     print(json.dumps(time_case(a.n, a.count, a.dtype, a.algo, a.order, a.group_size, a.iters, a.warmup, a.reps)))
 

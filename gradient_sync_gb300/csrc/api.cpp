@@ -268,7 +268,7 @@ void fused_tiling(const ar_desc& d, FusedParams& fp) {
     segs.push_back({0, L});
   }
   const int64_t W = d.dtype == AR_BF16 ? 8 : 4;
-  const int64_t tile = fused_tile_elems(d.dtype);
+  const int64_t tile = fused_tile_elems(d.dtype, N, d.order);
   int64_t tps = 1;
   for (auto& s : segs) {
     const int64_t lo = std::max(s.first, fp.e_lo), hi = std::min(s.second, fp.e_hi);
@@ -473,6 +473,34 @@ ar_status ar_execute_host(const ar_plan_t* plan, const void* const* host_in, voi
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   std::lock_guard<std::mutex> lock(g_host_mu);
 
+  if (plan->desc.algo == AR_FUSED) {
+    // Page-locked host memory on a unified-address system is directly
+    // readable and writable by kernels: over NVLink-C2C the single pass then
+    // reads host_in and writes host_out itself, with no staging copies.
+    std::vector<void*> in_dev(N, nullptr), out_dev(N, nullptr);
+    bool direct = true;
+    for (int r = 0; r < N && direct; ++r) {
+      cudaPointerAttributes a{}, b{};
+      if (cudaPointerGetAttributes(&a, host_in[r]) != cudaSuccess ||
+          cudaPointerGetAttributes(&b, host_out[r]) != cudaSuccess) {
+        cudaGetLastError();  // pageable memory on some drivers reports an error: not direct
+        direct = false;
+        break;
+      }
+      direct = a.type == cudaMemoryTypeHost && b.type == cudaMemoryTypeHost && a.devicePointer != nullptr &&
+               b.devicePointer != nullptr;
+      in_dev[r] = a.devicePointer;
+      out_dev[r] = b.devicePointer;
+    }
+    if (direct) {
+      const ar_status e = check_buffers(plan, in_dev.data(), out_dev.data(), nullptr);
+      if (e != AR_OK) return e;
+      const ar_status x = execute_fused(plan, in_dev.data(), out_dev.data(), 0, L, st);
+      if (x != AR_OK) return x;
+      return from_cuda(cudaStreamSynchronize(st));
+    }
+  }
+
   if (plan->desc.algo != AR_FUSED) {  // the schedule spans the whole buffer: copy, run, copy
     for (int r = 0; r < N; ++r)
       if (cudaMemcpyAsync(dev_bufs[r], host_in[r], size_t(L) * es, cudaMemcpyHostToDevice, st) != cudaSuccess)
@@ -635,7 +663,7 @@ ar_status ar_bucket_allreduce(int n_ranks, void* const* tensors, const size_t* c
   if (Lb == 0) return AR_OK;
   const auto b = cuts(0, Lb, N);
   const int64_t W = dtype == AR_BF16 ? 8 : 4;
-  const int64_t tile = fused_tile_elems(dtype);
+  const int64_t tile = fused_tile_elems(dtype, N, AR_ORDER_RING);
   const int max_group = std::min(AR_MAX_BUCKET_TENSORS, kMaxBucketPtrs / N);
   static thread_local BucketFusedParams bp;
   std::memset(&bp, 0, sizeof(bp));

@@ -128,41 +128,49 @@ struct Lane<true, false> {  // 1 x bf16
 //   kEnd:   this value completes the group partial; fold it into the total
 //   kFirst: the completed group partial is the first one (total = partial)
 // A ring or rank-order fold is one group of N; the hierarchical order is M
-// groups of G. Loads are issued NB ranks at a time before any add so that
-// NB 16-byte requests per thread are in flight.
+// groups of G. Each thread folds VPT vectors at once; loads are issued NB
+// ranks at a time before any add, so that NB * VPT 16-byte requests per
+// thread are in flight (VPT > 1 keeps that number up when N is small).
 // ---------------------------------------------------------------------------
 enum : uint8_t { kStart = 1, kEnd = 2, kFirst = 4 };
 
-template <class L, int NB>
-__device__ __forceinline__ void fold_sequence(float (&acc)[L::W], const char* const* seq_ptr,
-                                              const uint8_t* seq_flag, int n, int64_t e) {
-  float part[L::W];
+template <class L, int NB, int VPT>
+__device__ __forceinline__ void fold_sequence(float (&acc)[VPT][L::W], const char* const* seq_ptr,
+                                              const uint8_t* seq_flag, int n, const int64_t (&e)[VPT],
+                                              const bool (&ok)[VPT]) {
+  float part[VPT][L::W];
 #pragma unroll 1
   for (int base = 0; base < n; base += NB) {
-    typename L::raw_t v[NB];
+    typename L::raw_t v[NB][VPT];
 #pragma unroll
     for (int b = 0; b < NB; ++b)
-      if (base + b < n) v[b] = L::load(seq_ptr[base + b], e);
+#pragma unroll
+      for (int q = 0; q < VPT; ++q)
+        if (base + b < n && ok[q]) v[b][q] = L::load(seq_ptr[base + b], e[q]);
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       if (base + b < n) {
         const uint8_t fl = seq_flag[base + b];
-        float f[L::W];
-        L::widen(v[b], f);
-        if (fl & kStart) {
 #pragma unroll
-          for (int w = 0; w < L::W; ++w) part[w] = f[w];
-        } else {
+        for (int q = 0; q < VPT; ++q) {
+          if (!ok[q]) continue;
+          float f[L::W];
+          L::widen(v[b][q], f);
+          if (fl & kStart) {
 #pragma unroll
-          for (int w = 0; w < L::W; ++w) part[w] = fadd(part[w], f[w]);
-        }
-        if (fl & kEnd) {
-          if (fl & kFirst) {
-#pragma unroll
-            for (int w = 0; w < L::W; ++w) acc[w] = part[w];
+            for (int w = 0; w < L::W; ++w) part[q][w] = f[w];
           } else {
 #pragma unroll
-            for (int w = 0; w < L::W; ++w) acc[w] = fadd(acc[w], part[w]);
+            for (int w = 0; w < L::W; ++w) part[q][w] = fadd(part[q][w], f[w]);
+          }
+          if (fl & kEnd) {
+            if (fl & kFirst) {
+#pragma unroll
+              for (int w = 0; w < L::W; ++w) acc[q][w] = part[q][w];
+            } else {
+#pragma unroll
+              for (int w = 0; w < L::W; ++w) acc[q][w] = fadd(acc[q][w], part[q][w]);
+            }
           }
         }
       }

@@ -24,6 +24,14 @@
 // registers and stores it to all N ranks.
 #include "common.cuh"
 
+// Tuning knob (compile time): the minimum resident CTAs per SM that the
+// register allocation must allow. Two CTAs of 256 threads per SM, each thread
+// keeping about eight 16-byte loads in flight, measured best on GB300 (one
+// CTA left too few warps to cover HBM latency).
+#ifndef AR_FUSED_MINB
+#define AR_FUSED_MINB 2
+#endif
+
 namespace ar {
 
 namespace {
@@ -68,12 +76,12 @@ __device__ __forceinline__ void seg_range(const FusedParams& p, int seg, int64_t
   }
 }
 
-template <bool BF16, bool TREE, int NB>
-__global__ void __launch_bounds__(kThreads) fused_flat_kernel(const __grid_constant__ FusedParams p) {
+template <bool BF16, bool TREE, int NB, int VPT>
+__global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_flat_kernel(const __grid_constant__ FusedParams p) {
   using LV = Lane<BF16, true>;
   using LS = Lane<BF16, false>;
   constexpr int W = LV::W;
-  constexpr int64_t kTile = int64_t(kThreads) * W;
+  constexpr int64_t kTile = int64_t(kThreads) * W * VPT;
   __shared__ const char* s_seq[AR_MAX_RANKS];
   __shared__ uint8_t s_flag[AR_MAX_RANKS];
   __shared__ char* s_out[AR_MAX_RANKS];
@@ -104,18 +112,34 @@ __global__ void __launch_bounds__(kThreads) fused_flat_kernel(const __grid_const
     const int64_t a0 = round_up(clo, W);
     int64_t a1 = round_down(chi, W);
     if (a1 < a0) a1 = a0;
-    const int64_t e = a0 + tt * kTile + int64_t(threadIdx.x) * W;
-    if (e < a1) {
-      float acc[W];
-      if (TREE)
-        fold_tree<LV, NB>(acc, s_seq, n, e);
-      else
-        fold_sequence<LV, NB>(acc, s_seq, s_flag, n, e);
+    int64_t e[VPT];
+    bool ok[VPT];
+    bool any = false;
 #pragma unroll
-      for (int w = 0; w < W; ++w) acc[w] = fmul(acc[w], p.scale);
-      const typename LV::raw_t r = LV::narrow(acc);
-#pragma unroll 4
-      for (int q = 0; q < n; ++q) LV::store(s_out[q], e, r);
+    for (int q = 0; q < VPT; ++q) {
+      e[q] = a0 + tt * kTile + (int64_t(q) * kThreads + threadIdx.x) * W;
+      ok[q] = e[q] < a1;
+      any |= ok[q];
+    }
+    if (any) {
+      float acc[VPT][W];
+      if (TREE) {
+        fold_tree<LV, NB>(acc[0], s_seq, n, e[0]);
+      } else {
+        fold_sequence<LV, NB, VPT>(acc, s_seq, s_flag, n, e, ok);
+      }
+      typename LV::raw_t r[VPT];
+#pragma unroll
+      for (int q = 0; q < VPT; ++q) {
+#pragma unroll
+        for (int w = 0; w < W; ++w) acc[q][w] = fmul(acc[q][w], p.scale);
+        r[q] = LV::narrow(acc[q]);
+      }
+#pragma unroll 2
+      for (int d = 0; d < n; ++d)
+#pragma unroll
+        for (int q = 0; q < VPT; ++q)
+          if (ok[q]) LV::store(s_out[d], e[q], r[q]);
     }
     if (tt == 0) {  // ragged head [clo, min(a0, chi)) and tail [a1, chi)
       int64_t es = -1;
@@ -128,13 +152,15 @@ __global__ void __launch_bounds__(kThreads) fused_flat_kernel(const __grid_const
         if (es >= chi) es = -1;
       }
       if (es >= 0) {
-        float acc[1];
+        float acc[1][1];
+        const int64_t es1[1] = {es};
+        const bool ok1[1] = {true};
         if (TREE)
-          fold_tree<LS, 8>(acc, s_seq, n, es);
+          fold_tree<LS, 8>(acc[0], s_seq, n, es);
         else
-          fold_sequence<LS, 8>(acc, s_seq, s_flag, n, es);
-        acc[0] = fmul(acc[0], p.scale);
-        const typename LS::raw_t r = LS::narrow(acc);
+          fold_sequence<LS, 8, 1>(acc, s_seq, s_flag, n, es1, ok1);
+        acc[0][0] = fmul(acc[0][0], p.scale);
+        const typename LS::raw_t r = LS::narrow(acc[0]);
         for (int q = 0; q < n; ++q) LS::store(s_out[q], es, r);
       }
     }
@@ -145,13 +171,13 @@ __global__ void __launch_bounds__(kThreads) fused_flat_kernel(const __grid_const
 // (tensor, rank) pointer table; segments are the pieces of the tensors cut at
 // the ring's chunk boundaries over the packed bucket, so each segment is
 // folded in ring order from its chunk's rank.
-template <bool BF16, int NB>
-__global__ void __launch_bounds__(kThreads)
+template <bool BF16, int NB, int VPT>
+__global__ void __launch_bounds__(kThreads, AR_FUSED_MINB)
     fused_bucket_kernel(const __grid_constant__ BucketFusedParams p) {
   using LV = Lane<BF16, true>;
   using LS = Lane<BF16, false>;
   constexpr int W = LV::W;
-  constexpr int64_t kTile = int64_t(kThreads) * W;
+  constexpr int64_t kTile = int64_t(kThreads) * W * VPT;
   __shared__ const char* s_seq[AR_MAX_RANKS];
   __shared__ uint8_t s_flag[AR_MAX_RANKS];
   __shared__ char* s_out[AR_MAX_RANKS];
@@ -178,15 +204,30 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t a0 = round_up(sg.lo, W);
     int64_t a1 = round_down(sg.hi, W);
     if (a1 < a0) a1 = a0;
-    const int64_t e = a0 + tt * kTile + int64_t(threadIdx.x) * W;
-    if (e < a1) {
-      float acc[W];
-      fold_sequence<LV, NB>(acc, s_seq, s_flag, n, e);
+    int64_t e[VPT];
+    bool ok[VPT];
+    bool any = false;
 #pragma unroll
-      for (int w = 0; w < W; ++w) acc[w] = fmul(acc[w], p.scale);
-      const typename LV::raw_t r = LV::narrow(acc);
-#pragma unroll 4
-      for (int q = 0; q < n; ++q) LV::store(s_out[q], e, r);
+    for (int q = 0; q < VPT; ++q) {
+      e[q] = a0 + tt * kTile + (int64_t(q) * kThreads + threadIdx.x) * W;
+      ok[q] = e[q] < a1;
+      any |= ok[q];
+    }
+    if (any) {
+      float acc[VPT][W];
+      fold_sequence<LV, NB, VPT>(acc, s_seq, s_flag, n, e, ok);
+      typename LV::raw_t r[VPT];
+#pragma unroll
+      for (int q = 0; q < VPT; ++q) {
+#pragma unroll
+        for (int w = 0; w < W; ++w) acc[q][w] = fmul(acc[q][w], p.scale);
+        r[q] = LV::narrow(acc[q]);
+      }
+#pragma unroll 2
+      for (int d = 0; d < n; ++d)
+#pragma unroll
+        for (int q = 0; q < VPT; ++q)
+          if (ok[q]) LV::store(s_out[d], e[q], r[q]);
     }
     if (tt == 0) {
       int64_t es = -1;
@@ -199,10 +240,12 @@ __global__ void __launch_bounds__(kThreads)
         if (es >= sg.hi) es = -1;
       }
       if (es >= 0) {
-        float acc[1];
-        fold_sequence<LS, 8>(acc, s_seq, s_flag, n, es);
-        acc[0] = fmul(acc[0], p.scale);
-        const typename LS::raw_t r = LS::narrow(acc);
+        float acc[1][1];
+        const int64_t es1[1] = {es};
+        const bool ok1[1] = {true};
+        fold_sequence<LS, 8, 1>(acc, s_seq, s_flag, n, es1, ok1);
+        acc[0][0] = fmul(acc[0][0], p.scale);
+        const typename LS::raw_t r = LS::narrow(acc[0]);
         for (int q = 0; q < n; ++q) LS::store(s_out[q], es, r);
       }
     }
@@ -219,22 +262,44 @@ cudaError_t launch_persistent(void (*kernel)(P), const P& p, int64_t tiles, cuda
 
 }  // namespace
 
-int64_t fused_tile_elems(ar_dtype dtype) { return int64_t(kThreads) * (dtype == AR_BF16 ? 8 : 4); }
+// Vectors per thread for N ranks: about eight 16-byte loads in flight per
+// thread whatever N is (N loads per vector).
+int fused_vpt(int n, int order) {
+  if (order == AR_ORDER_TREE) return 1;
+  return n <= 2 ? 4 : n <= 4 ? 2 : 1;
+}
+
+int64_t fused_tile_elems(ar_dtype dtype, int n, int order) {
+  return int64_t(kThreads) * (dtype == AR_BF16 ? 8 : 4) * fused_vpt(n, order);
+}
+
+template <bool BF16>
+cudaError_t launch_fused_t(const FusedParams& p, int64_t tiles, cudaStream_t stream) {
+  if (p.order == AR_ORDER_TREE) return launch_persistent(fused_flat_kernel<BF16, true, 8, 1>, p, tiles, stream);
+  switch (fused_vpt(p.n, p.order)) {
+    case 4: return launch_persistent(fused_flat_kernel<BF16, false, 2, 4>, p, tiles, stream);
+    case 2: return launch_persistent(fused_flat_kernel<BF16, false, 4, 2>, p, tiles, stream);
+    default: return launch_persistent(fused_flat_kernel<BF16, false, 8, 1>, p, tiles, stream);
+  }
+}
 
 cudaError_t launch_fused(const FusedParams& p, ar_dtype dtype, cudaStream_t stream) {
   const int64_t tiles = int64_t(p.n_seg) * p.tiles_per_seg;
-  const bool tree = p.order == AR_ORDER_TREE;
-  if (dtype == AR_BF16)
-    return tree ? launch_persistent(fused_flat_kernel<true, true, 8>, p, tiles, stream)
-                : launch_persistent(fused_flat_kernel<true, false, 16>, p, tiles, stream);
-  return tree ? launch_persistent(fused_flat_kernel<false, true, 8>, p, tiles, stream)
-              : launch_persistent(fused_flat_kernel<false, false, 16>, p, tiles, stream);
+  return dtype == AR_BF16 ? launch_fused_t<true>(p, tiles, stream) : launch_fused_t<false>(p, tiles, stream);
+}
+
+template <bool BF16>
+cudaError_t launch_bucket_t(const BucketFusedParams& p, int64_t tiles, cudaStream_t stream) {
+  switch (fused_vpt(p.n, AR_ORDER_RING)) {
+    case 4: return launch_persistent(fused_bucket_kernel<BF16, 2, 4>, p, tiles, stream);
+    case 2: return launch_persistent(fused_bucket_kernel<BF16, 4, 2>, p, tiles, stream);
+    default: return launch_persistent(fused_bucket_kernel<BF16, 8, 1>, p, tiles, stream);
+  }
 }
 
 cudaError_t launch_bucket_fused(const BucketFusedParams& p, ar_dtype dtype, cudaStream_t stream) {
   const int64_t tiles = p.tile_start[p.n_seg];
-  if (dtype == AR_BF16) return launch_persistent(fused_bucket_kernel<true, 16>, p, tiles, stream);
-  return launch_persistent(fused_bucket_kernel<false, 16>, p, tiles, stream);
+  return dtype == AR_BF16 ? launch_bucket_t<true>(p, tiles, stream) : launch_bucket_t<false>(p, tiles, stream);
 }
 
 }  // namespace ar

@@ -136,13 +136,17 @@ ar_status ar_plan_desc(const ar_plan_t* plan, ar_desc* desc);
 ar_status ar_execute(const ar_plan_t* plan, void* const* bufs, void* const* outs, void* workspace,
                      void* stream);
 
-/* The same all-reduce from and to HOST memory (pinned for full speed):
- * copies host_in[r] to dev_bufs[r] for every rank, runs the plan in place on
- * dev_bufs, copies dev_bufs[r] back to host_out[r] (host_out[r] may equal
- * host_in[r]), and returns when the results are in host memory. AR_FUSED
- * plans are split into slabs of elements so that copies in both directions
- * overlap the reduction. dev_bufs and workspace are caller-owned device
- * memory as in ar_execute. */
+/* The same all-reduce from and to HOST memory; returns when the results are
+ * in host memory (host_out[r] may equal host_in[r]).
+ *  - AR_FUSED plans whose host buffers are page-locked and device-accessible
+ *    (pinned memory on a unified-address system such as Grace-Blackwell):
+ *    the single pass reads host_in and writes host_out directly over the
+ *    host link; dev_bufs are not touched.
+ *  - Other AR_FUSED plans: the buffers are cut into slabs; each slab is copied
+ *    to dev_bufs, reduced, and copied back, with the copies of neighbouring
+ *    slabs in both directions overlapping the reduction.
+ *  - Step plans: copy host_in to dev_bufs, run the plan in place, copy back.
+ * dev_bufs and workspace are caller-owned device memory as in ar_execute. */
 ar_status ar_execute_host(const ar_plan_t* plan, const void* const* host_in, void* const* host_out,
                           void* const* dev_bufs, void* workspace, void* stream);
 

@@ -205,13 +205,19 @@ def test_pack_unpack_f32_roundtrip(g):
             np.testing.assert_array_equal(to_host(dev[r][t], "f32"), grads[r][t] * np.float32(2.0))
 
 
+@pytest.mark.parametrize("pinned", [True, False])
 @pytest.mark.parametrize("algo", ["fused", "ring"])
-def test_execute_host_roundtrip(g, algo):
-    """Host buffers in and out (pinned), several slabs for the fused plan."""
+def test_execute_host_roundtrip(g, algo, pinned):
+    """Host buffers in and out: pinned buffers are read and written directly by
+    the fused kernel; pageable ones are staged through the device buffers in
+    several slabs."""
     N, L = 4, 9 * (1 << 20) + 5
     x = workloads.all_ranks(workloads.small_spec(N, L, "f32", "normal", seed=9))
-    host_in = [torch.from_numpy(x[r].copy()).pin_memory() for r in range(N)]
-    host_out = [torch.empty(L, dtype=torch.float32).pin_memory() for _ in range(N)]
+    host_in = [torch.from_numpy(x[r].copy()) for r in range(N)]
+    host_out = [torch.empty(L, dtype=torch.float32) for _ in range(N)]
+    if pinned:
+        host_in = [t.pin_memory() for t in host_in]
+        host_out = [t.pin_memory() for t in host_out]
     dev = [torch.empty(L, dtype=torch.float32, device="cuda") for _ in range(N)]
     plan = g.ar_plan(N, L, "f32", algo, order="ring")
     g.ar_execute_host(plan, host_in, host_out, dev)
