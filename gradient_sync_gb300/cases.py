@@ -47,7 +47,7 @@ def time_case(n, count, dtype="f32", algo="fused", order="ring", group_size=0, i
     st = plan.stats
     nbytes = n * count * esz
     if reps is None:  # calls per timing: enough work to resolve the time of small cases
-        reps = max(1, min(1000, (256 * MiB) // max(1, 2 * nbytes)))
+        reps = max(1, min(1000, (256 * MiB) // max(1, 2 * nbytes), 4000 // max(1, st["launches"])))
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         g.ar_execute(plan, bufs, outs=outs, workspace=ws)
@@ -148,7 +148,7 @@ def sweep(out=sys.stdout, max_total=64 * GiB):
             if n * S > max_total:
                 continue
             for algo, order in (("fused", "ring"), ("fused", "rank"), ("ring", "ring"), ("rabenseifner", "ring")):
-                iters = 20 if n * S < GiB else 5
+                iters = 10 if n * S < GiB else 5
                 res = time_case(n, S // 4, "f32", algo, order, iters=iters, warmup=3)
                 print(json.dumps(res), file=out, flush=True)
 

@@ -324,7 +324,6 @@ ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs
     sp.tile_start[1] = int32_t(std::max<int64_t>(1, (body + kStepTile - 1) / kStepTile));
     return from_cuda(launch_step(sp, d.dtype, OP_FINISH, sp.tile_start[1], false, stream));
   }
-  bool first = true;
   for (const Step& st : p->steps) {
     if (st.xfers.empty()) continue;
     sp.n_xfer = int(st.xfers.size());
@@ -337,9 +336,8 @@ ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs
       tiles += int(std::max<int64_t>(1, (body + kStepTile - 1) / kStepTile));
     }
     sp.tile_start[sp.n_xfer] = tiles;
-    const ar_status s = from_cuda(launch_step(sp, d.dtype, st.op, tiles, !first, stream));
+    const ar_status s = from_cuda(launch_step(sp, d.dtype, st.op, tiles, true, stream));
     if (s != AR_OK) return s;
-    first = false;
   }
   return AR_OK;
 }

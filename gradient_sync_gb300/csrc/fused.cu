@@ -85,6 +85,8 @@ __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_flat_kernel(con
   __shared__ const char* s_seq[AR_MAX_RANKS];
   __shared__ uint8_t s_flag[AR_MAX_RANKS];
   __shared__ char* s_out[AR_MAX_RANKS];
+  grid_dependency_wait();  // the previous kernel on the stream has finished and its writes are visible
+  grid_dependents_launch();
   const int n = p.n;
   if (threadIdx.x < n) s_out[threadIdx.x] = static_cast<char*>(p.out[threadIdx.x]);
   int cur = -1;
@@ -181,6 +183,8 @@ __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB)
   __shared__ const char* s_seq[AR_MAX_RANKS];
   __shared__ uint8_t s_flag[AR_MAX_RANKS];
   __shared__ char* s_out[AR_MAX_RANKS];
+  grid_dependency_wait();
+  grid_dependents_launch();
   const int n = p.n;
   int cur = -1;
   const int total = p.tile_start[p.n_seg];
@@ -252,12 +256,22 @@ __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB)
   }
 }
 
+// Launched with programmatic dependent launch: the kernel may be scheduled
+// while the previous kernel on the stream drains, and waits for it
+// (griddepcontrol.wait) before touching memory, so stream order holds.
 template <class P>
 cudaError_t launch_persistent(void (*kernel)(P), const P& p, int64_t tiles, cudaStream_t stream) {
   if (tiles <= 0) return cudaSuccess;
-  const int grid = persistent_grid(reinterpret_cast<const void*>(kernel), tiles);
-  kernel<<<grid, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(persistent_grid(reinterpret_cast<const void*>(kernel), tiles));
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 }  // namespace

@@ -16,6 +16,8 @@ namespace {
 
 template <bool BF16, bool UNPACK>
 __global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ PackParams p) {
+  grid_dependency_wait();  // stream order with the previous kernel (see launch_pack)
+  grid_dependents_launch();
   const int per_rank = p.tile_start[p.n_t];
   const int total = per_rank * p.n;
   for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -91,8 +93,16 @@ cudaError_t launch_pack(const PackParams& p, ar_dtype dtype, bool unpack, cudaSt
   if (tiles <= 0) return cudaSuccess;
   void (*k)(PackParams) = dtype == AR_BF16 ? (unpack ? pack_kernel<true, true> : pack_kernel<true, false>)
                                            : (unpack ? pack_kernel<false, true> : pack_kernel<false, false>);
-  k<<<persistent_grid(reinterpret_cast<const void*>(k), tiles), kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(persistent_grid(reinterpret_cast<const void*>(k), tiles));
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, p);
 }
 
 // Sticky status word of this library on each device, set by a kernel whose

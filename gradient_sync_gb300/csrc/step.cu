@@ -188,7 +188,7 @@ cudaError_t launch_op(const StepParams& p, StepOp op, int tiles, bool pdl, cudaS
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = pdl ? 1 : 0;  // safe either way: the kernel waits on griddepcontrol.wait first
   return cudaLaunchKernelEx(&cfg, k, p);
 }
 
