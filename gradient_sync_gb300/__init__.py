@@ -18,12 +18,14 @@ AR_OK, AR_EINVAL, AR_EUNSUPPORTED, AR_ENOMEM, AR_ECUDA, AR_ETIMEOUT = range(6)
 AR_F32, AR_BF16 = 0, 1
 AR_RING, AR_RABENSEIFNER, AR_HIER, AR_FUSED = 0, 1, 2, 3
 AR_ORDER_RING, AR_ORDER_RANK, AR_ORDER_TREE, AR_ORDER_HIER = 0, 1, 2, 3
+AR_ALLREDUCE, AR_REDUCE_SCATTER, AR_ALLGATHER = 0, 1, 2
 AR_MAX_RANKS = 64
 AR_MAX_BUCKET_TENSORS = 32
 
 ALGOS = {"ring": AR_RING, "rabenseifner": AR_RABENSEIFNER, "hier": AR_HIER, "fused": AR_FUSED}
 ORDERS = {"ring": AR_ORDER_RING, "rank": AR_ORDER_RANK, "tree": AR_ORDER_TREE, "hier": AR_ORDER_HIER}
 DTYPES = {"f32": AR_F32, "bf16": AR_BF16}
+COLLECTIVES = {"allreduce": AR_ALLREDUCE, "reduce_scatter": AR_REDUCE_SCATTER, "allgather": AR_ALLGATHER}
 
 
 class ArError(RuntimeError):
@@ -83,14 +85,15 @@ class Plan:
 
 
 def ar_plan(n_ranks: int, count: int, dtype="f32", algo="fused", group_size: int = 0, order="ring",
-            scale: float = 1.0) -> Plan:
+            scale: float = 1.0, collective="allreduce") -> Plan:
     """Validate the descriptor and build the schedule (host only)."""
     d = _lib.ArDesc(int(n_ranks), int(count), DTYPES.get(dtype, dtype), ALGOS.get(algo, algo),
-                    int(group_size), ORDERS.get(order, order), float(scale))
+                    int(group_size), ORDERS.get(order, order), float(scale),
+                    COLLECTIVES.get(collective, collective))
     h = _lib.c_void_p()
     _check(_lib.load().ar_plan(d, h), "ar_plan")
     return Plan(h.value, dict(n_ranks=n_ranks, count=count, dtype=dtype, algo=algo,
-                              group_size=group_size, order=order, scale=scale))
+                              group_size=group_size, order=order, scale=scale, collective=collective))
 
 
 def ar_plan_stats(plan: Plan) -> dict:

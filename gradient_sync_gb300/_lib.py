@@ -15,7 +15,7 @@ INTP = ctypes.POINTER(c_int)
 
 class ArDesc(ctypes.Structure):
     _fields_ = [("n_ranks", c_int), ("count", c_size_t), ("dtype", c_int), ("algo", c_int),
-                ("group_size", c_int), ("order", c_int), ("scale", c_float)]
+                ("group_size", c_int), ("order", c_int), ("scale", c_float), ("collective", c_int)]
 
 
 class ArStats(ctypes.Structure):

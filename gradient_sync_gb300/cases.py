@@ -37,12 +37,12 @@ def hbm_peak():
 
 
 def time_case(n, count, dtype="f32", algo="fused", order="ring", group_size=0, iters=20, warmup=5,
-              reps=None):
+              reps=None, graph=False, collective="allreduce"):
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
     esz = 4 if dtype == "f32" else 2
     bufs = [torch.rand(count, device="cuda").to(tdt) for _ in range(n)]
     outs = [torch.empty_like(b) for b in bufs]
-    plan = g.ar_plan(n, count, dtype, algo, group_size=group_size, order=order)
+    plan = g.ar_plan(n, count, dtype, algo, group_size=group_size, order=order, collective=collective)
     ws = g.workspace_for(plan)
     st = plan.stats
     nbytes = n * count * esz
@@ -52,12 +52,29 @@ def time_case(n, count, dtype="f32", algo="fused", order="ring", group_size=0, i
     for _ in range(warmup):
         g.ar_execute(plan, bufs, outs=outs, workspace=ws)
     torch.cuda.synchronize()
+    run = None
+    if graph:  # the reps calls captured once into a CUDA graph: device time without host launch cost
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            cg.capture_begin()
+            for _ in range(reps):
+                g.ar_execute(plan, bufs, outs=outs, workspace=ws, stream=side)
+            cg.capture_end()
+        stream.wait_stream(side)
+        cg.replay()
+        torch.cuda.synchronize()
+        run = cg.replay
     times = []
     for _ in range(iters):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(reps):
-            g.ar_execute(plan, bufs, outs=outs, workspace=ws)
+        if run is not None:
+            run()
+        else:
+            for _ in range(reps):
+                g.ar_execute(plan, bufs, outs=outs, workspace=ws)
         b.record(stream)
         b.synchronize()
         times.append(a.elapsed_time(b) / reps)
@@ -67,9 +84,12 @@ def time_case(n, count, dtype="f32", algo="fused", order="ring", group_size=0, i
     algbw = S / (ms * 1e-3) / 1e9
     hbm = st["hbm_bytes"] / (ms * 1e-3) / 1e9
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
-    res = {"n": n, "bytes_per_rank": S, "dtype": dtype, "algo": algo, "order": order if algo == "fused" else None,
+    factor = 2 * (n - 1) / n if collective == "allreduce" else (n - 1) / n  # busbw (primer §4.8)
+    res = {"n": n, "collective": collective, "bytes_per_rank": S, "dtype": dtype, "algo": algo,
+           "order": order if algo == "fused" else None,
+           "timing": "cuda graph" if graph else "launched from python",
            "group_size": group_size or None, "us": round(ms * 1e3, 2), "algbw": round(algbw, 2),
-           "busbw": round(algbw * 2 * (n - 1) / n, 2), "steps": st["steps"], "launches": st["launches"],
+           "busbw": round(algbw * factor, 2), "steps": st["steps"], "launches": st["launches"],
            "hbm_bytes": st["hbm_bytes"], "hbm_gbs": round(hbm, 1),
            "hbm_frac": round(hbm / hbm_peak(), 4) if nbytes > 4 * l2 else None}
     del bufs, outs, ws
@@ -141,7 +161,7 @@ def time_buckets(n=8, path="fused", iters=5, warmup=2, cap_bytes=25 * MiB):
     return res
 
 
-def sweep(out=sys.stdout, max_total=64 * GiB):
+def sweep(out=sys.stdout, max_total=64 * GiB, graph=False):
     for n in (2, 4, 8, 16, 64):
         for k in range(11):
             S = KiB * 4 ** k
@@ -149,7 +169,7 @@ def sweep(out=sys.stdout, max_total=64 * GiB):
                 continue
             for algo, order in (("fused", "ring"), ("fused", "rank"), ("ring", "ring"), ("rabenseifner", "ring")):
                 iters = 10 if n * S < GiB else 5
-                res = time_case(n, S // 4, "f32", algo, order, iters=iters, warmup=3)
+                res = time_case(n, S // 4, "f32", algo, order, iters=iters, warmup=3, graph=graph)
                 print(json.dumps(res), file=out, flush=True)
 
 
@@ -161,22 +181,25 @@ def main(argv=None):
     ap.add_argument("--count", type=int, default=8 * MiB)
     ap.add_argument("--dtype", default="f32")
     ap.add_argument("--group-size", type=int, default=0)
+    ap.add_argument("--collective", default="allreduce", choices=["allreduce", "reduce_scatter", "allgather"])
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--reps", type=int, default=None)
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--graph", action="store_true", help="replay the timed calls from a CUDA graph")
     ap.add_argument("--buckets", choices=["fused", "pack"], default=None)
     a = ap.parse_args(argv)
     from gradient_sync_gb300 import build
 
     build.build()
     if a.sweep:
-        sweep()
+        sweep(graph=a.graph)
         return
     if a.buckets:
         print(json.dumps(time_buckets(path=a.buckets, iters=a.iters, warmup=min(a.warmup, 3))))
         return
-    print(json.dumps(time_case(a.n, a.count, a.dtype, a.algo, a.order, a.group_size, a.iters, a.warmup, a.reps)))
+    print(json.dumps(time_case(a.n, a.count, a.dtype, a.algo, a.order, a.group_size, a.iters, a.warmup, a.reps,
+                               graph=a.graph, collective=a.collective)))
 
 
 if __name__ == "__main__":

@@ -73,6 +73,42 @@ void build_ring(ar_plan_t* p) {
   }
 }
 
+// Standalone ring reduce-scatter (primer §4.1 table: each rank ends with S/N
+// of the sum). Rank i must end with chunk i, so rank i sends chunk
+// (i - 1 - s) mod N at step s (the slice rule of the hierarchical
+// reduce-scatter, §4.4); after N-1 steps rank i holds the complete chunk i.
+void build_ring_reduce_scatter(ar_plan_t* p) {
+  const int N = p->desc.n_ranks;
+  const int64_t L = int64_t(p->desc.count);
+  const auto b = cuts(0, L, N);
+  for (int s = 0; s <= N - 2; ++s) {
+    Step st{OP_ADD, {}};
+    const bool last = s == N - 2;
+    for (int i = 0; i < N; ++i) {
+      const int c = int(imod(i - 1 - s, N));
+      add_xfer(st, i, (i + 1) % N, b[c], b[c + 1], s == 0 ? RAW : PART, RAW, last ? RES : PART, last);
+    }
+    p->steps.push_back(st);
+  }
+}
+
+// Standalone ring all-gather: rank i contributes chunk i and sends chunk
+// (i - s) mod N at step s; the receiver overwrites. The first step reads the
+// senders' own chunks from the inputs.
+void build_ring_allgather(ar_plan_t* p) {
+  const int N = p->desc.n_ranks;
+  const int64_t L = int64_t(p->desc.count);
+  const auto b = cuts(0, L, N);
+  for (int s = 0; s <= N - 2; ++s) {
+    Step st{OP_COPY, {}};
+    for (int i = 0; i < N; ++i) {
+      const int c = int(imod(i - s, N));
+      add_xfer(st, i, (i + 1) % N, b[c], b[c + 1], s == 0 ? RAW : RES, RES, RES, false);
+    }
+    p->steps.push_back(st);
+  }
+}
+
 // Rabenseifner: recursive halving reduce-scatter, recursive doubling
 // all-gather (primer §4.3, Fig. 4.5 and Animation 4.2). Step k = 1..log2 N:
 // rank i pairs with i xor 2^(k-1), keeps the lower half of its chunk range if
@@ -184,10 +220,19 @@ void compute_stats(ar_plan_t* p) {
   st = ar_stats{};
   p->ws_stride = rup(std::max<int64_t>(L, 1), 64);
   if (d.algo == AR_FUSED) {
+    const size_t es = esize(d.dtype), NL = size_t(N) * size_t(L);
     st.steps = N > 1 ? 1 : 0;
     st.launches = (L > 0 && N > 1) ? 1 : 0;
-    st.bytes_sent_per_rank = N > 1 ? size_t(L) * esize(d.dtype) : 0;
-    st.hbm_bytes = N > 1 ? 2 * size_t(N) * size_t(L) * esize(d.dtype) : 0;
+    if (d.collective == AR_ALLREDUCE) {  // every rank reads its buffer once and writes the sum once
+      st.bytes_sent_per_rank = N > 1 ? size_t(L) * es : 0;
+      st.hbm_bytes = N > 1 ? 2 * NL * es : 0;
+    } else if (d.collective == AR_REDUCE_SCATTER) {  // N*S read, each chunk written once
+      st.bytes_sent_per_rank = N > 1 ? size_t(L) * es : 0;
+      st.hbm_bytes = N > 1 ? (NL + size_t(L)) * es : 0;
+    } else {  // each chunk read once, written to every rank
+      st.bytes_sent_per_rank = N > 1 ? ((size_t(L) + N - 1) / N) * es : 0;
+      st.hbm_bytes = N > 1 ? (size_t(L) + NL) * es : 0;
+    }
     st.workspace_bytes = 0;
     return;
   }
@@ -202,13 +247,13 @@ void compute_stats(ar_plan_t* p) {
         st.hbm_bytes += len * (space_bytes(Space(t.xs), d.dtype) + space_bytes(Space(t.ys), d.dtype) +
                                space_bytes(Space(t.ds), d.dtype));
       } else {
-        sent[t.src] += len * esize(d.dtype);
-        st.hbm_bytes += len * 2 * esize(d.dtype);
+        sent[t.src] += len * space_bytes(Space(t.xs), d.dtype);
+        st.hbm_bytes += len * (space_bytes(Space(t.xs), d.dtype) + space_bytes(Space(t.ds), d.dtype));
       }
     }
   }
   st.bytes_sent_per_rank = N > 0 ? *std::max_element(sent.begin(), sent.end()) : 0;
-  const bool uses_ws = d.dtype == AR_BF16 && N > 1;
+  const bool uses_ws = d.dtype == AR_BF16 && N > 1 && d.collective != AR_ALLGATHER;
   st.workspace_bytes = uses_ws ? size_t(N) * size_t(p->ws_stride) * 4 : 0;
 }
 
@@ -254,7 +299,7 @@ void fused_tiling(const ar_desc& d, FusedParams& fp) {
   const int N = d.n_ranks;
   const int64_t L = int64_t(d.count);
   std::vector<std::pair<int64_t, int64_t>> segs;
-  if (d.order == AR_ORDER_RING) {
+  if (d.order == AR_ORDER_RING || d.collective != AR_ALLREDUCE) {
     const auto b = cuts(0, L, N);
     for (int c = 0; c < N; ++c) segs.push_back({b[c], b[c + 1]});
   } else if (d.order == AR_ORDER_HIER) {
@@ -268,7 +313,7 @@ void fused_tiling(const ar_desc& d, FusedParams& fp) {
     segs.push_back({0, L});
   }
   const int64_t W = d.dtype == AR_BF16 ? 8 : 4;
-  const int64_t tile = fused_tile_elems(d.dtype, N, d.order);
+  const int64_t tile = fused_tile_elems(d.dtype, N, d.order, d.collective);
   int64_t tps = 1;
   for (auto& s : segs) {
     const int64_t lo = std::max(s.first, fp.e_lo), hi = std::min(s.second, fp.e_hi);
@@ -290,13 +335,14 @@ ar_status execute_fused(const ar_plan_t* p, void* const* bufs, void* const* outs
     fp.out[r] = outs ? outs[r] : bufs[r];
   }
   fp.n = d.n_ranks;
-  fp.order = d.n_ranks == 1 ? AR_ORDER_RANK : d.order;
+  fp.collective = d.collective;
+  fp.order = d.n_ranks == 1 && d.collective == AR_ALLREDUCE ? AR_ORDER_RANK : d.order;
   fp.g = d.order == AR_ORDER_HIER ? d.group_size : d.n_ranks;
   fp.m = d.order == AR_ORDER_HIER ? d.n_ranks / d.group_size : 1;
   fp.count = int64_t(d.count);
   fp.e_lo = e_lo;
   fp.e_hi = e_hi;
-  fp.scale = d.scale;
+  fp.scale = d.collective == AR_ALLGATHER ? 1.0f : d.scale;  // an all-gather only copies
   fused_tiling(d, fp);
   return from_cuda(launch_fused(fp, d.dtype, stream));
 }
@@ -316,13 +362,37 @@ ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs
   sp.scale = d.scale;
   if (N == 1) {
     const bool in_place = outs == nullptr || outs[0] == bufs[0];
-    if (in_place && d.scale == 1.0f) return AR_OK;
+    const float scale = d.collective == AR_ALLGATHER ? 1.0f : d.scale;
+    if (in_place && scale == 1.0f) return AR_OK;
+    sp.scale = scale;
     sp.n_xfer = 1;
     sp.x[0] = Transfer{0, 0, RAW, RAW, RES, 1, 0, int64_t(d.count)};
     sp.tile_start[0] = 0;
     const int64_t body = std::max<int64_t>(rdown(d.count, kStepVec), 0);
     sp.tile_start[1] = int32_t(std::max<int64_t>(1, (body + kStepTile - 1) / kStepTile));
     return from_cuda(launch_step(sp, d.dtype, OP_FINISH, sp.tile_start[1], false, stream));
+  }
+  if (d.collective == AR_ALLGATHER && outs != nullptr) {
+    // out of place: every rank's own chunk is copied to its output first (the
+    // ring delivers only the other N-1 chunks)
+    Step own{OP_COPY, {}};
+    const auto b = cuts(0, int64_t(d.count), N);
+    for (int r = 0; r < N; ++r)
+      if (outs[r] != bufs[r]) add_xfer(own, r, r, b[r], b[r + 1], RAW, RES, RES, false);
+    if (!own.xfers.empty()) {
+      sp.n_xfer = int(own.xfers.size());
+      int tiles = 0;
+      for (int x = 0; x < sp.n_xfer; ++x) {
+        const Transfer& t = own.xfers[size_t(x)];
+        sp.x[x] = t;
+        sp.tile_start[x] = tiles;
+        const int64_t body = std::max<int64_t>(rdown(t.hi, kStepVec) - rup(t.lo, kStepVec), 0);
+        tiles += int(std::max<int64_t>(1, (body + kStepTile - 1) / kStepTile));
+      }
+      sp.tile_start[sp.n_xfer] = tiles;
+      const ar_status s = from_cuda(launch_step(sp, d.dtype, OP_COPY, tiles, true, stream));
+      if (s != AR_OK) return s;
+    }
   }
   for (const Step& st : p->steps) {
     if (st.xfers.empty()) continue;
@@ -387,6 +457,11 @@ ar_status ar_plan(const ar_desc* desc, ar_plan_t** out) {
   if (d.algo < AR_RING || d.algo > AR_FUSED) return AR_EINVAL;
   if (!std::isfinite(d.scale)) return AR_EINVAL;
   if (d.count > (size_t(1) << 40)) return AR_EINVAL;
+  if (d.collective < AR_ALLREDUCE || d.collective > AR_ALLGATHER) return AR_EINVAL;
+  if (d.collective != AR_ALLREDUCE) {
+    if (d.algo != AR_RING && d.algo != AR_FUSED) return AR_EUNSUPPORTED;
+    if (d.algo == AR_FUSED && d.order == AR_ORDER_HIER) return AR_EUNSUPPORTED;
+  }
   if (d.algo == AR_RABENSEIFNER && !is_pow2(N)) return AR_EINVAL;
   if (d.algo == AR_HIER && (d.group_size < 1 || N % d.group_size != 0)) return AR_EINVAL;
   if (d.algo == AR_FUSED) {
@@ -399,7 +474,9 @@ ar_status ar_plan(const ar_desc* desc, ar_plan_t** out) {
   try {
     p->desc = d;
     if (d.algo != AR_HIER && !(d.algo == AR_FUSED && d.order == AR_ORDER_HIER)) p->desc.group_size = 0;
-    if (N > 1) {
+    if (N > 1 && d.collective == AR_REDUCE_SCATTER) build_ring_reduce_scatter(p);
+    if (N > 1 && d.collective == AR_ALLGATHER) build_ring_allgather(p);
+    if (N > 1 && d.collective == AR_ALLREDUCE) {
       if (d.algo == AR_RING) build_ring(p);
       if (d.algo == AR_RABENSEIFNER) build_rabenseifner(p);
       if (d.algo == AR_HIER) build_hier(p);
@@ -661,7 +738,7 @@ ar_status ar_bucket_allreduce(int n_ranks, void* const* tensors, const size_t* c
   if (Lb == 0) return AR_OK;
   const auto b = cuts(0, Lb, N);
   const int64_t W = dtype == AR_BF16 ? 8 : 4;
-  const int64_t tile = fused_tile_elems(dtype, N, AR_ORDER_RING);
+  const int64_t tile = fused_tile_elems(dtype, N, AR_ORDER_RING, AR_ALLREDUCE);
   const int max_group = std::min(AR_MAX_BUCKET_TENSORS, kMaxBucketPtrs / N);
   static thread_local BucketFusedParams bp;
   std::memset(&bp, 0, sizeof(bp));

@@ -39,6 +39,18 @@ namespace {
 __device__ __forceinline__ void seq_position(const FusedParams& p, int seg, int pos, int& rank,
                                              uint8_t& flag) {
   const int n = p.n;
+  if (p.collective == AR_ALLGATHER) {  // one position: chunk seg comes from its owner
+    rank = seg;
+    flag = kStart | kEnd | kFirst;
+    return;
+  }
+  if (p.collective == AR_REDUCE_SCATTER && p.order == AR_ORDER_RING) {  // fold from rank seg+1
+    int r = seg + 1 + pos;
+    while (r >= n) r -= n;
+    rank = r;
+    flag = (pos == 0 ? kStart : 0) | (pos == n - 1 ? (kEnd | kFirst) : 0);
+    return;
+  }
   if (p.order == AR_ORDER_HIER) {
     const int g = p.g, m = p.m;
     const int k = seg / m, j = seg - (seg / m) * m;
@@ -62,7 +74,7 @@ __device__ __forceinline__ void seq_position(const FusedParams& p, int seg, int 
 
 __device__ __forceinline__ void seg_range(const FusedParams& p, int seg, int64_t& lo, int64_t& hi) {
   const int64_t L = p.count;
-  if (p.order == AR_ORDER_RING) {
+  if (p.order == AR_ORDER_RING || p.collective != AR_ALLREDUCE) {  // the N chunks
     lo = seg * L / p.n;
     hi = (seg + 1) * L / p.n;
   } else if (p.order == AR_ORDER_HIER) {
@@ -88,6 +100,8 @@ __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_flat_kernel(con
   grid_dependency_wait();  // the previous kernel on the stream has finished and its writes are visible
   grid_dependents_launch();
   const int n = p.n;
+  const int nf = p.collective == AR_ALLGATHER ? 1 : n;  // ranks folded per element
+  const bool owner_only = p.collective == AR_REDUCE_SCATTER;
   if (threadIdx.x < n) s_out[threadIdx.x] = static_cast<char*>(p.out[threadIdx.x]);
   int cur = -1;
   int64_t lo = 0, hi = 0;
@@ -126,9 +140,9 @@ __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_flat_kernel(con
     if (any) {
       float acc[VPT][W];
       if (TREE) {
-        fold_tree<LV, NB>(acc[0], s_seq, n, e[0]);
+        fold_tree<LV, NB>(acc[0], s_seq, nf, e[0]);
       } else {
-        fold_sequence<LV, NB, VPT>(acc, s_seq, s_flag, n, e, ok);
+        fold_sequence<LV, NB, VPT>(acc, s_seq, s_flag, nf, e, ok);
       }
       typename LV::raw_t r[VPT];
 #pragma unroll
@@ -137,11 +151,17 @@ __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_flat_kernel(con
         for (int w = 0; w < W; ++w) acc[q][w] = fmul(acc[q][w], p.scale);
         r[q] = LV::narrow(acc[q]);
       }
-#pragma unroll 2
-      for (int d = 0; d < n; ++d)
+      if (owner_only) {  // reduce-scatter: only the chunk's owner receives it
 #pragma unroll
         for (int q = 0; q < VPT; ++q)
-          if (ok[q]) LV::store(s_out[d], e[q], r[q]);
+          if (ok[q]) LV::store(s_out[seg], e[q], r[q]);
+      } else {
+#pragma unroll 2
+        for (int d = 0; d < n; ++d)
+#pragma unroll
+          for (int q = 0; q < VPT; ++q)
+            if (ok[q]) LV::store(s_out[d], e[q], r[q]);
+      }
     }
     if (tt == 0) {  // ragged head [clo, min(a0, chi)) and tail [a1, chi)
       int64_t es = -1;
@@ -158,12 +178,15 @@ __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_flat_kernel(con
         const int64_t es1[1] = {es};
         const bool ok1[1] = {true};
         if (TREE)
-          fold_tree<LS, 8>(acc[0], s_seq, n, es);
+          fold_tree<LS, 8>(acc[0], s_seq, nf, es);
         else
-          fold_sequence<LS, 8, 1>(acc, s_seq, s_flag, n, es1, ok1);
+          fold_sequence<LS, 8, 1>(acc, s_seq, s_flag, nf, es1, ok1);
         acc[0][0] = fmul(acc[0][0], p.scale);
         const typename LS::raw_t r = LS::narrow(acc[0]);
-        for (int q = 0; q < n; ++q) LS::store(s_out[q], es, r);
+        if (owner_only)
+          LS::store(s_out[seg], es, r);
+        else
+          for (int q = 0; q < n; ++q) LS::store(s_out[q], es, r);
       }
     }
   }
@@ -278,19 +301,22 @@ cudaError_t launch_persistent(void (*kernel)(P), const P& p, int64_t tiles, cuda
 
 // Vectors per thread for N ranks: about eight 16-byte loads in flight per
 // thread whatever N is (N loads per vector).
-int fused_vpt(int n, int order) {
+// (An all-gather folds one rank per element, so it takes the most vectors.)
+int fused_vpt(int n, int order, int collective) {
+  if (collective == AR_ALLGATHER) return 4;
   if (order == AR_ORDER_TREE) return 1;
   return n <= 2 ? 4 : n <= 4 ? 2 : 1;
 }
 
-int64_t fused_tile_elems(ar_dtype dtype, int n, int order) {
-  return int64_t(kThreads) * (dtype == AR_BF16 ? 8 : 4) * fused_vpt(n, order);
+int64_t fused_tile_elems(ar_dtype dtype, int n, int order, int collective) {
+  return int64_t(kThreads) * (dtype == AR_BF16 ? 8 : 4) * fused_vpt(n, order, collective);
 }
 
 template <bool BF16>
 cudaError_t launch_fused_t(const FusedParams& p, int64_t tiles, cudaStream_t stream) {
-  if (p.order == AR_ORDER_TREE) return launch_persistent(fused_flat_kernel<BF16, true, 8, 1>, p, tiles, stream);
-  switch (fused_vpt(p.n, p.order)) {
+  if (p.order == AR_ORDER_TREE && p.collective != AR_ALLGATHER)
+    return launch_persistent(fused_flat_kernel<BF16, true, 8, 1>, p, tiles, stream);
+  switch (fused_vpt(p.n, p.order, p.collective)) {
     case 4: return launch_persistent(fused_flat_kernel<BF16, false, 2, 4>, p, tiles, stream);
     case 2: return launch_persistent(fused_flat_kernel<BF16, false, 4, 2>, p, tiles, stream);
     default: return launch_persistent(fused_flat_kernel<BF16, false, 8, 1>, p, tiles, stream);
@@ -304,7 +330,7 @@ cudaError_t launch_fused(const FusedParams& p, ar_dtype dtype, cudaStream_t stre
 
 template <bool BF16>
 cudaError_t launch_bucket_t(const BucketFusedParams& p, int64_t tiles, cudaStream_t stream) {
-  switch (fused_vpt(p.n, AR_ORDER_RING)) {
+  switch (fused_vpt(p.n, AR_ORDER_RING, AR_ALLREDUCE)) {
     case 4: return launch_persistent(fused_bucket_kernel<BF16, 2, 4>, p, tiles, stream);
     case 2: return launch_persistent(fused_bucket_kernel<BF16, 4, 2>, p, tiles, stream);
     default: return launch_persistent(fused_bucket_kernel<BF16, 8, 1>, p, tiles, stream);

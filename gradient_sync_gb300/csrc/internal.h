@@ -64,6 +64,7 @@ struct FusedParams {
   const void* in[AR_MAX_RANKS];
   void* out[AR_MAX_RANKS];
   int n;            // ranks
+  int collective;   // ar_collective
   int order;        // ar_order
   int g, m;         // hierarchical group size and group count
   int n_seg;        // segments of constant summation order
@@ -113,7 +114,7 @@ constexpr int kPackTile = kThreads * 8;                   // 2048 elements
 cudaError_t launch_step(const StepParams& p, ar_dtype dtype, StepOp op, int total_tiles, bool pdl,
                         cudaStream_t stream);
 cudaError_t launch_fused(const FusedParams& p, ar_dtype dtype, cudaStream_t stream);
-int64_t fused_tile_elems(ar_dtype dtype, int n, int order);
+int64_t fused_tile_elems(ar_dtype dtype, int n, int order, int collective);
 cudaError_t launch_bucket_fused(const BucketFusedParams& p, ar_dtype dtype, cudaStream_t stream);
 cudaError_t launch_pack(const PackParams& p, ar_dtype dtype, bool unpack, cudaStream_t stream);
 cudaError_t read_device_status(unsigned int* value, bool clear);

@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
     }
     const Transfer tr = p.x[lo_i];
     const int64_t tt = t - p.tile_start[lo_i];
-    const Operand X = operand<BF16>(p, OP == OP_COPY ? RES : tr.xs, tr.src);
+    const Operand X = operand<BF16>(p, tr.xs, tr.src);  // copies: RES, or RAW (own chunk)
     const Operand Y = operand<BF16>(p, tr.ys, tr.dst);
     const Operand D = operand<BF16>(p, OP == OP_COPY ? RES : tr.ds, tr.dst);
     const bool fin = tr.fin != 0;

@@ -65,7 +65,9 @@ typedef enum { AR_F32 = 0, AR_BF16 = 1 } ar_dtype;
  * reduction"). */
 typedef enum { AR_RING = 0, AR_RABENSEIFNER = 1, AR_HIER = 2, AR_FUSED = 3 } ar_algo;
 
-/* Per-element summation order of AR_FUSED. Floating-point addition is not
+/* Per-element summation order of AR_FUSED. (For AR_REDUCE_SCATTER,
+ * AR_ORDER_RING is the order of its ring, which folds chunk c from rank c+1:
+ * ((g_{c+1} + g_{c+2}) + ...) + g_c.) Floating-point addition is not
  * associative, so the order is part of the result (Scaling ML Systems,
  * "Collective communication": bitwise identity across algorithms is not
  * guaranteed). Each order reproduces one schedule bit for bit:
@@ -80,6 +82,23 @@ typedef enum { AR_RING = 0, AR_RABENSEIFNER = 1, AR_HIER = 2, AR_FUSED = 3 } ar_
  *                 partials folded from group j for sub-chunk j.          */
 typedef enum { AR_ORDER_RING = 0, AR_ORDER_RANK = 1, AR_ORDER_TREE = 2, AR_ORDER_HIER = 3 } ar_order;
 
+/* Which collective (primer §4.1, table of collectives; the all-reduce is a
+ * reduce-scatter followed by an all-gather).
+ *  AR_ALLREDUCE:      every rank ends with the sum of all N buffers.
+ *  AR_REDUCE_SCATTER: rank r ends with chunk r of the sum, in chunk r's range
+ *                     [floor(r*count/N), floor((r+1)*count/N)) of its output
+ *                     buffer; the other elements of that buffer are left
+ *                     unspecified (the step executor keeps partial sums there).
+ *  AR_ALLGATHER:      rank r contributes chunk r of its input buffer (its other
+ *                     elements are ignored); every rank ends with all N chunks.
+ *                     Values are copied; `scale` is ignored.
+ * Buffers keep the all-reduce's shape: count elements per rank. The
+ * reduce-scatter and all-gather run as AR_RING (N-1 steps, rank i sending
+ * chunk (i-1-s) resp. (i-s) mod N at step s, so that rank i owns chunk i) or
+ * AR_FUSED (orders RING, RANK or TREE for the reduce-scatter); the other
+ * algorithms return AR_EUNSUPPORTED. */
+typedef enum { AR_ALLREDUCE = 0, AR_REDUCE_SCATTER = 1, AR_ALLGATHER = 2 } ar_collective;
+
 typedef struct {
   int n_ranks;     /* N, 1..AR_MAX_RANKS */
   size_t count;    /* elements per rank buffer, >= 0 */
@@ -88,6 +107,7 @@ typedef struct {
   int group_size;  /* AR_HIER, AR_ORDER_HIER: G >= 1 with N % G == 0; else ignored */
   ar_order order;  /* AR_FUSED only */
   float scale;     /* multiplies the complete fp32 sum once (1.0f = plain sum) */
+  ar_collective collective; /* AR_ALLREDUCE (0) unless set */
 } ar_desc;
 
 /* Accounting of one ar_execute (primer §4.2 and §4.3 cost formulas). */

@@ -17,7 +17,8 @@ Modules:
 * ``numerics``  -- bf16 widening/narrowing, the fp64 definition of the sum,
                    and the fused single-pass sums in each declared order.
 * ``schedules`` -- step-by-step simulations of the ring, Rabenseifner and
-                   hierarchical all-reduce with per-rank mailboxes and
+                   hierarchical all-reduce, and of the standalone ring
+                   reduce-scatter and all-gather, with per-rank mailboxes and
                    byte/step counters.
 * ``buckets``   -- DDP-style bucket assignment and the bucketed gradient sync.
 
@@ -32,4 +33,4 @@ from .chunks import chunk_bounds, chunk_of  # noqa: F401
 from .numerics import (bf16_to_f32, f32_to_bf16_rne, fused_sum, reference_sum_f64,  # noqa: F401
                        abs_sum_f64)
 from .schedules import (hierarchical_allreduce, rabenseifner_allreduce,  # noqa: F401
-                        ring_allreduce, RunStats)
+                        ring_allgather, ring_allreduce, ring_reduce_scatter, RunStats)

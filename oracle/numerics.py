@@ -101,6 +101,9 @@ def fused_sum(x, order: str, idx=None, L: int | None = None, group_size: int = 0
       ((g_c + g_{c+1}) + ...) + g_{c-1}, rank indices mod N. This is the order
       in which the ring's reduce-scatter carries chunk c around the ring (the
       primer, §4.2: rank i sends chunk (i - s) mod N at step s).
+    * ``"ring_rs"``: an element of chunk c is folded starting at rank c+1:
+      ((g_{c+1} + g_{c+2}) + ...) + g_c, the order of the standalone ring
+      reduce-scatter in which rank c ends with chunk c.
     * ``"rank"``: ((g_0 + g_1) + ...) + g_{N-1} for every element.
     * ``"tree"``: a balanced binary tree over ranks in index order, the order
       of recursive halving with partners at distance 1 first (the primer,
@@ -121,12 +124,13 @@ def fused_sum(x, order: str, idx=None, L: int | None = None, group_size: int = 0
     out = np.empty(K, dtype=np.float32)
     if order == "rank":
         out[:] = _left_fold(x, list(range(N)))
-    elif order == "ring":
+    elif order in ("ring", "ring_rs"):
         c_of = chunk_of(idx, L, N)
+        first = 0 if order == "ring" else 1
         for c in range(N):
             cols = np.nonzero(c_of == c)[0]
             if cols.size:
-                out[cols] = _left_fold(x, [(c + i) % N for i in range(N)], cols)
+                out[cols] = _left_fold(x, [(c + first + i) % N for i in range(N)], cols)
     elif order == "tree":
         if N & (N - 1):
             raise ValueError("tree order needs a power-of-two rank count")

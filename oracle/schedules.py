@@ -251,6 +251,44 @@ def hierarchical_allreduce(x, group_size, idx=None, L=None, combine=_add, finish
     return w.x, w.stats
 
 
+def ring_reduce_scatter(x, idx=None, L=None, combine=_add, finish=None, server_of=None, trace=None):
+    """Standalone ring reduce-scatter: every rank ends with one chunk of the sum.
+
+    The primer's table of collectives (§4.1) defines the operation (all ranks
+    hold S, each ends with S/N of the sum, sending (N-1)/N*S) but not which
+    chunk each rank keeps. Reading taken: rank i keeps chunk i, the usual
+    assignment. On the ring that is the slice rule of the hierarchical
+    reduce-scatter (primer §4.4): at step s = 0..N-2 rank i sends chunk
+    (i - 1 - s) mod N to rank i+1, which adds its own copy. After N-1 steps
+    rank i holds the complete chunk i; its other chunks hold partial sums.
+    """
+    w = _World(x, idx, L, server_of, trace)
+    N = w.N
+    b = chunk_bounds(w.L, N)
+    if N > 1:
+        last = _ring_phase(w, [(list(range(N)), 0, w.L)], lambda p, s: p - 1 - s, True, combine,
+                           "reduce-scatter")[0]
+    else:
+        last = [0]
+    for i in range(N):
+        c = last[i]
+        w.stats.owned[i] = (b[c], b[c + 1])
+        _apply_finish(w, i, b[c], b[c + 1], finish)
+    return w.x, w.stats
+
+
+def ring_allgather(x, idx=None, L=None, server_of=None, trace=None):
+    """Standalone ring all-gather: rank i contributes chunk i of its buffer and
+    every rank ends with all N chunks (primer §4.1 table: (N-1)/N*S sent per
+    rank). Step s = 0..N-2: rank i sends chunk (i - s) mod N to rank i+1, which
+    overwrites its copy (the slice rule of the hierarchical all-gather, §4.4)."""
+    w = _World(x, idx, L, server_of, trace)
+    N = w.N
+    if N > 1:
+        _ring_phase(w, [(list(range(N)), 0, w.L)], lambda p, s: p - s, False, _add, "all-gather")
+    return w.x, w.stats
+
+
 # ----------------------------------------------------------------- helpers
 
 
@@ -270,6 +308,8 @@ def finish_bf16(scale: float = 1.0):
 
 
 SCHEDULES = {
+    "ring_reduce_scatter": ring_reduce_scatter,
+    "ring_allgather": ring_allgather,
     "ring": ring_allreduce,
     "rabenseifner": rabenseifner_allreduce,
     "hier": hierarchical_allreduce,

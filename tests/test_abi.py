@@ -182,3 +182,37 @@ def test_bucket_calls_reject(g):
         g.ar_bucket_allreduce(bad, [10, 10, 10], 0, 3, "bf16", 0.5, stream=0)  # misaligned
     with pytest.raises(g.ArError):
         g.ar_bucket_pack(ok, [10, 10, 10], 0, 3, "bf16", [0x9000000, 0], stream=0)  # null bucket
+
+
+@pytest.mark.parametrize("N,L", [(2, 5), (3, 7), (4, 4), (5, 4099), (8, 1000), (16, 50), (64, 4096)])
+@pytest.mark.parametrize("coll", ["reduce_scatter", "allgather"])
+def test_ring_collective_tables_match_oracle(g, coll, N, L):
+    plan = g.ar_plan(N, L, "f32", "ring", collective=coll)
+    fn = schedules.ring_reduce_scatter if coll == "reduce_scatter" else schedules.ring_allgather
+    st, steps = _oracle_steps(fn, N, L)
+    stats = plan.stats
+    assert stats["steps"] == st.steps == N - 1
+    for s in range(stats["steps"]):
+        op, rows = g.ar_plan_transfers(plan, s)
+        assert op == ("reduce" if coll == "reduce_scatter" else "copy")
+        assert set(rows) == steps.get(s, set()), s
+    assert stats["bytes_sent_per_rank"] == 4 * int(st.elements_sent.max())
+    assert stats["hbm_bytes"] == 4 * (st.element_reads + st.element_writes)
+
+
+def test_collective_validation(g):
+    for algo in ("rabenseifner", "hier"):
+        for coll in ("reduce_scatter", "allgather"):
+            with pytest.raises(g.ArError) as e:
+                g.ar_plan(8, 100, "f32", algo, group_size=4, collective=coll)
+            assert e.value.status == g.AR_EUNSUPPORTED
+    with pytest.raises(g.ArError) as e:
+        g.ar_plan(8, 100, "f32", "fused", group_size=4, order="hier", collective="reduce_scatter")
+    assert e.value.status == g.AR_EUNSUPPORTED
+    with pytest.raises(g.ArError) as e:
+        g.ar_plan(8, 100, "f32", "fused", collective=7)
+    assert e.value.status == g.AR_EINVAL
+    rs = g.ar_plan(16, 1 << 20, "f32", "fused", collective="reduce_scatter").stats
+    ag = g.ar_plan(16, 1 << 20, "f32", "fused", collective="allgather").stats
+    assert rs["hbm_bytes"] == (16 + 1) * (1 << 20) * 4 and ag["hbm_bytes"] == (16 + 1) * (1 << 20) * 4
+    assert g.ar_plan(16, 1 << 20, "bf16", "ring", collective="allgather").stats["workspace_bytes"] == 0

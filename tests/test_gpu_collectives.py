@@ -1,0 +1,101 @@
+"""GPU parity of the standalone reduce-scatter and all-gather (ZeRO/FSDP halves)
+against the oracle: step-by-step ring and fused single pass, fp32 and bf16, in
+place and out of place, ragged chunk boundaries."""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from _gpu import assert_bits_equal, to_device, to_host, widened
+from oracle import numerics, schedules
+from oracle.chunks import chunk_bounds
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def g():
+    from gradient_sync_gb300 import build
+
+    build.build()
+    import gradient_sync_gb300 as g
+
+    return g
+
+
+SIZES = [(1, 9), (2, 7), (3, 1000), (4, 4099), (8, 20003), (16, 100003), (64, 5000)]
+
+
+def _run(g, x, dtype, algo, coll, order="ring", scale=1.0, out_of_place=False):
+    N, L = x.shape
+    devs = [to_device(x[r], dtype) for r in range(N)]
+    outs = [torch.full_like(d, 7.0) for d in devs] if out_of_place else None
+    plan = g.ar_plan(N, L, dtype, algo, order=order, scale=scale, collective=coll)
+    ws = g.workspace_for(plan)
+    if ws is not None:
+        ws.fill_(0xFF)
+    g.ar_execute(plan, devs, outs=outs, workspace=ws)
+    torch.cuda.synchronize()
+    if out_of_place:
+        for r in range(N):
+            np.testing.assert_array_equal(to_host(devs[r], dtype), x[r])
+    return [to_host(t, dtype) for t in (outs if out_of_place else devs)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("algo,order", [("ring", "ring"), ("fused", "ring"), ("fused", "rank"), ("fused", "tree")])
+@pytest.mark.parametrize("N,L", SIZES)
+def test_reduce_scatter(g, dtype, algo, order, N, L):
+    if order == "tree" and N & (N - 1):
+        pytest.skip("tree order needs a power-of-two rank count")
+    scale = 0.25 if L % 2 else 1.0
+    x = workloads.all_ranks(workloads.small_spec(N, L, dtype, "normal", seed=N + 3 * L))
+    got = _run(g, x, dtype, algo, "reduce_scatter", order, scale, out_of_place=(N % 2 == 0))
+    xf = widened(x, dtype)
+    if algo == "ring":
+        finish = schedules.finish_bf16(scale) if dtype == "bf16" else schedules.finish_scale(scale)
+        out, _ = schedules.ring_reduce_scatter(xf, finish=finish)
+        want_rows = [numerics.f32_to_bf16_rne(out[r]) if dtype == "bf16" else out[r] for r in range(N)]
+    else:
+        s = numerics.fused_sum(xf, "ring_rs" if order == "ring" else order, scale=scale)
+        w = numerics.f32_to_bf16_rne(s) if dtype == "bf16" else s
+        want_rows = [w] * N
+    b = chunk_bounds(L, N)
+    for r in range(N):
+        seg = slice(b[r], b[r + 1])
+        assert_bits_equal(got[r][seg], want_rows[r][seg], f"rank {r}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("algo", ["ring", "fused"])
+@pytest.mark.parametrize("N,L", SIZES)
+@pytest.mark.parametrize("out_of_place", [False, True])
+def test_allgather(g, dtype, algo, N, L, out_of_place):
+    x = workloads.all_ranks(workloads.small_spec(N, L, dtype, "uniform", seed=N * 5 + L))
+    got = _run(g, x, dtype, algo, "allgather", scale=3.0, out_of_place=out_of_place)  # scale is ignored
+    want, _ = schedules.ring_allgather(x)
+    b = chunk_bounds(L, N)
+    assert np.array_equal(want[0], np.concatenate([x[c, b[c]:b[c + 1]] for c in range(N)]))
+    for r in range(N):
+        assert_bits_equal(got[r], want[r], f"rank {r}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_reduce_scatter_then_allgather_equals_allreduce(g, dtype):
+    """The two halves in sequence give the all-reduce in the order of one
+    hierarchical group of N, bit for bit (primer §4.1)."""
+    N, L = 16, 1 << 20
+    x = workloads.all_ranks(workloads.small_spec(N, L, dtype, "normal", seed=77))
+    devs = [to_device(x[r], dtype) for r in range(N)]
+    rs = g.ar_plan(N, L, dtype, "ring", collective="reduce_scatter")
+    ag = g.ar_plan(N, L, dtype, "ring", collective="allgather")
+    g.ar_execute(rs, devs, workspace=g.workspace_for(rs))
+    g.ar_execute(ag, devs)
+    torch.cuda.synchronize()
+    plan = g.ar_plan(N, L, dtype, "fused", order="hier", group_size=N)
+    ref = [to_device(x[r], dtype) for r in range(N)]
+    g.ar_execute(plan, ref)
+    torch.cuda.synchronize()
+    for r in (0, 9):
+        assert_bits_equal(to_host(devs[r], dtype), to_host(ref[r], dtype), f"rank {r}")
