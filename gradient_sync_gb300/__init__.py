@@ -16,13 +16,15 @@ from . import _lib
 # ---- enums of include/ar.h
 AR_OK, AR_EINVAL, AR_EUNSUPPORTED, AR_ENOMEM, AR_ECUDA, AR_ETIMEOUT = range(6)
 AR_F32, AR_BF16 = 0, 1
-AR_RING, AR_RABENSEIFNER, AR_HIER, AR_FUSED = 0, 1, 2, 3
+AR_RING, AR_RABENSEIFNER, AR_HIER, AR_FUSED, AR_AUTO = 0, 1, 2, 3, 4
 AR_ORDER_RING, AR_ORDER_RANK, AR_ORDER_TREE, AR_ORDER_HIER = 0, 1, 2, 3
 AR_ALLREDUCE, AR_REDUCE_SCATTER, AR_ALLGATHER = 0, 1, 2
 AR_MAX_RANKS = 64
 AR_MAX_BUCKET_TENSORS = 32
 
-ALGOS = {"ring": AR_RING, "rabenseifner": AR_RABENSEIFNER, "hier": AR_HIER, "fused": AR_FUSED}
+ALGOS = {"ring": AR_RING, "rabenseifner": AR_RABENSEIFNER, "hier": AR_HIER, "fused": AR_FUSED, "auto": AR_AUTO}
+ALGO_NAMES = {v: k for k, v in ALGOS.items()}
+AR_DEVICE_ALPHA_S, AR_DEVICE_BW = 1.5e-6, 6.0e12
 ORDERS = {"ring": AR_ORDER_RING, "rank": AR_ORDER_RANK, "tree": AR_ORDER_TREE, "hier": AR_ORDER_HIER}
 DTYPES = {"f32": AR_F32, "bf16": AR_BF16}
 COLLECTIVES = {"allreduce": AR_ALLREDUCE, "reduce_scatter": AR_REDUCE_SCATTER, "allgather": AR_ALLGATHER}
@@ -94,6 +96,36 @@ def ar_plan(n_ranks: int, count: int, dtype="f32", algo="fused", group_size: int
     _check(_lib.load().ar_plan(d, h), "ar_plan")
     return Plan(h.value, dict(n_ranks=n_ranks, count=count, dtype=dtype, algo=algo,
                               group_size=group_size, order=order, scale=scale, collective=collective))
+
+
+def ar_plan_desc(plan: Plan) -> dict:
+    """The plan's descriptor as the library holds it (AR_AUTO resolved)."""
+    d = _lib.ArDesc()
+    _check(_lib.load().ar_plan_desc(plan.handle, d), "ar_plan_desc")
+    return {"n_ranks": d.n_ranks, "count": d.count, "dtype": d.dtype, "algo": ALGO_NAMES.get(d.algo, d.algo),
+            "group_size": d.group_size, "order": d.order, "scale": d.scale, "collective": d.collective}
+
+
+def fabric(alpha, bw_local, bw_net=None, ranks_per_server=0, in_network=False, shared_memory=False):
+    """An ar_fabric: seconds per round, bytes/s inside and between servers."""
+    return _lib.ArFabric(float(alpha), float(bw_local), float(bw_net if bw_net is not None else bw_local),
+                         int(ranks_per_server), int(bool(in_network)), int(bool(shared_memory)))
+
+
+def ar_plan_predict(plan: Plan, fab) -> float:
+    """Predicted seconds of one ar_execute of the plan on a fabric (round model)."""
+    t = ctypes.c_double()
+    _check(_lib.load().ar_plan_predict(plan.handle, fab, t), "ar_plan_predict")
+    return t.value
+
+
+def ar_select(n_ranks, count, fab, dtype="f32", order="ring", scale=1.0, collective="allreduce"):
+    """(algorithm name, group size, predicted seconds) of the fastest algorithm on a fabric."""
+    d = _lib.ArDesc(int(n_ranks), int(count), DTYPES.get(dtype, dtype), AR_FUSED, 0, ORDERS.get(order, order),
+                    float(scale), COLLECTIVES.get(collective, collective))
+    a, gs, t = _lib.c_int(), _lib.c_int(), ctypes.c_double()
+    _check(_lib.load().ar_select(d, fab, a, gs, t), "ar_select")
+    return ALGO_NAMES[a.value], gs.value, t.value
 
 
 def ar_plan_stats(plan: Plan) -> dict:

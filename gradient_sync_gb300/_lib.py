@@ -23,6 +23,11 @@ class ArStats(ctypes.Structure):
                 ("hbm_bytes", c_size_t), ("workspace_bytes", c_size_t)]
 
 
+class ArFabric(ctypes.Structure):
+    _fields_ = [("alpha", ctypes.c_double), ("bw_local", ctypes.c_double), ("bw_net", ctypes.c_double),
+                ("ranks_per_server", c_int), ("in_network", c_int), ("shared_memory", c_int)]
+
+
 # name -> (restype, argtypes), in the order of include/ar.h
 SIGNATURES = {
     "ar_plan": (c_int, [ctypes.POINTER(ArDesc), ctypes.POINTER(c_void_p)]),
@@ -32,6 +37,9 @@ SIGNATURES = {
     "ar_execute_host": (c_int, [c_void_p, VOIDPP, VOIDPP, VOIDPP, c_void_p, c_void_p]),
     "ar_execute_noalloc": (c_int, [c_void_p, VOIDPP, VOIDPP, c_void_p]),
     "ar_plan_destroy": (None, [c_void_p]),
+    "ar_plan_predict": (c_int, [c_void_p, ctypes.POINTER(ArFabric), ctypes.POINTER(ctypes.c_double)]),
+    "ar_select": (c_int, [ctypes.POINTER(ArDesc), ctypes.POINTER(ArFabric), INTP, INTP,
+                          ctypes.POINTER(ctypes.c_double)]),
     "ar_plan_transfers": (c_int, [c_void_p, c_int, INTP, INTP, ctypes.POINTER(ctypes.c_int64), c_int]),
     "ar_bucket_plan": (c_int, [SIZEP, c_int, c_size_t, c_size_t, INTP, INTP]),
     "ar_bucket_pack": (c_int, [c_int, VOIDPP, SIZEP, c_int, c_int, c_int, c_int, VOIDPP, c_void_p]),

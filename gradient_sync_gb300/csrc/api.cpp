@@ -454,6 +454,16 @@ ar_status ar_plan(const ar_desc* desc, ar_plan_t** out) {
   const int N = d.n_ranks;
   if (N < 1 || N > AR_MAX_RANKS) return AR_EINVAL;
   if (d.dtype != AR_F32 && d.dtype != AR_BF16) return AR_EINVAL;
+  if (d.algo == AR_AUTO) {  // resolve under this GPU's own fabric, then plan the choice
+    const ar_fabric dev = {AR_DEVICE_ALPHA_S, AR_DEVICE_BW, AR_DEVICE_BW, 0, 0, 1};
+    ar_desc r = d;
+    r.algo = AR_FUSED;
+    int gs = 0;
+    const ar_status s = ar_select(&d, &dev, &r.algo, &gs, nullptr);
+    if (s != AR_OK) return s;
+    if (r.algo == AR_HIER) r.group_size = gs;
+    return ar_plan(&r, out);
+  }
   if (d.algo < AR_RING || d.algo > AR_FUSED) return AR_EINVAL;
   if (!std::isfinite(d.scale)) return AR_EINVAL;
   if (d.count > (size_t(1) << 40)) return AR_EINVAL;
@@ -623,6 +633,86 @@ ar_status ar_execute_host(const ar_plan_t* plan, const void* const* host_in, voi
         return AR_ECUDA;
   }
   return from_cuda(cudaStreamSynchronize(hp->d2h));
+}
+
+// ---------------------------------------------------------------- cost model
+
+static bool fabric_ok(const ar_fabric* f) {
+  auto pos = [](double x) { return std::isfinite(x) && x > 0; };
+  return f != nullptr && std::isfinite(f->alpha) && f->alpha >= 0 && pos(f->bw_local) &&
+         (f->shared_memory || pos(f->bw_net)) && f->ranks_per_server >= 0;
+}
+
+ar_status ar_plan_predict(const ar_plan_t* plan, const ar_fabric* f, double* seconds) {
+  if (plan == nullptr || seconds == nullptr || !fabric_ok(f)) return AR_EINVAL;
+  const ar_desc& d = plan->desc;
+  const ar_stats& st = plan->stats;
+  const int N = d.n_ranks, rps = f->ranks_per_server;
+  if (f->shared_memory) {  // one memory for all ranks: each launch, then all its bytes
+    *seconds = st.launches * f->alpha + double(st.hbm_bytes) / f->bw_local;
+    return AR_OK;
+  }
+  if (d.algo == AR_FUSED) {
+    if (!f->in_network) return AR_EUNSUPPORTED;
+    const bool multi = rps > 0 && N > rps;
+    // one round: a rank sends its whole buffer up (reduce-scatter, all-reduce)
+    // or receives the whole result (all-gather, all-reduce)
+    *seconds = N > 1 ? f->alpha + double(d.count) * esize(d.dtype) / (multi ? f->bw_net : f->bw_local) : 0.0;
+    return AR_OK;
+  }
+  auto bw = [&](int a, int b) {
+    return (rps == 0 || a / rps == b / rps) ? f->bw_local : f->bw_net;
+  };
+  double T = 0;
+  for (const Step& s : plan->steps) {
+    double worst = 0;
+    for (const Transfer& t : s.xfers) {
+      const double bytes = double(t.hi - t.lo) * space_bytes(Space(t.xs), d.dtype);
+      worst = std::max(worst, bytes / bw(t.src, t.dst));
+    }
+    T += f->alpha + worst;
+  }
+  *seconds = T;
+  return AR_OK;
+}
+
+ar_status ar_select(const ar_desc* desc, const ar_fabric* f, ar_algo* algo, int* group_size,
+                    double* seconds) {
+  if (desc == nullptr || algo == nullptr || !fabric_ok(f)) return AR_EINVAL;
+  const int N = desc->n_ranks;
+  std::vector<std::pair<ar_algo, int>> cand = {{AR_RING, 0}};
+  if (desc->collective == AR_ALLREDUCE) {
+    if (is_pow2(N)) cand.push_back({AR_RABENSEIFNER, 0});
+    const int G = f->ranks_per_server;
+    if (G > 1 && G < N && N % G == 0) cand.push_back({AR_HIER, G});
+  }
+  if (f->in_network || f->shared_memory) cand.push_back({AR_FUSED, 0});
+  bool found = false;
+  double best = 0;
+  ar_status last = AR_EINVAL;
+  for (const auto& c : cand) {
+    ar_desc d = *desc;
+    d.algo = c.first;
+    if (c.first == AR_HIER) d.group_size = c.second;
+    if (c.first == AR_FUSED && d.order == AR_ORDER_HIER && d.collective != AR_ALLREDUCE) d.order = AR_ORDER_RING;
+    ar_plan_t* p = nullptr;
+    last = ar_plan(&d, &p);
+    if (last != AR_OK) continue;
+    double t = 0;
+    last = ar_plan_predict(p, f, &t);
+    const int gs = p->desc.group_size;
+    ar_plan_destroy(p);
+    if (last != AR_OK) continue;
+    if (!found || t < best) {
+      found = true;
+      best = t;
+      *algo = c.first;
+      if (group_size) *group_size = gs;
+    }
+  }
+  if (!found) return last;
+  if (seconds) *seconds = best;
+  return AR_OK;
 }
 
 // ---------------------------------------------------------------- buckets

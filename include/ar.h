@@ -63,7 +63,15 @@ typedef enum { AR_F32 = 0, AR_BF16 = 1 } ar_dtype;
  * of every rank is read once and written once, the traffic of a rank that
  * sends its buffer once and receives the sum once (primer §4.4, "In-network
  * reduction"). */
-typedef enum { AR_RING = 0, AR_RABENSEIFNER = 1, AR_HIER = 2, AR_FUSED = 3 } ar_algo;
+typedef enum { AR_RING = 0, AR_RABENSEIFNER = 1, AR_HIER = 2, AR_FUSED = 3, AR_AUTO = 4 } ar_algo;
+/* AR_AUTO: ar_plan picks the algorithm with ar_select under this GPU's own
+ * fabric (virtual ranks in one HBM: every step costs AR_DEVICE_ALPHA_S plus
+ * its HBM bytes at AR_DEVICE_BW, both measured on GB300) and records the
+ * choice in the plan's descriptor (ar_plan_desc). With one shared memory the
+ * single pass always moves the fewest bytes in the fewest steps, so AR_AUTO
+ * resolves to AR_FUSED. */
+#define AR_DEVICE_ALPHA_S 1.5e-6 /* per dependent kernel launch, graph-replayed */
+#define AR_DEVICE_BW 6.0e12      /* bytes/s of algorithmic HBM traffic */
 
 /* Per-element summation order of AR_FUSED. (For AR_REDUCE_SCATTER,
  * AR_ORDER_RING is the order of its ring, which folds chunk c from rank c+1:
@@ -131,8 +139,8 @@ typedef struct ar_plan ar_plan_t;
 /* Validate `desc` and build the schedule's step tables on the host (no GPU
  * call). Errors (AR_EINVAL): desc or out NULL; n_ranks outside
  * 1..AR_MAX_RANKS; unknown dtype/algo/order; AR_RABENSEIFNER or
- * AR_ORDER_TREE with N not a power of two (primer §4.3: "N must be a power of
- * two"); AR_HIER or AR_ORDER_HIER with group_size < 1 or N % group_size != 0;
+ * AR_ORDER_TREE with N not a power of two (primer §4.3: Rabenseifner needs a
+ * power-of-two N); AR_HIER or AR_ORDER_HIER with group_size < 1 or N % group_size != 0;
  * scale not finite. AR_ENOMEM if the host tables cannot be allocated. On
  * success *out owns the tables until ar_plan_destroy. */
 ar_status ar_plan(const ar_desc* desc, ar_plan_t** out);
@@ -209,6 +217,45 @@ ar_status ar_execute_host(const ar_plan_t* plan, const void* const* host_in, voi
 ar_status ar_execute_noalloc(const ar_plan_t* plan, void* const* bufs, void* const* outs, void* stream);
 
 void ar_plan_destroy(ar_plan_t* plan);
+
+/* ---------------------------------------------------------------- cost model
+ * The primer's alpha-beta model (§4.3: T = alpha * dependent steps + bytes /
+ * B) evaluated as the AI Infra Book's round model (ch. 7, §7.1.2 and §7.2.1:
+ * rounds run one after another, transfers inside a round in parallel on
+ * their own links, T = sum over rounds of (alpha + max over the round's
+ * transfers of bytes / B_link)), over the plan's own step tables. */
+typedef struct {
+  double alpha;          /* seconds per dependent step (round) */
+  double bw_local;       /* bytes/s of a rank's link to a rank in the same server */
+  double bw_net;         /* bytes/s of a rank's link to a rank in another server */
+  int ranks_per_server;  /* r and r' share a server iff r/ranks_per_server ==
+                            r'/ranks_per_server; 0 = all ranks in one server */
+  int in_network;        /* 1: switches reduce in flight, so AR_FUSED runs as
+                            in-network reduction: one round in which every rank
+                            sends its buffer once and receives the result once
+                            (primer §4.4) */
+  int shared_memory;     /* 1: all ranks share one memory of bandwidth bw_local
+                            (virtual ranks on one GPU): a step costs alpha plus
+                            its algorithmic memory bytes / bw_local */
+} ar_fabric;
+
+/* Predicted seconds of one ar_execute of `plan` on `fabric`. Transfer bytes
+ * are the payload as stored (fp32 partial sums 4 bytes, bf16 values 2).
+ * AR_EINVAL: NULL pointers, alpha < 0, a bandwidth <= 0 or not finite.
+ * AR_EUNSUPPORTED: an AR_FUSED plan on a fabric that neither reduces in the
+ * network nor shares memory. */
+ar_status ar_plan_predict(const ar_plan_t* plan, const ar_fabric* fabric, double* seconds);
+
+/* The algorithm with the smallest predicted time for `desc` on `fabric`
+ * among AR_RING, AR_RABENSEIFNER (N a power of two), AR_HIER with
+ * group_size = ranks_per_server (when that divides N and lies strictly
+ * between 1 and N) and AR_FUSED (in-network or shared memory); only AR_RING
+ * and AR_FUSED for a reduce-scatter or all-gather. desc->algo is ignored.
+ * Writes the choice to *algo (and its group size to *group_size if not NULL)
+ * and its predicted time to *seconds (if not NULL). The choice NCCL makes per
+ * call from its tables (primer §4.5), here from the model. */
+ar_status ar_select(const ar_desc* desc, const ar_fabric* fabric, ar_algo* algo, int* group_size,
+                    double* seconds);
 
 /* Introspection of a step plan's schedule (host only). For step `step`
  * (0 <= step < ar_stats.steps), writes *op (0 = reduce: the receiver adds,
