@@ -87,15 +87,15 @@ class Plan:
 
 
 def ar_plan(n_ranks: int, count: int, dtype="f32", algo="fused", group_size: int = 0, order="ring",
-            scale: float = 1.0, collective="allreduce") -> Plan:
+            scale: float = 1.0, collective="allreduce", sm_budget: int = 0) -> Plan:
     """Validate the descriptor and build the schedule (host only)."""
     d = _lib.ArDesc(int(n_ranks), int(count), DTYPES.get(dtype, dtype), ALGOS.get(algo, algo),
                     int(group_size), ORDERS.get(order, order), float(scale),
-                    COLLECTIVES.get(collective, collective))
+                    COLLECTIVES.get(collective, collective), int(sm_budget))
     h = _lib.c_void_p()
     _check(_lib.load().ar_plan(d, h), "ar_plan")
-    return Plan(h.value, dict(n_ranks=n_ranks, count=count, dtype=dtype, algo=algo,
-                              group_size=group_size, order=order, scale=scale, collective=collective))
+    return Plan(h.value, dict(n_ranks=n_ranks, count=count, dtype=dtype, algo=algo, group_size=group_size,
+                              order=order, scale=scale, collective=collective, sm_budget=sm_budget))
 
 
 def ar_plan_desc(plan: Plan) -> dict:
@@ -103,7 +103,8 @@ def ar_plan_desc(plan: Plan) -> dict:
     d = _lib.ArDesc()
     _check(_lib.load().ar_plan_desc(plan.handle, d), "ar_plan_desc")
     return {"n_ranks": d.n_ranks, "count": d.count, "dtype": d.dtype, "algo": ALGO_NAMES.get(d.algo, d.algo),
-            "group_size": d.group_size, "order": d.order, "scale": d.scale, "collective": d.collective}
+            "group_size": d.group_size, "order": d.order, "scale": d.scale, "collective": d.collective,
+            "sm_budget": d.sm_budget}
 
 
 def fabric(alpha, bw_local, bw_net=None, ranks_per_server=0, in_network=False, shared_memory=False):
@@ -122,7 +123,7 @@ def ar_plan_predict(plan: Plan, fab) -> float:
 def ar_select(n_ranks, count, fab, dtype="f32", order="ring", scale=1.0, collective="allreduce"):
     """(algorithm name, group size, predicted seconds) of the fastest algorithm on a fabric."""
     d = _lib.ArDesc(int(n_ranks), int(count), DTYPES.get(dtype, dtype), AR_FUSED, 0, ORDERS.get(order, order),
-                    float(scale), COLLECTIVES.get(collective, collective))
+                    float(scale), COLLECTIVES.get(collective, collective), 0)
     a, gs, t = _lib.c_int(), _lib.c_int(), ctypes.c_double()
     _check(_lib.load().ar_select(d, fab, a, gs, t), "ar_select")
     return ALGO_NAMES[a.value], gs.value, t.value
@@ -226,10 +227,11 @@ def ar_bucket_unpack(bucket, scale: float, out_dtype, tensors, counts, t_begin: 
                                         ptrs, cnt, nt, t_begin, t_end, _stream(stream)), "ar_bucket_unpack")
 
 
-def ar_bucket_allreduce(tensors, counts, t_begin: int, t_end: int, dtype, scale: float, stream=None):
+def ar_bucket_allreduce(tensors, counts, t_begin: int, t_end: int, dtype, scale: float, stream=None,
+                        sm_budget: int = 0):
     n, ptrs, cnt, nt = _marshal(tensors, counts)
     _check(_lib.load().ar_bucket_allreduce(n, ptrs, cnt, nt, t_begin, t_end, DTYPES.get(dtype, dtype),
-                                           float(scale), _stream(stream)), "ar_bucket_allreduce")
+                                           float(scale), int(sm_budget), _stream(stream)), "ar_bucket_allreduce")
 
 
 # ---------------------------------------------------------------- status

@@ -3,6 +3,7 @@
     python -m gradient_sync_gb300.cases --algo fused --order ring --n 16 --count 8388608 --iters 3
     python -m gradient_sync_gb300.cases --sweep > sweep.jsonl
     python -m gradient_sync_gb300.cases --buckets fused|pack --iters 5
+    python -m gradient_sync_gb300.cases --overlap --n 8 --tokens 4096 --sm-budget 32 --iters 5
 
 Each timed case prints one JSON line: time per call (median of CUDA-event
 timings on the launching stream, after warm-up), algbw = S/T, busbw =
@@ -188,6 +189,9 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--graph", action="store_true", help="replay the timed calls from a CUDA graph")
     ap.add_argument("--buckets", choices=["fused", "pack"], default=None)
+    ap.add_argument("--overlap", action="store_true", help="bucketed sync overlapped with a synthetic backward")
+    ap.add_argument("--tokens", type=int, default=4096)
+    ap.add_argument("--sm-budget", type=int, default=0)
     a = ap.parse_args(argv)
     from gradient_sync_gb300 import build
 
@@ -197,6 +201,12 @@ def main(argv=None):
         return
     if a.buckets:
         print(json.dumps(time_buckets(path=a.buckets, iters=a.iters, warmup=min(a.warmup, 3))))
+        return
+    if a.overlap:
+        from gradient_sync_gb300.overlap import time_overlap
+
+        print(json.dumps(time_overlap(n_ranks=a.n, tokens=a.tokens, sm_budget=a.sm_budget, iters=a.iters,
+                                      warmup=min(a.warmup, 3))))
         return
     print(json.dumps(time_case(a.n, a.count, a.dtype, a.algo, a.order, a.group_size, a.iters, a.warmup, a.reps,
                                graph=a.graph, collective=a.collective)))

@@ -344,7 +344,7 @@ ar_status execute_fused(const ar_plan_t* p, void* const* bufs, void* const* outs
   fp.e_hi = e_hi;
   fp.scale = d.collective == AR_ALLGATHER ? 1.0f : d.scale;  // an all-gather only copies
   fused_tiling(d, fp);
-  return from_cuda(launch_fused(fp, d.dtype, stream));
+  return from_cuda(launch_fused(fp, d.dtype, d.sm_budget, stream));
 }
 
 ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs, void* workspace,
@@ -370,7 +370,7 @@ ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs
     sp.tile_start[0] = 0;
     const int64_t body = std::max<int64_t>(rdown(d.count, kStepVec), 0);
     sp.tile_start[1] = int32_t(std::max<int64_t>(1, (body + kStepTile - 1) / kStepTile));
-    return from_cuda(launch_step(sp, d.dtype, OP_FINISH, sp.tile_start[1], false, stream));
+    return from_cuda(launch_step(sp, d.dtype, OP_FINISH, sp.tile_start[1], false, d.sm_budget, stream));
   }
   if (d.collective == AR_ALLGATHER && outs != nullptr) {
     // out of place: every rank's own chunk is copied to its output first (the
@@ -390,7 +390,7 @@ ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs
         tiles += int(std::max<int64_t>(1, (body + kStepTile - 1) / kStepTile));
       }
       sp.tile_start[sp.n_xfer] = tiles;
-      const ar_status s = from_cuda(launch_step(sp, d.dtype, OP_COPY, tiles, true, stream));
+      const ar_status s = from_cuda(launch_step(sp, d.dtype, OP_COPY, tiles, true, d.sm_budget, stream));
       if (s != AR_OK) return s;
     }
   }
@@ -406,7 +406,7 @@ ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs
       tiles += int(std::max<int64_t>(1, (body + kStepTile - 1) / kStepTile));
     }
     sp.tile_start[sp.n_xfer] = tiles;
-    const ar_status s = from_cuda(launch_step(sp, d.dtype, st.op, tiles, true, stream));
+    const ar_status s = from_cuda(launch_step(sp, d.dtype, st.op, tiles, true, d.sm_budget, stream));
     if (s != AR_OK) return s;
   }
   return AR_OK;
@@ -468,6 +468,7 @@ ar_status ar_plan(const ar_desc* desc, ar_plan_t** out) {
   if (!std::isfinite(d.scale)) return AR_EINVAL;
   if (d.count > (size_t(1) << 40)) return AR_EINVAL;
   if (d.collective < AR_ALLREDUCE || d.collective > AR_ALLGATHER) return AR_EINVAL;
+  if (d.sm_budget < 0) return AR_EINVAL;
   if (d.collective != AR_ALLREDUCE) {
     if (d.algo != AR_RING && d.algo != AR_FUSED) return AR_EUNSUPPORTED;
     if (d.algo == AR_FUSED && d.order == AR_ORDER_HIER) return AR_EUNSUPPORTED;
@@ -816,11 +817,12 @@ ar_status ar_bucket_unpack(int n_ranks, const void* const* bucket, float scale, 
 }
 
 ar_status ar_bucket_allreduce(int n_ranks, void* const* tensors, const size_t* counts, int n_tensors,
-                              int t_begin, int t_end, ar_dtype dtype, float scale, void* stream) {
+                              int t_begin, int t_end, ar_dtype dtype, float scale, int sm_budget,
+                              void* stream) {
   ar_status s = check_bucket_args(n_ranks, tensors, counts, n_tensors, t_begin, t_end);
   if (s != AR_OK) return s;
   if (dtype != AR_F32 && dtype != AR_BF16) return AR_EINVAL;
-  if (!std::isfinite(scale)) return AR_EINVAL;
+  if (!std::isfinite(scale) || sm_budget < 0) return AR_EINVAL;
   const int N = n_ranks;
   const auto off = packed_offsets(counts, t_begin, t_end);
   int64_t Lb = 0;
@@ -841,7 +843,7 @@ ar_status ar_bucket_allreduce(int n_ranks, void* const* tensors, const size_t* c
     bp.n = N;
     bp.scale = scale;
     bp.tile_start[bp.n_seg] = tiles;
-    const cudaError_t e = launch_bucket_fused(bp, dtype, static_cast<cudaStream_t>(stream));
+    const cudaError_t e = launch_bucket_fused(bp, dtype, sm_budget, static_cast<cudaStream_t>(stream));
     std::memset(&bp, 0, sizeof(bp));
     nt = 0;
     tiles = 0;

@@ -230,34 +230,40 @@ __device__ __forceinline__ void fold_tree(float (&acc)[L::W], const char* const*
 // ---------------------------------------------------------------------------
 // Host side: persistent grids. A kernel gets min(tiles, resident CTAs) blocks,
 // where resident = CTAs per SM at kThreads threads (occupancy calculator)
-// times the SM count, so the grid is a whole number of waves over all SMs.
-// Cached per (device, kernel).
+// times the SM count (or the caller's SM budget, if smaller), so the grid is
+// a whole number of waves over the SMs it may use. Cached per (device, kernel).
 // ---------------------------------------------------------------------------
-inline int persistent_grid(const void* kernel, int64_t tiles) {
+inline int persistent_grid(const void* kernel, int64_t tiles, int sm_budget = 0) {
   struct Entry {
     int device;
     const void* kernel;
-    int blocks;
+    int per_sm;
+    int sms;
   };
   static std::mutex mu;
   static std::vector<Entry> cache;
   int dev = 0;
   cudaGetDevice(&dev);
-  int blocks = 0;
+  int per_sm = 0, sms = 0;
   {
     std::lock_guard<std::mutex> lock(mu);
     for (const Entry& e : cache)
-      if (e.device == dev && e.kernel == kernel) blocks = e.blocks;
+      if (e.device == dev && e.kernel == kernel) {
+        per_sm = e.per_sm;
+        sms = e.sms;
+      }
   }
-  if (blocks == 0) {
-    int sms = 0, per_sm = 0;
+  if (per_sm == 0) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess)
       per_sm = 1;
-    blocks = (sms > 0 ? sms : 1) * (per_sm > 0 ? per_sm : 1);
+    if (sms <= 0) sms = 1;
+    if (per_sm <= 0) per_sm = 1;
     std::lock_guard<std::mutex> lock(mu);
-    cache.push_back({dev, kernel, blocks});
+    cache.push_back({dev, kernel, per_sm, sms});
   }
+  const int use = (sm_budget > 0 && sm_budget < sms) ? sm_budget : sms;
+  const int64_t blocks = int64_t(per_sm) * use;
   return int(tiles < blocks ? tiles : blocks);
 }
 

@@ -283,10 +283,10 @@ __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB)
 // while the previous kernel on the stream drains, and waits for it
 // (griddepcontrol.wait) before touching memory, so stream order holds.
 template <class P>
-cudaError_t launch_persistent(void (*kernel)(P), const P& p, int64_t tiles, cudaStream_t stream) {
+cudaError_t launch_persistent(void (*kernel)(P), const P& p, int64_t tiles, int sm_budget, cudaStream_t stream) {
   if (tiles <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(persistent_grid(reinterpret_cast<const void*>(kernel), tiles));
+  cfg.gridDim = dim3(persistent_grid(reinterpret_cast<const void*>(kernel), tiles, sm_budget));
   cfg.blockDim = dim3(kThreads);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -313,33 +313,35 @@ int64_t fused_tile_elems(ar_dtype dtype, int n, int order, int collective) {
 }
 
 template <bool BF16>
-cudaError_t launch_fused_t(const FusedParams& p, int64_t tiles, cudaStream_t stream) {
+cudaError_t launch_fused_t(const FusedParams& p, int64_t tiles, int sm_budget, cudaStream_t stream) {
   if (p.order == AR_ORDER_TREE && p.collective != AR_ALLGATHER)
-    return launch_persistent(fused_flat_kernel<BF16, true, 8, 1>, p, tiles, stream);
+    return launch_persistent(fused_flat_kernel<BF16, true, 8, 1>, p, tiles, sm_budget, stream);
   switch (fused_vpt(p.n, p.order, p.collective)) {
-    case 4: return launch_persistent(fused_flat_kernel<BF16, false, 2, 4>, p, tiles, stream);
-    case 2: return launch_persistent(fused_flat_kernel<BF16, false, 4, 2>, p, tiles, stream);
-    default: return launch_persistent(fused_flat_kernel<BF16, false, 8, 1>, p, tiles, stream);
+    case 4: return launch_persistent(fused_flat_kernel<BF16, false, 2, 4>, p, tiles, sm_budget, stream);
+    case 2: return launch_persistent(fused_flat_kernel<BF16, false, 4, 2>, p, tiles, sm_budget, stream);
+    default: return launch_persistent(fused_flat_kernel<BF16, false, 8, 1>, p, tiles, sm_budget, stream);
   }
 }
 
-cudaError_t launch_fused(const FusedParams& p, ar_dtype dtype, cudaStream_t stream) {
+cudaError_t launch_fused(const FusedParams& p, ar_dtype dtype, int sm_budget, cudaStream_t stream) {
   const int64_t tiles = int64_t(p.n_seg) * p.tiles_per_seg;
-  return dtype == AR_BF16 ? launch_fused_t<true>(p, tiles, stream) : launch_fused_t<false>(p, tiles, stream);
+  return dtype == AR_BF16 ? launch_fused_t<true>(p, tiles, sm_budget, stream)
+                          : launch_fused_t<false>(p, tiles, sm_budget, stream);
 }
 
 template <bool BF16>
-cudaError_t launch_bucket_t(const BucketFusedParams& p, int64_t tiles, cudaStream_t stream) {
+cudaError_t launch_bucket_t(const BucketFusedParams& p, int64_t tiles, int sm_budget, cudaStream_t stream) {
   switch (fused_vpt(p.n, AR_ORDER_RING, AR_ALLREDUCE)) {
-    case 4: return launch_persistent(fused_bucket_kernel<BF16, 2, 4>, p, tiles, stream);
-    case 2: return launch_persistent(fused_bucket_kernel<BF16, 4, 2>, p, tiles, stream);
-    default: return launch_persistent(fused_bucket_kernel<BF16, 8, 1>, p, tiles, stream);
+    case 4: return launch_persistent(fused_bucket_kernel<BF16, 2, 4>, p, tiles, sm_budget, stream);
+    case 2: return launch_persistent(fused_bucket_kernel<BF16, 4, 2>, p, tiles, sm_budget, stream);
+    default: return launch_persistent(fused_bucket_kernel<BF16, 8, 1>, p, tiles, sm_budget, stream);
   }
 }
 
-cudaError_t launch_bucket_fused(const BucketFusedParams& p, ar_dtype dtype, cudaStream_t stream) {
+cudaError_t launch_bucket_fused(const BucketFusedParams& p, ar_dtype dtype, int sm_budget, cudaStream_t stream) {
   const int64_t tiles = p.tile_start[p.n_seg];
-  return dtype == AR_BF16 ? launch_bucket_t<true>(p, tiles, stream) : launch_bucket_t<false>(p, tiles, stream);
+  return dtype == AR_BF16 ? launch_bucket_t<true>(p, tiles, sm_budget, stream)
+                          : launch_bucket_t<false>(p, tiles, sm_budget, stream);
 }
 
 }  // namespace ar

@@ -112,10 +112,10 @@ constexpr int64_t kStepTile = kThreads * kStepVec * kStepUnroll;  // 4096
 constexpr int kPackTile = kThreads * 8;                   // 2048 elements
 
 cudaError_t launch_step(const StepParams& p, ar_dtype dtype, StepOp op, int total_tiles, bool pdl,
-                        cudaStream_t stream);
-cudaError_t launch_fused(const FusedParams& p, ar_dtype dtype, cudaStream_t stream);
+                        int sm_budget, cudaStream_t stream);
+cudaError_t launch_fused(const FusedParams& p, ar_dtype dtype, int sm_budget, cudaStream_t stream);
 int64_t fused_tile_elems(ar_dtype dtype, int n, int order, int collective);
-cudaError_t launch_bucket_fused(const BucketFusedParams& p, ar_dtype dtype, cudaStream_t stream);
+cudaError_t launch_bucket_fused(const BucketFusedParams& p, ar_dtype dtype, int sm_budget, cudaStream_t stream);
 cudaError_t launch_pack(const PackParams& p, ar_dtype dtype, bool unpack, cudaStream_t stream);
 cudaError_t read_device_status(unsigned int* value, bool clear);
 

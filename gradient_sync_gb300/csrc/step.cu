@@ -175,12 +175,12 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
 }
 
 template <bool BF16>
-cudaError_t launch_op(const StepParams& p, StepOp op, int tiles, bool pdl, cudaStream_t stream) {
+cudaError_t launch_op(const StepParams& p, StepOp op, int tiles, bool pdl, int sm_budget, cudaStream_t stream) {
   void (*k)(StepParams) = op == OP_ADD ? step_kernel<BF16, OP_ADD>
                           : op == OP_COPY ? step_kernel<BF16, OP_COPY>
                                           : step_kernel<BF16, OP_FINISH>;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(persistent_grid(reinterpret_cast<const void*>(k), tiles));
+  cfg.gridDim = dim3(persistent_grid(reinterpret_cast<const void*>(k), tiles, sm_budget));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -195,10 +195,10 @@ cudaError_t launch_op(const StepParams& p, StepOp op, int tiles, bool pdl, cudaS
 }  // namespace
 
 cudaError_t launch_step(const StepParams& p, ar_dtype dtype, StepOp op, int total_tiles, bool pdl,
-                        cudaStream_t stream) {
+                        int sm_budget, cudaStream_t stream) {
   if (total_tiles <= 0) return cudaSuccess;
-  return dtype == AR_BF16 ? launch_op<true>(p, op, total_tiles, pdl, stream)
-                          : launch_op<false>(p, op, total_tiles, pdl, stream);
+  return dtype == AR_BF16 ? launch_op<true>(p, op, total_tiles, pdl, sm_budget, stream)
+                          : launch_op<false>(p, op, total_tiles, pdl, sm_budget, stream);
 }
 
 }  // namespace ar

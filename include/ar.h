@@ -116,6 +116,10 @@ typedef struct {
   ar_order order;  /* AR_FUSED only */
   float scale;     /* multiplies the complete fp32 sum once (1.0f = plain sum) */
   ar_collective collective; /* AR_ALLREDUCE (0) unless set */
+  int sm_budget;   /* at most this many SMs' worth of CTAs per kernel (0 = all SMs).
+                      A collective that overlaps computation takes only part of
+                      the GPU, as a NCCL channel takes one SM (primer §4.5).
+                      Results do not depend on it. */
 } ar_desc;
 
 /* Accounting of one ar_execute (primer §4.2 and §4.3 cost formulas). */
@@ -307,9 +311,10 @@ ar_status ar_bucket_unpack(int n_ranks, const void* const* bucket, float scale, 
  * element e runs in ring order over the packed bucket (chunk boundaries at
  * floor(c * bucket_count / N)), so the result is bit-identical to
  * ar_bucket_pack + AR_RING (fp32) + ar_bucket_unpack. dtype is the tensors'
- * type. In place. */
+ * type. In place. sm_budget as in ar_desc (0 = all SMs). */
 ar_status ar_bucket_allreduce(int n_ranks, void* const* tensors, const size_t* counts, int n_tensors,
-                              int t_begin, int t_end, ar_dtype dtype, float scale, void* stream);
+                              int t_begin, int t_end, ar_dtype dtype, float scale, int sm_budget,
+                              void* stream);
 
 /* ---------------------------------------------------------------- status */
 
