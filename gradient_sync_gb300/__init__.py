@@ -19,6 +19,7 @@ AR_F32, AR_BF16 = 0, 1
 AR_RING, AR_RABENSEIFNER, AR_HIER, AR_FUSED, AR_AUTO = 0, 1, 2, 3, 4
 AR_ORDER_RING, AR_ORDER_RANK, AR_ORDER_TREE, AR_ORDER_HIER = 0, 1, 2, 3
 AR_ALLREDUCE, AR_REDUCE_SCATTER, AR_ALLGATHER = 0, 1, 2
+AR_KERNEL_AUTO, AR_KERNEL_LOADS, AR_KERNEL_BULK = 0, 1, 2
 AR_MAX_RANKS = 64
 AR_MAX_BUCKET_TENSORS = 32
 
@@ -28,6 +29,8 @@ AR_DEVICE_ALPHA_S, AR_DEVICE_BW = 1.5e-6, 6.0e12
 ORDERS = {"ring": AR_ORDER_RING, "rank": AR_ORDER_RANK, "tree": AR_ORDER_TREE, "hier": AR_ORDER_HIER}
 DTYPES = {"f32": AR_F32, "bf16": AR_BF16}
 COLLECTIVES = {"allreduce": AR_ALLREDUCE, "reduce_scatter": AR_REDUCE_SCATTER, "allgather": AR_ALLGATHER}
+KERNELS = {"auto": AR_KERNEL_AUTO, "loads": AR_KERNEL_LOADS, "bulk": AR_KERNEL_BULK}
+KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 
 
 class ArError(RuntimeError):
@@ -87,15 +90,16 @@ class Plan:
 
 
 def ar_plan(n_ranks: int, count: int, dtype="f32", algo="fused", group_size: int = 0, order="ring",
-            scale: float = 1.0, collective="allreduce", sm_budget: int = 0) -> Plan:
+            scale: float = 1.0, collective="allreduce", sm_budget: int = 0, kernel="auto") -> Plan:
     """Validate the descriptor and build the schedule (host only)."""
     d = _lib.ArDesc(int(n_ranks), int(count), DTYPES.get(dtype, dtype), ALGOS.get(algo, algo),
                     int(group_size), ORDERS.get(order, order), float(scale),
-                    COLLECTIVES.get(collective, collective), int(sm_budget))
+                    COLLECTIVES.get(collective, collective), int(sm_budget), KERNELS.get(kernel, kernel))
     h = _lib.c_void_p()
     _check(_lib.load().ar_plan(d, h), "ar_plan")
     return Plan(h.value, dict(n_ranks=n_ranks, count=count, dtype=dtype, algo=algo, group_size=group_size,
-                              order=order, scale=scale, collective=collective, sm_budget=sm_budget))
+                              order=order, scale=scale, collective=collective, sm_budget=sm_budget,
+                              kernel=kernel))
 
 
 def ar_plan_desc(plan: Plan) -> dict:
@@ -104,7 +108,7 @@ def ar_plan_desc(plan: Plan) -> dict:
     _check(_lib.load().ar_plan_desc(plan.handle, d), "ar_plan_desc")
     return {"n_ranks": d.n_ranks, "count": d.count, "dtype": d.dtype, "algo": ALGO_NAMES.get(d.algo, d.algo),
             "group_size": d.group_size, "order": d.order, "scale": d.scale, "collective": d.collective,
-            "sm_budget": d.sm_budget}
+            "sm_budget": d.sm_budget, "kernel": KERNEL_NAMES.get(d.kernel, d.kernel)}
 
 
 def fabric(alpha, bw_local, bw_net=None, ranks_per_server=0, in_network=False, shared_memory=False):
@@ -228,10 +232,11 @@ def ar_bucket_unpack(bucket, scale: float, out_dtype, tensors, counts, t_begin: 
 
 
 def ar_bucket_allreduce(tensors, counts, t_begin: int, t_end: int, dtype, scale: float, stream=None,
-                        sm_budget: int = 0):
+                        sm_budget: int = 0, kernel="auto"):
     n, ptrs, cnt, nt = _marshal(tensors, counts)
     _check(_lib.load().ar_bucket_allreduce(n, ptrs, cnt, nt, t_begin, t_end, DTYPES.get(dtype, dtype),
-                                           float(scale), int(sm_budget), _stream(stream)), "ar_bucket_allreduce")
+                                           float(scale), int(sm_budget), KERNELS.get(kernel, kernel),
+                                           _stream(stream)), "ar_bucket_allreduce")
 
 
 # ---------------------------------------------------------------- status
@@ -239,6 +244,11 @@ def ar_bucket_allreduce(tensors, counts, t_begin: int, t_end: int, dtype, scale:
 
 def ar_device_status(clear: bool = True) -> int:
     return _lib.load().ar_device_status(1 if clear else 0)
+
+
+def ar_selftest_wait_timeout(polls: int = 1000, stream=None):
+    """Run the bounded-wait self-test kernel (see include/ar.h)."""
+    _check(_lib.load().ar_selftest_wait_timeout(int(polls), _stream(stream)), "ar_selftest_wait_timeout")
 
 
 def ar_status_string(status: int) -> str:

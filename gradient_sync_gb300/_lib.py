@@ -16,7 +16,7 @@ INTP = ctypes.POINTER(c_int)
 class ArDesc(ctypes.Structure):
     _fields_ = [("n_ranks", c_int), ("count", c_size_t), ("dtype", c_int), ("algo", c_int),
                 ("group_size", c_int), ("order", c_int), ("scale", c_float), ("collective", c_int),
-                ("sm_budget", c_int)]
+                ("sm_budget", c_int), ("kernel", c_int)]
 
 
 class ArStats(ctypes.Structure):
@@ -46,8 +46,10 @@ SIGNATURES = {
     "ar_bucket_pack": (c_int, [c_int, VOIDPP, SIZEP, c_int, c_int, c_int, c_int, VOIDPP, c_void_p]),
     "ar_bucket_unpack": (c_int, [c_int, VOIDPP, c_float, c_int, VOIDPP, SIZEP, c_int, c_int, c_int,
                                  c_void_p]),
-    "ar_bucket_allreduce": (c_int, [c_int, VOIDPP, SIZEP, c_int, c_int, c_int, c_int, c_float, c_int, c_void_p]),
+    "ar_bucket_allreduce": (c_int, [c_int, VOIDPP, SIZEP, c_int, c_int, c_int, c_int, c_float, c_int, c_int,
+                                    c_void_p]),
     "ar_device_status": (c_int, [c_int]),
+    "ar_selftest_wait_timeout": (c_int, [ctypes.c_uint, c_void_p]),
     "ar_status_string": (ctypes.c_char_p, [c_int]),
     "ar_version": (c_int, []),
 }

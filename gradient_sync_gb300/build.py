@@ -20,9 +20,9 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libar_gb300.so")
 
-CUDA_SOURCES = ["fused.cu", "step.cu", "pack.cu", "noalloc.cu"]
+CUDA_SOURCES = ["fused.cu", "fused_tma.cu", "step.cu", "pack.cu", "noalloc.cu"]
 CXX_SOURCES = ["api.cpp"]
-HEADERS = ["internal.h", "common.cuh"]
+HEADERS = ["internal.h", "common.cuh", "bulk.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -38,12 +38,13 @@ def hbm_peak():
 
 
 def time_case(n, count, dtype="f32", algo="fused", order="ring", group_size=0, iters=20, warmup=5,
-              reps=None, graph=False, collective="allreduce"):
+              reps=None, graph=False, collective="allreduce", sm_budget=0, kernel="auto"):
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
     esz = 4 if dtype == "f32" else 2
     bufs = [torch.rand(count, device="cuda").to(tdt) for _ in range(n)]
     outs = [torch.empty_like(b) for b in bufs]
-    plan = g.ar_plan(n, count, dtype, algo, group_size=group_size, order=order, collective=collective)
+    plan = g.ar_plan(n, count, dtype, algo, group_size=group_size, order=order, collective=collective,
+                     sm_budget=sm_budget, kernel=kernel)
     ws = g.workspace_for(plan)
     st = plan.stats
     nbytes = n * count * esz
@@ -86,7 +87,7 @@ def time_case(n, count, dtype="f32", algo="fused", order="ring", group_size=0, i
     hbm = st["hbm_bytes"] / (ms * 1e-3) / 1e9
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     factor = 2 * (n - 1) / n if collective == "allreduce" else (n - 1) / n  # busbw (primer §4.8)
-    res = {"n": n, "collective": collective, "bytes_per_rank": S, "dtype": dtype, "algo": algo,
+    res = {"n": n, "collective": collective, "sm_budget": sm_budget, "kernel": kernel, "bytes_per_rank": S, "dtype": dtype, "algo": algo,
            "order": order if algo == "fused" else None,
            "timing": "cuda graph" if graph else "launched from python",
            "group_size": group_size or None, "us": round(ms * 1e3, 2), "algbw": round(algbw, 2),
@@ -192,6 +193,7 @@ def main(argv=None):
     ap.add_argument("--overlap", action="store_true", help="bucketed sync overlapped with a synthetic backward")
     ap.add_argument("--tokens", type=int, default=4096)
     ap.add_argument("--sm-budget", type=int, default=0)
+    ap.add_argument("--kernel", default="auto", choices=["auto", "loads", "bulk"])
     a = ap.parse_args(argv)
     from gradient_sync_gb300 import build
 
@@ -206,10 +208,11 @@ def main(argv=None):
         from gradient_sync_gb300.overlap import time_overlap
 
         print(json.dumps(time_overlap(n_ranks=a.n, tokens=a.tokens, sm_budget=a.sm_budget, iters=a.iters,
-                                      warmup=min(a.warmup, 3))))
+                                      warmup=min(a.warmup, 3), kernel=a.kernel)))
         return
     print(json.dumps(time_case(a.n, a.count, a.dtype, a.algo, a.order, a.group_size, a.iters, a.warmup, a.reps,
-                               graph=a.graph, collective=a.collective)))
+                               graph=a.graph, collective=a.collective, sm_budget=a.sm_budget,
+                               kernel=a.kernel)))
 
 
 if __name__ == "__main__":

@@ -294,8 +294,9 @@ ar_status check_buffers(const ar_plan_t* p, void* const* bufs, void* const* outs
 
 ar_status from_cuda(cudaError_t e) { return e == cudaSuccess ? AR_OK : AR_ECUDA; }
 
-// Segment count and tiles per segment of a fused launch over [e_lo, e_hi).
-void fused_tiling(const ar_desc& d, FusedParams& fp) {
+// Segment count and tiles per segment of a fused launch over [e_lo, e_hi),
+// for tiles of `tile` elements.
+void fused_tiling(const ar_desc& d, FusedParams& fp, int64_t tile) {
   const int N = d.n_ranks;
   const int64_t L = int64_t(d.count);
   std::vector<std::pair<int64_t, int64_t>> segs;
@@ -313,7 +314,6 @@ void fused_tiling(const ar_desc& d, FusedParams& fp) {
     segs.push_back({0, L});
   }
   const int64_t W = d.dtype == AR_BF16 ? 8 : 4;
-  const int64_t tile = fused_tile_elems(d.dtype, N, d.order, d.collective);
   int64_t tps = 1;
   for (auto& s : segs) {
     const int64_t lo = std::max(s.first, fp.e_lo), hi = std::min(s.second, fp.e_hi);
@@ -343,7 +343,12 @@ ar_status execute_fused(const ar_plan_t* p, void* const* bufs, void* const* outs
   fp.e_lo = e_lo;
   fp.e_hi = e_hi;
   fp.scale = d.collective == AR_ALLGATHER ? 1.0f : d.scale;  // an all-gather only copies
-  fused_tiling(d, fp);
+  int stages = 0, tile_bytes = 0;
+  if (d.kernel == AR_KERNEL_BULK && tma_shape(d.n_ranks, stages, tile_bytes)) {  // checked at plan time
+    fused_tiling(d, fp, tile_bytes / int64_t(esize(d.dtype)));
+    return from_cuda(launch_fused_tma(fp, d.dtype, stages, tile_bytes, d.sm_budget, stream));
+  }
+  fused_tiling(d, fp, fused_tile_elems(d.dtype, d.n_ranks, d.order, d.collective));
   return from_cuda(launch_fused(fp, d.dtype, d.sm_budget, stream));
 }
 
@@ -469,6 +474,11 @@ ar_status ar_plan(const ar_desc* desc, ar_plan_t** out) {
   if (d.count > (size_t(1) << 40)) return AR_EINVAL;
   if (d.collective < AR_ALLREDUCE || d.collective > AR_ALLGATHER) return AR_EINVAL;
   if (d.sm_budget < 0) return AR_EINVAL;
+  if (d.kernel < AR_KERNEL_AUTO || d.kernel > AR_KERNEL_BULK) return AR_EINVAL;
+  if (d.kernel == AR_KERNEL_BULK && d.algo == AR_FUSED && N > 1) {
+    int stages = 0, tile_bytes = 0;
+    if (d.collective != AR_ALLREDUCE || !tma_shape(N, stages, tile_bytes)) return AR_EUNSUPPORTED;
+  }
   if (d.collective != AR_ALLREDUCE) {
     if (d.algo != AR_RING && d.algo != AR_FUSED) return AR_EUNSUPPORTED;
     if (d.algo == AR_FUSED && d.order == AR_ORDER_HIER) return AR_EUNSUPPORTED;
@@ -818,11 +828,12 @@ ar_status ar_bucket_unpack(int n_ranks, const void* const* bucket, float scale, 
 
 ar_status ar_bucket_allreduce(int n_ranks, void* const* tensors, const size_t* counts, int n_tensors,
                               int t_begin, int t_end, ar_dtype dtype, float scale, int sm_budget,
-                              void* stream) {
+                              ar_kernel kernel, void* stream) {
   ar_status s = check_bucket_args(n_ranks, tensors, counts, n_tensors, t_begin, t_end);
   if (s != AR_OK) return s;
   if (dtype != AR_F32 && dtype != AR_BF16) return AR_EINVAL;
   if (!std::isfinite(scale) || sm_budget < 0) return AR_EINVAL;
+  if (kernel < AR_KERNEL_AUTO || kernel > AR_KERNEL_BULK) return AR_EINVAL;
   const int N = n_ranks;
   const auto off = packed_offsets(counts, t_begin, t_end);
   int64_t Lb = 0;
@@ -830,7 +841,10 @@ ar_status ar_bucket_allreduce(int n_ranks, void* const* tensors, const size_t* c
   if (Lb == 0) return AR_OK;
   const auto b = cuts(0, Lb, N);
   const int64_t W = dtype == AR_BF16 ? 8 : 4;
-  const int64_t tile = fused_tile_elems(dtype, N, AR_ORDER_RING, AR_ALLREDUCE);
+  int stages = 0, tile_bytes = 0;
+  const bool tma = kernel == AR_KERNEL_BULK;
+  if (tma && !tma_shape(N, stages, tile_bytes)) return AR_EUNSUPPORTED;
+  const int64_t tile = tma ? tile_bytes / int64_t(esize(dtype)) : fused_tile_elems(dtype, N, AR_ORDER_RING, AR_ALLREDUCE);
   const int max_group = std::min(AR_MAX_BUCKET_TENSORS, kMaxBucketPtrs / N);
   static thread_local BucketFusedParams bp;
   std::memset(&bp, 0, sizeof(bp));
@@ -843,7 +857,8 @@ ar_status ar_bucket_allreduce(int n_ranks, void* const* tensors, const size_t* c
     bp.n = N;
     bp.scale = scale;
     bp.tile_start[bp.n_seg] = tiles;
-    const cudaError_t e = launch_bucket_fused(bp, dtype, sm_budget, static_cast<cudaStream_t>(stream));
+    const cudaError_t e = tma ? launch_bucket_tma(bp, dtype, stages, tile_bytes, sm_budget, static_cast<cudaStream_t>(stream))
+                              : launch_bucket_fused(bp, dtype, sm_budget, static_cast<cudaStream_t>(stream));
     std::memset(&bp, 0, sizeof(bp));
     nt = 0;
     tiles = 0;
@@ -885,6 +900,11 @@ ar_status ar_device_status(int clear) {
   unsigned int v = 0;
   if (read_device_status(&v, clear != 0) != cudaSuccess) return AR_ECUDA;
   return v != 0 ? AR_ETIMEOUT : AR_OK;
+}
+
+ar_status ar_selftest_wait_timeout(unsigned int polls, void* stream) {
+  if (polls == 0) return AR_EINVAL;
+  return from_cuda(launch_wait_timeout(polls, static_cast<cudaStream_t>(stream)));
 }
 
 const char* ar_status_string(ar_status status) {

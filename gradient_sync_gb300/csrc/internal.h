@@ -118,5 +118,12 @@ int64_t fused_tile_elems(ar_dtype dtype, int n, int order, int collective);
 cudaError_t launch_bucket_fused(const BucketFusedParams& p, ar_dtype dtype, int sm_budget, cudaStream_t stream);
 cudaError_t launch_pack(const PackParams& p, ar_dtype dtype, bool unpack, cudaStream_t stream);
 cudaError_t read_device_status(unsigned int* value, bool clear);
+// The bulk-copy variant of the fused all-reduce (fused_tma.cu).
+bool tma_shape(int n, int& stages, int& tile_bytes);
+cudaError_t launch_fused_tma(const FusedParams& p, ar_dtype dtype, int stages, int tile_bytes, int sm_budget,
+                             cudaStream_t stream);
+cudaError_t launch_bucket_tma(const BucketFusedParams& p, ar_dtype dtype, int stages, int tile_bytes, int sm_budget,
+                              cudaStream_t stream);
+cudaError_t launch_wait_timeout(uint32_t polls, cudaStream_t stream);
 
 }  // namespace ar

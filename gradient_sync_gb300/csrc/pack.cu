@@ -105,17 +105,4 @@ cudaError_t launch_pack(const PackParams& p, ar_dtype dtype, bool unpack, cudaSt
   return cudaLaunchKernelEx(&cfg, k, p);
 }
 
-// Sticky status word of this library on each device, set by a kernel whose
-// bounded wait ran out (no kernel of this build waits yet; the word reads 0).
-__device__ unsigned int g_ar_status_word;
-
-cudaError_t read_device_status(unsigned int* value, bool clear) {
-  cudaError_t err = cudaDeviceSynchronize();
-  if (err != cudaSuccess) return err;
-  err = cudaMemcpyFromSymbol(value, g_ar_status_word, sizeof(unsigned int));
-  if (err != cudaSuccess || !clear) return err;
-  const unsigned int zero = 0;
-  return cudaMemcpyToSymbol(g_ar_status_word, &zero, sizeof(unsigned int));
-}
-
 }  // namespace ar

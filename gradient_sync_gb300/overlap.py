@@ -36,7 +36,8 @@ class BucketedReducer:
     finish() before using the results.
     """
 
-    def __init__(self, grads, counts=None, cap_bytes=25 * MiB, scale=None, comm_stream=None, sm_budget=0):
+    def __init__(self, grads, counts=None, cap_bytes=25 * MiB, scale=None, comm_stream=None, sm_budget=0,
+                 kernel="auto"):
         self.dtype = "bf16" if grads[0][0].dtype == torch.bfloat16 else "f32"
         self.n = len(grads)
         self.table = g.TensorTable(grads, counts)
@@ -51,12 +52,13 @@ class BucketedReducer:
         self.comm = comm_stream or torch.cuda.Stream()
         self.comm_handle = int(self.comm.cuda_stream)
         self.sm_budget = sm_budget
+        self.kernel = kernel
         self._remaining = [k for _, _, k in self.buckets]
 
     def launch(self, b):
         lo, hi, _ = self.buckets[b]
         g.ar_bucket_allreduce(self.table, None, lo, hi, self.dtype, self.scale, stream=self.comm_handle,
-                              sm_budget=self.sm_budget)
+                              sm_budget=self.sm_budget, kernel=self.kernel)
 
     def ready(self, t):
         """Gradient t is complete on the current stream."""
@@ -76,7 +78,7 @@ class BucketedReducer:
         cur = int(torch.cuda.current_stream().cuda_stream)
         for lo, hi, _ in self.buckets:
             g.ar_bucket_allreduce(self.table, None, lo, hi, self.dtype, self.scale, stream=cur,
-                                  sm_budget=self.sm_budget)
+                                  sm_budget=self.sm_budget, kernel=self.kernel)
 
 
 class SyntheticBackward:
@@ -169,7 +171,7 @@ def _time(fn, stream, iters):
     return times[len(times) // 2]
 
 
-def time_overlap(n_ranks=8, tokens=4096, sm_budget=0, iters=5, warmup=2, layers=16):
+def time_overlap(n_ranks=8, tokens=4096, sm_budget=0, iters=5, warmup=2, layers=16, kernel="auto"):
     """Milliseconds of: the backward alone, the gradient sync alone, the two in
     sequence, and overlapped; plus the exposed communication and what the
     critical-path model predicts from the measured bucket readiness and
@@ -179,7 +181,7 @@ def time_overlap(n_ranks=8, tokens=4096, sm_budget=0, iters=5, warmup=2, layers=
     tensors = workloads.transformer_tensors(layers=layers)
     counts = [c for _, c in tensors]
     grads = [[torch.randn(c, device="cuda").to(torch.bfloat16) for c in counts] for _ in range(n_ranks)]
-    red = BucketedReducer(grads, counts, sm_budget=sm_budget)
+    red = BucketedReducer(grads, counts, sm_budget=sm_budget, kernel=kernel)
     bwd = SyntheticBackward(tensors, tokens=tokens)
     main = torch.cuda.current_stream()
 
@@ -220,12 +222,14 @@ def time_overlap(n_ranks=8, tokens=4096, sm_budget=0, iters=5, warmup=2, layers=
     handle = int(main.cuda_stream)
     for lo, hi, _ in red.buckets:
         durations.append(_time(lambda: g.ar_bucket_allreduce(red.table, None, lo, hi, red.dtype, red.scale,
-                                                             stream=handle, sm_budget=sm_budget), main, 3))
+                                                             stream=handle, sm_budget=sm_budget,
+                                                             kernel=kernel), main, 3))
     predicted = critical_path(ready, durations, start.elapsed_time(end))
     del grads
     torch.cuda.empty_cache()
     return {"workload": f"{layers}-layer transformer backward, {tokens} tokens, bucketed sync of {n_ranks} ranks",
-            "n_ranks": n_ranks, "tokens": tokens, "sm_budget": sm_budget, "buckets": len(red.buckets),
+            "n_ranks": n_ranks, "tokens": tokens, "sm_budget": sm_budget, "kernel": kernel,
+            "buckets": len(red.buckets),
             "backward_tflop": round(bwd.flops() / 1e12, 3),
             "ms_compute": round(t_compute, 3), "ms_comm": round(t_comm, 3), "ms_sequential": round(t_seq, 3),
             "ms_overlapped": round(t_ovl, 3), "ms_exposed": round(t_ovl - t_compute, 3),

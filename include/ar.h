@@ -107,6 +107,24 @@ typedef enum { AR_ORDER_RING = 0, AR_ORDER_RANK = 1, AR_ORDER_TREE = 2, AR_ORDER
  * algorithms return AR_EUNSUPPORTED. */
 typedef enum { AR_ALLREDUCE = 0, AR_REDUCE_SCATTER = 1, AR_ALLGATHER = 2 } ar_collective;
 
+/* Which kernel runs the single pass (AR_FUSED all-reduce and
+ * ar_bucket_allreduce). Both compute the same result, bit for bit; they differ
+ * in how bytes move between HBM and the SM.
+ *  AR_KERNEL_AUTO:  the library's choice (currently AR_KERNEL_LOADS, the
+ *                   faster of the two at every SM budget measured).
+ *  AR_KERNEL_LOADS: persistent register pipeline, 2 CTAs per SM; each thread
+ *                   keeps a batch of 16-byte loads in flight.
+ *  AR_KERNEL_BULK:  one CTA per SM; a producer warp stages every rank's slice
+ *                   of a tile in shared memory with bulk copies (TMA) through a
+ *                   ring of mbarrier-guarded stages; consumer warps fold from
+ *                   shared memory and the result leaves through bulk stores.
+ *                   All-reduce only, N <= 24 (the stages must fit in shared
+ *                   memory); otherwise ar_plan returns AR_EUNSUPPORTED. Its
+ *                   waits are bounded: a wait that runs out sets the device
+ *                   status word (ar_device_status) instead of hanging.
+ * The step executors (AR_RING, AR_RABENSEIFNER, AR_HIER) ignore it. */
+typedef enum { AR_KERNEL_AUTO = 0, AR_KERNEL_LOADS = 1, AR_KERNEL_BULK = 2 } ar_kernel;
+
 typedef struct {
   int n_ranks;     /* N, 1..AR_MAX_RANKS */
   size_t count;    /* elements per rank buffer, >= 0 */
@@ -120,6 +138,7 @@ typedef struct {
                       A collective that overlaps computation takes only part of
                       the GPU, as a NCCL channel takes one SM (primer §4.5).
                       Results do not depend on it. */
+  ar_kernel kernel; /* AR_KERNEL_AUTO (0) unless set */
 } ar_desc;
 
 /* Accounting of one ar_execute (primer §4.2 and §4.3 cost formulas). */
@@ -311,17 +330,26 @@ ar_status ar_bucket_unpack(int n_ranks, const void* const* bucket, float scale, 
  * element e runs in ring order over the packed bucket (chunk boundaries at
  * floor(c * bucket_count / N)), so the result is bit-identical to
  * ar_bucket_pack + AR_RING (fp32) + ar_bucket_unpack. dtype is the tensors'
- * type. In place. sm_budget as in ar_desc (0 = all SMs). */
+ * type. In place. sm_budget and kernel as in ar_desc (0 = all SMs, automatic
+ * kernel); AR_KERNEL_BULK with N > 24 returns AR_EUNSUPPORTED. */
 ar_status ar_bucket_allreduce(int n_ranks, void* const* tensors, const size_t* counts, int n_tensors,
                               int t_begin, int t_end, ar_dtype dtype, float scale, int sm_budget,
-                              void* stream);
+                              ar_kernel kernel, void* stream);
 
 /* ---------------------------------------------------------------- status */
 
 /* Read (and clear, if clear != 0) the calling device's sticky status word,
- * set by a kernel whose bounded device-side wait ran out. Synchronises the
- * device. Returns AR_OK or AR_ETIMEOUT (or AR_ECUDA). */
+ * set by a kernel whose bounded device-side wait ran out (the bulk-copy
+ * all-reduce's mbarrier waits). Synchronises the device. Returns AR_OK or
+ * AR_ETIMEOUT (or AR_ECUDA). */
 ar_status ar_device_status(int clear);
+
+/* Failure-path self-test: launches one thread that waits, with a bound of
+ * `polls` polls, on an mbarrier that nothing will ever complete. The wait gives
+ * up, sets the device status word and the kernel returns; a following
+ * ar_device_status reports AR_ETIMEOUT. This exercises the same bounded wait
+ * that the bulk-copy kernels use, without any fault and without a hang. */
+ar_status ar_selftest_wait_timeout(unsigned int polls, void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* ar_status_string(ar_status status);

@@ -216,3 +216,26 @@ def test_collective_validation(g):
     ag = g.ar_plan(16, 1 << 20, "f32", "fused", collective="allgather").stats
     assert rs["hbm_bytes"] == (16 + 1) * (1 << 20) * 4 and ag["hbm_bytes"] == (16 + 1) * (1 << 20) * 4
     assert g.ar_plan(16, 1 << 20, "bf16", "ring", collective="allgather").stats["workspace_bytes"] == 0
+
+
+def test_kernel_choice_validation(g):
+    with pytest.raises(g.ArError) as e:
+        g.ar_plan(8, 100, "f32", "fused", kernel=3)
+    assert e.value.status == g.AR_EINVAL
+    for bad in (dict(n_ranks=25), dict(collective="reduce_scatter"), dict(collective="allgather")):
+        args = dict(n_ranks=8, count=100, dtype="f32", algo="fused", kernel="bulk")
+        args.update(bad)
+        with pytest.raises(g.ArError) as e:  # the stages must fit in shared memory; all-reduce only
+            g.ar_plan(**args)
+        assert e.value.status == g.AR_EUNSUPPORTED, bad
+    for n in (1, 2, 16, 24):
+        assert g.ar_plan_desc(g.ar_plan(n, 100, "bf16", "fused", kernel="bulk"))["kernel"] == "bulk"
+    assert g.ar_plan_desc(g.ar_plan(64, 100, "f32", "ring", kernel="bulk"))["kernel"] == "bulk"  # ignored
+    assert g.ar_plan_desc(g.ar_plan(8, 100, "f32", "fused"))["kernel"] == "auto"
+    ok = [[0x100000 * (r * 4 + t + 1) for t in range(3)] for r in range(25)]
+    with pytest.raises(g.ArError) as e:
+        g.ar_bucket_allreduce(ok, [10, 10, 10], 0, 3, "bf16", 0.5, stream=0, kernel="bulk")
+    assert e.value.status == g.AR_EUNSUPPORTED
+    with pytest.raises(g.ArError) as e:
+        g.ar_bucket_allreduce(ok[:4], [10, 10, 10], 0, 3, "bf16", 0.5, stream=0, kernel=7)
+    assert e.value.status == g.AR_EINVAL

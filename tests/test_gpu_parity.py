@@ -229,3 +229,48 @@ def test_execute_host_roundtrip(g, algo, pinned):
 
 def test_device_status_is_clear(g):
     assert g.ar_device_status(clear=True) == g.AR_OK
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("order", ["ring", "rank", "tree", "hier"])
+@pytest.mark.parametrize("N,L", [(2, 1), (2, 70001), (3, 7), (4, 1000), (5, 4099), (8, 20003), (16, 100003),
+                                 (16, 1 << 18), (24, 50000), (12, 777)])
+@pytest.mark.parametrize("sm_budget", [0, 7])
+def test_fused_bulk_copy_pipeline_matches_oracle(g, dtype, order, N, L, sm_budget):
+    """The bulk-copy (TMA) kernel gives the register pipeline's result, bit for
+    bit, on the whole GPU and on a few SMs."""
+    if order == "tree" and N & (N - 1):
+        pytest.skip("tree order needs a power-of-two rank count")
+    G = _group(N) if order == "hier" else 0
+    x = workloads.all_ranks(workloads.small_spec(N, L, dtype, "normal", seed=N * 3 + L))
+    devs = [to_device(x[r], dtype) for r in range(N)]
+    outs = [torch.empty_like(d) for d in devs] if L % 2 else None
+    plan = g.ar_plan(N, L, dtype, "fused", group_size=G, order=order, scale=0.5, sm_budget=sm_budget,
+                     kernel="bulk")
+    g.ar_execute(plan, devs, outs=outs)
+    torch.cuda.synchronize()
+    want = expected("fused", order, x, dtype, G, 0.5)
+    for r in range(N):
+        assert_bits_equal(to_host((outs or devs)[r], dtype), want, f"rank {r}")
+
+
+@pytest.mark.parametrize("kernel", ["auto", "loads", "bulk"])
+@pytest.mark.parametrize("sm_budget", [0, 9])
+def test_bucket_paths_with_sm_budget(g, sm_budget, kernel):
+    from oracle import buckets as ob
+
+    N = 8
+    counts = [5, 1000, 37, 40960, 9, 2051, 777, 64, 3, 100_000]
+    rng = np.random.default_rng(sm_budget + 1)
+    grads = [[numerics.f32_to_bf16_rne((rng.standard_normal(c) * 1e-3).astype(np.float32)) for c in counts]
+             for _ in range(N)]
+    cap = 2 * 50_000
+    dev = [[to_device(grads[r][t], "bf16") for t in range(len(counts))] for r in range(N)]
+    for b in ob.bucket_plan(counts, 2, cap):
+        lo, hi = min(b), max(b) + 1
+        g.ar_bucket_allreduce(dev, counts, lo, hi, "bf16", 1.0 / N, sm_budget=sm_budget, kernel=kernel)
+        torch.cuda.synchronize()
+        want = ob.sync_bucket(grads, b, counts, 1.0 / N)
+        for t in b:
+            for r in range(N):
+                assert_bits_equal(to_host(dev[r][t], "bf16"), want[(t, 0)][r], f"t={t} r={r}")
