@@ -16,10 +16,11 @@ Modules:
 * ``chunks``    -- how a buffer of L elements is cut into N chunks.
 * ``numerics``  -- bf16 widening/narrowing, the fp64 definition of the sum,
                    and the fused single-pass sums in each declared order.
-* ``schedules`` -- step-by-step simulations of the ring, Rabenseifner and
-                   hierarchical all-reduce, and of the standalone ring
-                   reduce-scatter and all-gather, with per-rank mailboxes and
-                   byte/step counters.
+* ``schedules`` -- step-by-step simulations of the ring, Rabenseifner,
+                   hierarchical, recursive-doubling, double-binary-tree and
+                   torus (dimension-ordered) all-reduce, and of the standalone
+                   ring reduce-scatter and all-gather, with per-rank mailboxes
+                   and byte/step counters.
 * ``buckets``   -- DDP-style bucket assignment and the bucketed gradient sync.
 
 Parity pins: every function here is pinned by a test against a value the
@@ -33,4 +34,5 @@ from .chunks import chunk_bounds, chunk_of  # noqa: F401
 from .numerics import (bf16_to_f32, f32_to_bf16_rne, fused_sum, reference_sum_f64,  # noqa: F401
                        abs_sum_f64)
 from .schedules import (hierarchical_allreduce, rabenseifner_allreduce,  # noqa: F401
-                        ring_allgather, ring_allreduce, ring_reduce_scatter, RunStats)
+                        ring_allgather, ring_allreduce, ring_reduce_scatter, RunStats,
+                        recursive_doubling_allreduce, double_binary_tree_allreduce, torus_allreduce)

@@ -289,6 +289,215 @@ def ring_allgather(x, idx=None, L=None, server_of=None, trace=None):
     return w.x, w.stats
 
 
+def recursive_doubling_allreduce(x, idx=None, L=None, combine=_add, finish=None, server_of=None,
+                                 trace=None):
+    """Recursive doubling (primer §4.3, "Trees: latency-optimal, bandwidth-poor",
+    Fig. 4.5). N must be a power of two. Step k = 1..log2 N: every rank i sends
+    its whole buffer to p = i xor 2^(k-1) and adds the whole buffer p sends.
+    After log2 N steps every rank holds the full sum, so ``finish`` runs on
+    every rank's whole buffer and every rank owns [0, L)."""
+    w = _World(x, idx, L, server_of, trace)
+    N = w.N
+    if N & (N - 1):
+        raise ValueError("recursive doubling needs a power-of-two rank count")
+    every = w.cols(0, w.L)
+    for k in range(1, N.bit_length()):
+        d = 1 << (k - 1)
+        mailbox = []
+        for i in range(N):
+            mailbox.append((i ^ d, w.x[i, every].copy()))
+            w.count_send(i, i ^ d, 0, w.L, True)
+        for p, payload in mailbox:
+            w.x[p, every] = combine(payload, w.x[p, every])
+        w.end_step(f"doubling {k}")
+    for i in range(N):
+        w.stats.owned[i] = (0, w.L)
+        _apply_finish(w, i, 0, w.L, finish)
+    return w.x, w.stats
+
+
+def binary_tree(N):
+    """Tree 1 of the double binary tree over ranks 0..N-1 (primer §4.3, Fig. 4.6).
+
+    Reading of the figure (8 nodes: root 0 above 4, then 2 and 6, then the odd
+    ranks as leaves; the inner nodes are the even ranks): ranks 1..N-1 form the
+    in-order binary tree in which rank r with lowest set bit b >= 2 has
+    children r - b/2 and r + b/2 (the right child's offset halved until it
+    names a rank below N; none if it reaches 0), and the top of that tree, the
+    largest power of two below N, hangs under the root, rank 0. Odd ranks are
+    leaves. Returns (parent, children): parent[0] = -1, children in ascending
+    rank order.
+    """
+    parent = [-1] * N
+    children = [[] for _ in range(N)]
+
+    def link(a, c):
+        assert parent[c] == -1 and c != 0, (a, c)
+        parent[c] = a
+        children[a].append(c)
+
+    if N > 1:
+        link(0, 1 << ((N - 1).bit_length() - 1))
+        for r in range(1, N):
+            b = r & -r
+            if b < 2:
+                continue
+            link(r, r - b // 2)
+            off = b // 2
+            while off >= 1 and r + off >= N:
+                off //= 2
+            if off >= 1:
+                link(r, r + off)
+    for c in children:
+        c.sort()
+    return parent, children
+
+
+def double_binary_trees(N):
+    """The two trees of the double binary tree: tree 1 from ``binary_tree`` and
+    tree 2 its mirror, rank r becoming N-1-r (primer §4.3, Fig. 4.6). Returns
+    [(parent, children), (parent, children)]."""
+    p1, c1 = binary_tree(N)
+    m = [N - 1 - r for r in range(N)]
+    p2 = [-1] * N
+    c2 = [[] for _ in range(N)]
+    for r in range(N):
+        if p1[r] >= 0:
+            p2[m[r]] = m[p1[r]]
+        c2[m[r]] = sorted(m[c] for c in c1[r])
+    return [(p1, c1), (p2, c2)]
+
+
+def tree_depths(parent):
+    """Depth of every node below its root (root 0)."""
+    depth = []
+    for r in range(len(parent)):
+        d, q = 0, r
+        while parent[q] >= 0:
+            q = parent[q]
+            d += 1
+        depth.append(d)
+    return depth
+
+
+def double_binary_tree_allreduce(x, idx=None, L=None, combine=_add, finish=None, server_of=None,
+                                 trace=None, n_trees=2):
+    """All-reduce over NCCL-style double binary trees (primer §4.3, Fig. 4.6 and
+    the table of ring, tree and Rabenseifner; Scaling ML Systems, "Double
+    binary tree").
+
+    With two trees, tree t carries half t of the buffer ([0, floor(L/2)) and
+    the rest); with ``n_trees=1``, tree 1 carries all of it (a plain binary
+    tree). Reduce: level by level from the deepest inner nodes up, every inner
+    node receives its children's partial sums of its tree's half and folds
+    them into its own copy: (own + first child) + second child, children in
+    ascending rank order. Both trees run their levels in the same steps (tree
+    2 is a mirror image, so the levels line up). The root's sum is complete:
+    ``finish`` runs there. Broadcast: level by level from the root down, every
+    parent sends the result to its children, which overwrite their copies.
+
+    Byte counters follow the data movement of a step: a child's send reads its
+    copy; a receiving node reads its own copy once and writes it once, however
+    many children it has.
+    """
+    w = _World(x, idx, L, server_of, trace)
+    N = w.N
+    if n_trees not in (1, 2):
+        raise ValueError("one or two trees")
+    trees = double_binary_trees(N)[:n_trees]
+    halves = chunk_bounds(w.L, n_trees)
+    depths = [tree_depths(p) for p, _ in trees]
+    top = max(max(d) for d in depths) if N > 1 else 0
+    s = w.stats
+    for level in range(top - 1, -1, -1):
+        mailbox = []
+        for t, (parent, children) in enumerate(trees):
+            lo, hi = halves[t], halves[t + 1]
+            cols = w.cols(lo, hi)
+            for r in range(N):
+                if depths[t][r] != level or not children[r]:
+                    continue
+                payloads = [w.x[c, cols].copy() for c in children[r]]
+                for c in children[r]:
+                    s.sends.append((s.steps, c, r, lo, hi))
+                    s.elements_sent[c] += hi - lo
+                    s.element_reads += hi - lo
+                    if server_of is not None and server_of[c] != server_of[r]:
+                        s.cross_elements += hi - lo
+                s.element_reads += hi - lo
+                s.element_writes += hi - lo
+                mailbox.append((r, cols, payloads))
+        for r, cols, payloads in mailbox:
+            acc = w.x[r, cols]
+            for pl in payloads:
+                acc = combine(pl, acc)
+            w.x[r, cols] = acc
+        w.end_step(f"tree reduce {level}")
+    for t, (parent, _) in enumerate(trees):
+        root = parent.index(-1)
+        s.owned[(t, root)] = (halves[t], halves[t + 1])
+        _apply_finish(w, root, halves[t], halves[t + 1], finish)
+    for level in range(top):
+        mailbox = []
+        for t, (parent, children) in enumerate(trees):
+            lo, hi = halves[t], halves[t + 1]
+            cols = w.cols(lo, hi)
+            for r in range(N):
+                if depths[t][r] != level:
+                    continue
+                for c in children[r]:
+                    mailbox.append((c, cols, w.x[r, cols].copy()))
+                    w.count_send(r, c, lo, hi, False)
+        for c, cols, payload in mailbox:
+            w.x[c, cols] = payload
+        w.end_step(f"tree broadcast {level}")
+    return w.x, w.stats
+
+
+def torus_allreduce(x, dims, idx=None, L=None, combine=_add, finish=None, server_of=None, trace=None):
+    """Dimension-ordered all-reduce on an X x Y (x Z) torus (Scaling ML Systems,
+    "Collective communication", section on torus topologies, the TPU-pod
+    figure and the three-step list).
+
+    Rank (x, y, z) is x + X*(y + Y*z). Dimension by dimension (X, then Y, then
+    Z) every line of ranks along that dimension, in coordinate order, runs the
+    ring all-reduce of ``ring_allreduce`` over the whole buffer cut into as many
+    chunks as the line has ranks; all lines of a dimension run in lockstep.
+    The next dimension reduces the partial sums the previous one left on every
+    rank. ``finish`` runs once, on the owners of the last dimension's chunks.
+    Steps: the sum of 2(D-1) over the dimensions (4 x 4: 12, against 30 for a
+    flat ring of 16).
+    """
+    w = _World(x, idx, L, server_of, trace)
+    N = w.N
+    dims = [int(d) for d in dims] + [1] * (3 - len(dims))
+    X, Y, Z = dims
+    if min(dims) < 1 or X * Y * Z != N:
+        raise ValueError("torus dimensions must multiply to the rank count")
+    stride = [1, X, X * Y]
+    active = [d for d in range(3) if dims[d] > 1]
+    if not active:
+        w.stats.owned[0] = (0, w.L)
+        _apply_finish(w, 0, 0, w.L, finish)
+        return w.x, w.stats
+    for d in active:
+        D = dims[d]
+        lines = []
+        for r in range(N):
+            if (r // stride[d]) % D == 0:  # first rank of its line
+                lines.append(([r + p * stride[d] for p in range(D)], 0, w.L))
+        last = _ring_phase(w, lines, lambda p, s: p - s, True, combine, f"dim {'XYZ'[d]} reduce-scatter")
+        if d == active[-1]:
+            b = chunk_bounds(w.L, D)
+            for li, (members, _, _) in enumerate(lines):
+                for p, r in enumerate(members):
+                    c = last[li][p]
+                    w.stats.owned[r] = (b[c], b[c + 1])
+                    _apply_finish(w, r, b[c], b[c + 1], finish)
+        _ring_phase(w, lines, lambda p, s: p + 1 - s, False, combine, f"dim {'XYZ'[d]} all-gather")
+    return w.x, w.stats
+
+
 # ----------------------------------------------------------------- helpers
 
 
@@ -313,4 +522,7 @@ SCHEDULES = {
     "ring": ring_allreduce,
     "rabenseifner": rabenseifner_allreduce,
     "hier": hierarchical_allreduce,
+    "recdoubling": recursive_doubling_allreduce,
+    "dbtree": double_binary_tree_allreduce,
+    "torus": torus_allreduce,
 }

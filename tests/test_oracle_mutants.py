@@ -111,3 +111,84 @@ def test_mutant_bf16_truncation(monkeypatch):
     monkeypatch.setattr(numerics, "f32_to_bf16_rne", trunc)
     with pytest.raises(AssertionError):
         props.test_bf16_rne_matches_torch_conversion()
+
+
+# ---- schedule variants (recursive doubling, double binary tree, torus)
+
+import test_oracle_variants as variants  # noqa: E402
+
+
+def test_mutant_doubling_far_partner_first(monkeypatch):
+    src = schedules.recursive_doubling_allreduce
+
+    def far_first(x, **kw):
+        # distance N/2 first: run on ranks with their bits reversed
+        N = x.shape[0]
+        k = N.bit_length() - 1
+        rev = [int(format(i, f"0{k}b")[::-1], 2) if k else 0 for i in range(N)]
+        out, st = src(x[rev].copy(), **kw)
+        st.sends = [(s, rev[a], rev[b], lo, hi) for s, a, b, lo, hi in st.sends]
+        return out[np.argsort(rev)], st
+
+    monkeypatch.setattr(schedules, "recursive_doubling_allreduce", far_first)
+    with pytest.raises(AssertionError):
+        variants.test_recursive_doubling_fig_4_5(read_golden)
+    with pytest.raises(AssertionError):
+        variants.test_recursive_doubling_order_is_the_balanced_tree(8)
+
+
+def test_mutant_tree_without_mirror(monkeypatch):
+    monkeypatch.setattr(schedules, "double_binary_trees",
+                        lambda N: [schedules.binary_tree(N), schedules.binary_tree(N)])
+    with pytest.raises(AssertionError):
+        variants.test_double_binary_tree_fig_4_6(read_golden)
+    with pytest.raises(AssertionError):
+        variants.test_double_binary_tree_inner_nodes_disjoint(8)
+
+
+def test_mutant_tree_children_folded_high_first(monkeypatch):
+    orig = schedules.double_binary_trees
+
+    def reversed_children(N):
+        return [(p, [sorted(c, reverse=True) for c in ch]) for p, ch in orig(N)]
+
+    monkeypatch.setattr(schedules, "double_binary_trees", reversed_children)
+    with pytest.raises(AssertionError):
+        variants.test_double_binary_tree_order_closed_form(16, read_golden)
+
+
+def test_mutant_tree_root_without_child(monkeypatch):
+    orig = schedules.binary_tree
+
+    def no_top(N):  # the in-order tree left dangling, rank 0 alone
+        p, c = orig(N)
+        if N > 1:
+            top = c[0][0]
+            c[0] = []
+            p[top] = -1
+        return p, c
+
+    monkeypatch.setattr(schedules, "binary_tree", no_top)
+    with pytest.raises(AssertionError):
+        variants.test_double_binary_tree_fig_4_6(read_golden)
+
+
+def test_mutant_torus_columns_first(monkeypatch):
+    src = schedules.torus_allreduce
+
+    def y_first(x, dims, **kw):  # run the transposed torus: Y lines first
+        dims = list(dims) + [1] * (3 - len(dims))
+        X, Y, Z = dims
+        perm = [xx + X * (yy + Y * zz) for zz in range(Z) for xx in range(X) for yy in range(Y)]
+        out, st = src(x[perm].copy(), (Y, X, Z), **kw)
+        return out[np.argsort(perm)], st
+
+    monkeypatch.setattr(schedules, "torus_allreduce", y_first)
+    with pytest.raises(AssertionError):
+        variants.test_torus_order_closed_form((2, 8))
+
+
+def test_mutant_torus_line_ring_starts_one_late(monkeypatch):
+    _plant_ring_rule(monkeypatch, "dim X reduce-scatter", lambda p, s: p - 1 - s)
+    with pytest.raises(AssertionError):
+        variants.test_torus_order_closed_form((4, 4))
