@@ -23,7 +23,9 @@ AR_KERNEL_AUTO, AR_KERNEL_LOADS, AR_KERNEL_BULK = 0, 1, 2
 AR_MAX_RANKS = 64
 AR_MAX_BUCKET_TENSORS = 32
 
-ALGOS = {"ring": AR_RING, "rabenseifner": AR_RABENSEIFNER, "hier": AR_HIER, "fused": AR_FUSED, "auto": AR_AUTO}
+AR_RECDOUBLING, AR_DBTREE, AR_TORUS = 5, 6, 7
+ALGOS = {"ring": AR_RING, "rabenseifner": AR_RABENSEIFNER, "hier": AR_HIER, "fused": AR_FUSED, "auto": AR_AUTO,
+         "recdoubling": AR_RECDOUBLING, "dbtree": AR_DBTREE, "torus": AR_TORUS}
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 AR_DEVICE_ALPHA_S, AR_DEVICE_BW = 1.5e-6, 6.0e12
 ORDERS = {"ring": AR_ORDER_RING, "rank": AR_ORDER_RANK, "tree": AR_ORDER_TREE, "hier": AR_ORDER_HIER}
@@ -90,16 +92,19 @@ class Plan:
 
 
 def ar_plan(n_ranks: int, count: int, dtype="f32", algo="fused", group_size: int = 0, order="ring",
-            scale: float = 1.0, collective="allreduce", sm_budget: int = 0, kernel="auto") -> Plan:
+            scale: float = 1.0, collective="allreduce", sm_budget: int = 0, kernel="auto",
+            torus_dims=(0, 0, 0)) -> Plan:
     """Validate the descriptor and build the schedule (host only)."""
+    dims = (list(torus_dims) + [0, 0, 0])[:3]
     d = _lib.ArDesc(int(n_ranks), int(count), DTYPES.get(dtype, dtype), ALGOS.get(algo, algo),
                     int(group_size), ORDERS.get(order, order), float(scale),
-                    COLLECTIVES.get(collective, collective), int(sm_budget), KERNELS.get(kernel, kernel))
+                    COLLECTIVES.get(collective, collective), int(sm_budget), KERNELS.get(kernel, kernel),
+                    (_lib.c_int * 3)(*[int(v) for v in dims]))
     h = _lib.c_void_p()
     _check(_lib.load().ar_plan(d, h), "ar_plan")
     return Plan(h.value, dict(n_ranks=n_ranks, count=count, dtype=dtype, algo=algo, group_size=group_size,
                               order=order, scale=scale, collective=collective, sm_budget=sm_budget,
-                              kernel=kernel))
+                              kernel=kernel, torus_dims=tuple(dims)))
 
 
 def ar_plan_desc(plan: Plan) -> dict:
@@ -108,7 +113,8 @@ def ar_plan_desc(plan: Plan) -> dict:
     _check(_lib.load().ar_plan_desc(plan.handle, d), "ar_plan_desc")
     return {"n_ranks": d.n_ranks, "count": d.count, "dtype": d.dtype, "algo": ALGO_NAMES.get(d.algo, d.algo),
             "group_size": d.group_size, "order": d.order, "scale": d.scale, "collective": d.collective,
-            "sm_budget": d.sm_budget, "kernel": KERNEL_NAMES.get(d.kernel, d.kernel)}
+            "sm_budget": d.sm_budget, "kernel": KERNEL_NAMES.get(d.kernel, d.kernel),
+            "torus_dims": tuple(d.torus_dims)}
 
 
 def fabric(alpha, bw_local, bw_net=None, ranks_per_server=0, in_network=False, shared_memory=False):

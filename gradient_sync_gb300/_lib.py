@@ -16,7 +16,7 @@ INTP = ctypes.POINTER(c_int)
 class ArDesc(ctypes.Structure):
     _fields_ = [("n_ranks", c_int), ("count", c_size_t), ("dtype", c_int), ("algo", c_int),
                 ("group_size", c_int), ("order", c_int), ("scale", c_float), ("collective", c_int),
-                ("sm_budget", c_int), ("kernel", c_int)]
+                ("sm_budget", c_int), ("kernel", c_int), ("torus_dims", c_int * 3)]
 
 
 class ArStats(ctypes.Structure):

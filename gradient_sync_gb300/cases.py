@@ -38,13 +38,13 @@ def hbm_peak():
 
 
 def time_case(n, count, dtype="f32", algo="fused", order="ring", group_size=0, iters=20, warmup=5,
-              reps=None, graph=False, collective="allreduce", sm_budget=0, kernel="auto"):
+              reps=None, graph=False, collective="allreduce", sm_budget=0, kernel="auto", torus_dims=(0, 0, 0)):
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
     esz = 4 if dtype == "f32" else 2
     bufs = [torch.rand(count, device="cuda").to(tdt) for _ in range(n)]
     outs = [torch.empty_like(b) for b in bufs]
     plan = g.ar_plan(n, count, dtype, algo, group_size=group_size, order=order, collective=collective,
-                     sm_budget=sm_budget, kernel=kernel)
+                     sm_budget=sm_budget, kernel=kernel, torus_dims=torus_dims)
     ws = g.workspace_for(plan)
     st = plan.stats
     nbytes = n * count * esz
@@ -90,7 +90,8 @@ def time_case(n, count, dtype="f32", algo="fused", order="ring", group_size=0, i
     res = {"n": n, "collective": collective, "sm_budget": sm_budget, "kernel": kernel, "bytes_per_rank": S, "dtype": dtype, "algo": algo,
            "order": order if algo == "fused" else None,
            "timing": "cuda graph" if graph else "launched from python",
-           "group_size": group_size or None, "us": round(ms * 1e3, 2), "algbw": round(algbw, 2),
+           "group_size": group_size or None, "torus_dims": list(torus_dims) if algo == "torus" else None,
+           "us": round(ms * 1e3, 2), "algbw": round(algbw, 2),
            "busbw": round(algbw * factor, 2), "steps": st["steps"], "launches": st["launches"],
            "hbm_bytes": st["hbm_bytes"], "hbm_gbs": round(hbm, 1),
            "hbm_frac": round(hbm / hbm_peak(), 4) if nbytes > 4 * l2 else None}
@@ -194,6 +195,7 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=4096)
     ap.add_argument("--sm-budget", type=int, default=0)
     ap.add_argument("--kernel", default="auto", choices=["auto", "loads", "bulk"])
+    ap.add_argument("--dims", default="0,0,0", help="torus dimensions X,Y[,Z] for --algo torus")
     a = ap.parse_args(argv)
     from gradient_sync_gb300 import build
 
@@ -212,7 +214,7 @@ def main(argv=None):
         return
     print(json.dumps(time_case(a.n, a.count, a.dtype, a.algo, a.order, a.group_size, a.iters, a.warmup, a.reps,
                                graph=a.graph, collective=a.collective, sm_budget=a.sm_budget,
-                               kernel=a.kernel)))
+                               kernel=a.kernel, torus_dims=tuple(int(v) for v in a.dims.split(",")))))
 
 
 if __name__ == "__main__":

@@ -29,19 +29,26 @@ std::vector<int64_t> cuts(int64_t lo, int64_t hi, int n) {
   return b;
 }
 
-void add_xfer(Step& st, int src, int dst, int64_t lo, int64_t hi, Space xs, Space ys, Space ds,
-              bool fin) {
-  if (hi <= lo) return;  // L < N leaves some chunks empty
+Transfer make_xfer(int src, int dst, int64_t lo, int64_t hi, Space xs, Space ys, Space ds, bool fin) {
   Transfer t;
   t.src = int16_t(src);
   t.dst = int16_t(dst);
+  t.src2 = -1;
   t.xs = xs;
   t.ys = ys;
   t.ds = ds;
+  t.x2s = RAW;
   t.fin = fin ? 1 : 0;
+  t.pair = 0;
   t.lo = lo;
   t.hi = hi;
-  st.xfers.push_back(t);
+  return t;
+}
+
+void add_xfer(Step& st, int src, int dst, int64_t lo, int64_t hi, Space xs, Space ys, Space ds,
+              bool fin) {
+  if (hi <= lo) return;  // L < N leaves some chunks empty
+  st.xfers.push_back(make_xfer(src, dst, lo, hi, xs, ys, ds, fin));
 }
 
 // Ring all-reduce (primer ch. 4, "Collective communication: algorithms, cost
@@ -210,7 +217,187 @@ void build_hier(ar_plan_t* p) {
   }
 }
 
+// Recursive doubling (primer §4.3, "Trees: latency-optimal, bandwidth-poor",
+// Fig. 4.5): log2 N steps; in step k ranks i and i xor 2^(k-1) exchange their
+// whole buffers and both add, so every rank holds the full sum at the end.
+// One transfer per pair (from its lower rank) with `pair` set: the thread
+// that adds an element writes the sum to both partners.
+void build_recdoubling(ar_plan_t* p) {
+  const int N = p->desc.n_ranks;
+  const int64_t L = int64_t(p->desc.count);
+  int K = 0;
+  while ((1 << K) < N) ++K;
+  for (int k = 1; k <= K; ++k) {
+    const int d = 1 << (k - 1);
+    Step st{OP_ADD, {}};
+    const Space in = k == 1 ? RAW : PART;
+    for (int i = 0; i < N; ++i) {
+      if (i & d || L == 0) continue;
+      Transfer t = make_xfer(i, i ^ d, 0, L, in, in, k == K ? RES : PART, k == K);
+      t.pair = 1;
+      st.xfers.push_back(t);
+    }
+    p->steps.push_back(st);
+  }
+}
+
+// The two trees of the double binary tree (primer §4.3, Fig. 4.6). Tree 1:
+// ranks 1..N-1 as the in-order binary tree -- rank r with lowest set bit
+// b >= 2 has children r - b/2 and r + b/2, the right offset halved until the
+// child is a rank below N -- whose top (the largest power of two below N)
+// hangs under the root, rank 0; odd ranks are leaves. Tree 2 mirrors it:
+// rank r becomes N-1-r. Children are kept in ascending rank order.
+struct Tree {
+  std::vector<int> parent, depth;
+  std::vector<std::vector<int>> children;
+};
+
+std::vector<Tree> double_binary_trees(int N) {
+  Tree t1;
+  t1.parent.assign(N, -1);
+  t1.children.assign(N, {});
+  auto link = [&](int a, int c) {
+    t1.parent[c] = a;
+    t1.children[a].push_back(c);
+  };
+  if (N > 1) {
+    int top = 1;
+    while (top * 2 <= N - 1) top *= 2;
+    link(0, top);
+    for (int r = 1; r < N; ++r) {
+      const int b = r & -r;
+      if (b < 2) continue;
+      link(r, r - b / 2);
+      int off = b / 2;
+      while (off >= 1 && r + off >= N) off /= 2;
+      if (off >= 1) link(r, r + off);
+    }
+  }
+  Tree t2;
+  t2.parent.assign(N, -1);
+  t2.children.assign(N, {});
+  for (int r = 0; r < N; ++r) {
+    const int m = N - 1 - r;
+    if (t1.parent[r] >= 0) t2.parent[m] = N - 1 - t1.parent[r];
+    for (int c : t1.children[r]) t2.children[m].push_back(N - 1 - c);
+  }
+  std::vector<Tree> trees = {t1, t2};
+  for (Tree& t : trees) {
+    for (auto& c : t.children) std::sort(c.begin(), c.end());
+    t.depth.assign(N, 0);
+    for (int r = 0; r < N; ++r)
+      for (int q = r; t.parent[q] >= 0; q = t.parent[q]) ++t.depth[r];
+  }
+  return trees;
+}
+
+// All-reduce over the double binary tree: tree t carries half t of the
+// buffer. Reduce, level by level from the deepest inner nodes up (both trees
+// in the same steps: the mirror has the same levels): an inner node folds
+// (own + first child) + second child into its partial sum, the root's sum
+// is final (scaled and rounded once). Broadcast, from the root down: each
+// parent's result overwrites its children's copies.
+void build_dbtree(ar_plan_t* p) {
+  const int N = p->desc.n_ranks;
+  const int64_t L = int64_t(p->desc.count);
+  const auto trees = double_binary_trees(N);
+  const auto half = cuts(0, L, 2);
+  int top = 0;
+  for (const Tree& t : trees)
+    for (int r = 0; r < N; ++r) top = std::max(top, t.depth[r]);
+  for (int level = top - 1; level >= 0; --level) {
+    Step st{OP_ADD, {}};
+    for (int ti = 0; ti < 2; ++ti) {
+      const Tree& t = trees[size_t(ti)];
+      for (int r = 0; r < N; ++r) {
+        const auto& ch = t.children[size_t(r)];
+        if (t.depth[size_t(r)] != level || ch.empty() || half[ti + 1] <= half[ti]) continue;
+        auto space = [&](int c) { return t.children[size_t(c)].empty() ? RAW : PART; };
+        const bool root = t.parent[size_t(r)] < 0;
+        Transfer x = make_xfer(ch[0], r, half[ti], half[ti + 1], space(ch[0]), RAW, root ? RES : PART, root);
+        if (ch.size() > 1) {
+          x.src2 = int16_t(ch[1]);
+          x.x2s = space(ch[1]);
+        }
+        st.xfers.push_back(x);
+      }
+    }
+    p->steps.push_back(st);
+  }
+  for (int level = 0; level < top; ++level) {
+    Step st{OP_COPY, {}};
+    for (int ti = 0; ti < 2; ++ti) {
+      const Tree& t = trees[size_t(ti)];
+      for (int r = 0; r < N; ++r)
+        if (t.depth[size_t(r)] == level)
+          for (int c : t.children[size_t(r)]) add_xfer(st, r, c, half[ti], half[ti + 1], RES, RES, RES, false);
+    }
+    p->steps.push_back(st);
+  }
+}
+
+// Dimension-ordered all-reduce on an X x Y x Z torus (Scaling ML Systems,
+// "Collective communication", torus section): rank (x, y, z) is
+// x + X*(y + Y*z); dimension by dimension every line of ranks along it runs
+// the ring all-reduce (ring rules as in build_ring, over the whole buffer cut
+// into D chunks). Between dimensions the lines' sums stay fp32 partials; the
+// last dimension's owners scale and round once.
+void build_torus(ar_plan_t* p) {
+  const int N = p->desc.n_ranks;
+  const int64_t L = int64_t(p->desc.count);
+  int dims[3];
+  for (int k = 0; k < 3; ++k) dims[k] = std::max(p->desc.torus_dims[k], 1);
+  const int stride[3] = {1, dims[0], dims[0] * dims[1]};
+  int last = -1;
+  for (int k = 0; k < 3; ++k)
+    if (dims[k] > 1) last = k;
+  bool first = true;
+  for (int k = 0; k < 3; ++k) {
+    const int D = dims[k];
+    if (D == 1) continue;
+    const auto b = cuts(0, L, D);
+    std::vector<int> heads;  // first rank of every line along dimension k
+    for (int r = 0; r < N; ++r)
+      if ((r / stride[k]) % D == 0) heads.push_back(r);
+    const bool fin_dim = k == last;
+    for (int s = 0; s <= D - 2; ++s) {
+      Step st{OP_ADD, {}};
+      const bool fin = fin_dim && s == D - 2;
+      for (int h : heads)
+        for (int q = 0; q < D; ++q) {
+          const int c = int(imod(q - s, D));
+          const Space xs = first ? (s == 0 ? RAW : PART) : PART;
+          add_xfer(st, h + q * stride[k], h + ((q + 1) % D) * stride[k], b[c], b[c + 1], xs, first ? RAW : PART,
+                   fin ? RES : PART, fin);
+        }
+      p->steps.push_back(st);
+    }
+    const Space sp = fin_dim ? RES : PART;
+    for (int s = 0; s <= D - 2; ++s) {
+      Step st{OP_COPY, {}};
+      for (int h : heads)
+        for (int q = 0; q < D; ++q) {
+          const int c = int(imod(q + 1 - s, D));
+          add_xfer(st, h + q * stride[k], h + ((q + 1) % D) * stride[k], b[c], b[c + 1], sp, sp, sp, false);
+        }
+      p->steps.push_back(st);
+    }
+    first = false;
+  }
+}
+
 size_t space_bytes(Space s, ar_dtype d) { return s == PART ? 4 : esize(d); }
+
+// Every point-to-point send a transfer stands for: (src, dst, bytes per
+// element). An exchange is two sends; a second source is one more.
+template <class F>
+void for_each_send(const Step& s, const Transfer& t, ar_dtype dt, F&& f) {
+  f(int(t.src), int(t.dst), space_bytes(Space(t.xs), dt));
+  if (s.op == OP_ADD && t.src2 >= 0) f(int(t.src2), int(t.dst), space_bytes(Space(t.x2s), dt));
+  if (s.op == OP_ADD && t.pair) f(int(t.dst), int(t.src), space_bytes(Space(t.ys), dt));
+}
+
+int launches_of(const Step& s) { return int((s.xfers.size() + kMaxXfers - 1) / kMaxXfers); }
 
 void compute_stats(ar_plan_t* p) {
   const ar_desc& d = p->desc;
@@ -239,17 +426,18 @@ void compute_stats(ar_plan_t* p) {
   st.steps = int(p->steps.size());
   std::vector<size_t> sent(N, 0);
   for (const Step& s : p->steps) {
-    if (!s.xfers.empty()) st.launches += 1;
+    st.launches += launches_of(s);
     for (const Transfer& t : s.xfers) {
       const size_t len = size_t(t.hi - t.lo);
+      for_each_send(s, t, d.dtype, [&](int src, int, size_t eb) { sent[size_t(src)] += len * eb; });
+      // every operand read once and every destination written once
+      size_t b = space_bytes(Space(t.xs), d.dtype) + space_bytes(Space(t.ds), d.dtype);
       if (s.op == OP_ADD) {
-        sent[t.src] += len * space_bytes(Space(t.xs), d.dtype);
-        st.hbm_bytes += len * (space_bytes(Space(t.xs), d.dtype) + space_bytes(Space(t.ys), d.dtype) +
-                               space_bytes(Space(t.ds), d.dtype));
-      } else {
-        sent[t.src] += len * space_bytes(Space(t.xs), d.dtype);
-        st.hbm_bytes += len * (space_bytes(Space(t.xs), d.dtype) + space_bytes(Space(t.ds), d.dtype));
+        b += space_bytes(Space(t.ys), d.dtype);
+        if (t.src2 >= 0) b += space_bytes(Space(t.x2s), d.dtype);
+        if (t.pair) b += space_bytes(Space(t.ds), d.dtype);
       }
+      st.hbm_bytes += len * b;
     }
   }
   st.bytes_sent_per_rank = N > 0 ? *std::max_element(sent.begin(), sent.end()) : 0;
@@ -371,7 +559,7 @@ ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs
     if (in_place && scale == 1.0f) return AR_OK;
     sp.scale = scale;
     sp.n_xfer = 1;
-    sp.x[0] = Transfer{0, 0, RAW, RAW, RES, 1, 0, int64_t(d.count)};
+    sp.x[0] = make_xfer(0, 0, 0, int64_t(d.count), RAW, RAW, RES, true);
     sp.tile_start[0] = 0;
     const int64_t body = std::max<int64_t>(rdown(d.count, kStepVec), 0);
     sp.tile_start[1] = int32_t(std::max<int64_t>(1, (body + kStepTile - 1) / kStepTile));
@@ -400,19 +588,22 @@ ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs
     }
   }
   for (const Step& st : p->steps) {
-    if (st.xfers.empty()) continue;
-    sp.n_xfer = int(st.xfers.size());
-    int tiles = 0;
-    for (int x = 0; x < sp.n_xfer; ++x) {
-      const Transfer& t = st.xfers[x];
-      sp.x[x] = t;
-      sp.tile_start[x] = tiles;
-      const int64_t body = std::max<int64_t>(rdown(t.hi, kStepVec) - rup(t.lo, kStepVec), 0);
-      tiles += int(std::max<int64_t>(1, (body + kStepTile - 1) / kStepTile));
+    // a step's transfers are independent (none writes what another reads), so
+    // a step with more transfers than one launch holds runs as several
+    for (size_t x0 = 0; x0 < st.xfers.size(); x0 += kMaxXfers) {
+      sp.n_xfer = int(std::min<size_t>(kMaxXfers, st.xfers.size() - x0));
+      int tiles = 0;
+      for (int x = 0; x < sp.n_xfer; ++x) {
+        const Transfer& t = st.xfers[x0 + size_t(x)];
+        sp.x[x] = t;
+        sp.tile_start[x] = tiles;
+        const int64_t body = std::max<int64_t>(rdown(t.hi, kStepVec) - rup(t.lo, kStepVec), 0);
+        tiles += int(std::max<int64_t>(1, (body + kStepTile - 1) / kStepTile));
+      }
+      sp.tile_start[sp.n_xfer] = tiles;
+      const ar_status s = from_cuda(launch_step(sp, d.dtype, st.op, tiles, true, d.sm_budget, stream));
+      if (s != AR_OK) return s;
     }
-    sp.tile_start[sp.n_xfer] = tiles;
-    const ar_status s = from_cuda(launch_step(sp, d.dtype, st.op, tiles, true, d.sm_budget, stream));
-    if (s != AR_OK) return s;
   }
   return AR_OK;
 }
@@ -469,7 +660,7 @@ ar_status ar_plan(const ar_desc* desc, ar_plan_t** out) {
     if (r.algo == AR_HIER) r.group_size = gs;
     return ar_plan(&r, out);
   }
-  if (d.algo < AR_RING || d.algo > AR_FUSED) return AR_EINVAL;
+  if (d.algo < AR_RING || d.algo > AR_TORUS || d.algo == AR_AUTO) return AR_EINVAL;
   if (!std::isfinite(d.scale)) return AR_EINVAL;
   if (d.count > (size_t(1) << 40)) return AR_EINVAL;
   if (d.collective < AR_ALLREDUCE || d.collective > AR_ALLGATHER) return AR_EINVAL;
@@ -479,11 +670,19 @@ ar_status ar_plan(const ar_desc* desc, ar_plan_t** out) {
     int stages = 0, tile_bytes = 0;
     if (d.collective != AR_ALLREDUCE || !tma_shape(N, stages, tile_bytes)) return AR_EUNSUPPORTED;
   }
+  if (d.algo == AR_TORUS) {
+    int prod = 1;
+    for (int k = 0; k < 3; ++k) {
+      if (d.torus_dims[k] < 0 || d.torus_dims[k] > AR_MAX_RANKS) return AR_EINVAL;
+      prod *= std::max(d.torus_dims[k], 1);
+    }
+    if (prod != N) return AR_EINVAL;
+  }
   if (d.collective != AR_ALLREDUCE) {
     if (d.algo != AR_RING && d.algo != AR_FUSED) return AR_EUNSUPPORTED;
     if (d.algo == AR_FUSED && d.order == AR_ORDER_HIER) return AR_EUNSUPPORTED;
   }
-  if (d.algo == AR_RABENSEIFNER && !is_pow2(N)) return AR_EINVAL;
+  if ((d.algo == AR_RABENSEIFNER || d.algo == AR_RECDOUBLING) && !is_pow2(N)) return AR_EINVAL;
   if (d.algo == AR_HIER && (d.group_size < 1 || N % d.group_size != 0)) return AR_EINVAL;
   if (d.algo == AR_FUSED) {
     if (d.order < AR_ORDER_RING || d.order > AR_ORDER_HIER) return AR_EINVAL;
@@ -495,12 +694,17 @@ ar_status ar_plan(const ar_desc* desc, ar_plan_t** out) {
   try {
     p->desc = d;
     if (d.algo != AR_HIER && !(d.algo == AR_FUSED && d.order == AR_ORDER_HIER)) p->desc.group_size = 0;
+    if (d.algo != AR_TORUS)
+      for (int k = 0; k < 3; ++k) p->desc.torus_dims[k] = 0;
     if (N > 1 && d.collective == AR_REDUCE_SCATTER) build_ring_reduce_scatter(p);
     if (N > 1 && d.collective == AR_ALLGATHER) build_ring_allgather(p);
     if (N > 1 && d.collective == AR_ALLREDUCE) {
       if (d.algo == AR_RING) build_ring(p);
       if (d.algo == AR_RABENSEIFNER) build_rabenseifner(p);
       if (d.algo == AR_HIER) build_hier(p);
+      if (d.algo == AR_RECDOUBLING) build_recdoubling(p);
+      if (d.algo == AR_DBTREE) build_dbtree(p);
+      if (d.algo == AR_TORUS) build_torus(p);
     }
     compute_stats(p);
   } catch (const std::bad_alloc&) {
@@ -531,15 +735,18 @@ ar_status ar_plan_transfers(const ar_plan_t* plan, int step, int* op, int* n_xfe
   if (plan->desc.algo == AR_FUSED || step < 0 || step >= int(plan->steps.size())) return AR_EINVAL;
   const Step& st = plan->steps[size_t(step)];
   *op = st.op == OP_ADD ? 0 : 1;
-  *n_xfers = int(st.xfers.size());
-  if (xfers != nullptr)
-    for (int i = 0; i < *n_xfers && i < max_xfers; ++i) {
-      const Transfer& t = st.xfers[size_t(i)];
-      xfers[4 * i + 0] = t.src;
-      xfers[4 * i + 1] = t.dst;
-      xfers[4 * i + 2] = t.lo;
-      xfers[4 * i + 3] = t.hi;
-    }
+  int n = 0;
+  for (const Transfer& t : st.xfers)
+    for_each_send(st, t, plan->desc.dtype, [&](int src, int dst, size_t) {
+      if (xfers != nullptr && n < max_xfers) {
+        xfers[4 * n + 0] = src;
+        xfers[4 * n + 1] = dst;
+        xfers[4 * n + 2] = t.lo;
+        xfers[4 * n + 3] = t.hi;
+      }
+      ++n;
+    });
+  *n_xfers = n;
   return AR_OK;
 }
 
@@ -677,10 +884,10 @@ ar_status ar_plan_predict(const ar_plan_t* plan, const ar_fabric* f, double* sec
   double T = 0;
   for (const Step& s : plan->steps) {
     double worst = 0;
-    for (const Transfer& t : s.xfers) {
-      const double bytes = double(t.hi - t.lo) * space_bytes(Space(t.xs), d.dtype);
-      worst = std::max(worst, bytes / bw(t.src, t.dst));
-    }
+    for (const Transfer& t : s.xfers)
+      for_each_send(s, t, d.dtype, [&](int src, int dst, size_t eb) {
+        worst = std::max(worst, double(t.hi - t.lo) * double(eb) / bw(src, dst));
+      });
     T += f->alpha + worst;
   }
   *seconds = T;
@@ -691,13 +898,18 @@ ar_status ar_select(const ar_desc* desc, const ar_fabric* f, ar_algo* algo, int*
                     double* seconds) {
   if (desc == nullptr || algo == nullptr || !fabric_ok(f)) return AR_EINVAL;
   const int N = desc->n_ranks;
-  std::vector<std::pair<ar_algo, int>> cand = {{AR_RING, 0}};
+  // earlier candidates win ties: the single pass first (with N = 2 an
+  // exchange moves the same bytes in the same one step)
+  std::vector<std::pair<ar_algo, int>> cand;
+  if (f->in_network || f->shared_memory) cand.push_back({AR_FUSED, 0});
+  cand.push_back({AR_RING, 0});
   if (desc->collective == AR_ALLREDUCE) {
     if (is_pow2(N)) cand.push_back({AR_RABENSEIFNER, 0});
+    if (is_pow2(N)) cand.push_back({AR_RECDOUBLING, 0});
+    cand.push_back({AR_DBTREE, 0});
     const int G = f->ranks_per_server;
     if (G > 1 && G < N && N % G == 0) cand.push_back({AR_HIER, G});
   }
-  if (f->in_network || f->shared_memory) cand.push_back({AR_FUSED, 0});
   bool found = false;
   double best = 0;
   ar_status last = AR_EINVAL;

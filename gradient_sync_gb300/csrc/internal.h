@@ -20,12 +20,15 @@ enum Space : uint8_t { RAW = 0, PART = 1, RES = 2 };
 enum StepOp : int { OP_ADD = 0, OP_COPY = 1, OP_FINISH = 2 };
 
 // One send/receive of a step: rank `dst` receives elements [lo, hi) from
-// rank `src`. ADD: dst_space[dst] = X[src] + Y[dst] (final: times scale,
-// rounded to the output type, written to RES). COPY: RES[dst] = RES[src].
-// FINISH (one rank): RES[dst] = scale * X[src], rounded to the output type.
+// rank `src`. ADD: D[dst] = X[src] + Y[dst], then + X2[src2] when src2 >= 0
+// (a tree node receiving from two children in one step); final: times scale,
+// rounded to the output type. With `pair`, src receives the same sum in
+// D[src] (an exchange: fp32 addition commutes, so both partners hold the
+// same bits). COPY: D[dst] = X[src], operands of one type. FINISH (one
+// rank): RES[dst] = scale * X[src], rounded to the output type.
 struct Transfer {
-  int16_t src, dst;
-  uint8_t xs, ys, ds, fin;
+  int16_t src, dst, src2;
+  uint8_t xs, ys, ds, x2s, fin, pair;
   int64_t lo, hi;
 };
 

@@ -14,7 +14,9 @@
 //
 // Within a step no transfer writes a range another transfer reads (every
 // rank receives a different piece than the one it sends), so a step is safe
-// in place.
+// in place. An exchange (`pair`: both partners receive the same sum, as in
+// recursive doubling) reads both copies of an element and writes both from
+// the same thread, so it is safe in place too.
 #include "common.cuh"
 
 namespace ar {
@@ -108,22 +110,27 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
     }
     const Transfer tr = p.x[lo_i];
     const int64_t tt = t - p.tile_start[lo_i];
-    const Operand X = operand<BF16>(p, tr.xs, tr.src);  // copies: RES, or RAW (own chunk)
+    const Operand X = operand<BF16>(p, tr.xs, tr.src);
     const Operand Y = operand<BF16>(p, tr.ys, tr.dst);
-    const Operand D = operand<BF16>(p, OP == OP_COPY ? RES : tr.ds, tr.dst);
+    const Operand D = operand<BF16>(p, tr.ds, tr.dst);
+    const bool two = OP == OP_ADD && tr.src2 >= 0;  // uniform over the transfer
+    const bool pair = OP == OP_ADD && tr.pair != 0;
+    const Operand X2 = operand<BF16>(p, tr.x2s, two ? tr.src2 : tr.dst);
+    const Operand D2 = operand<BF16>(p, tr.ds, tr.src);
     const bool fin = tr.fin != 0;
     const int64_t a0 = round_up(tr.lo, kStepVec);
     int64_t a1 = round_down(tr.hi, kStepVec);
     if (a1 < a0) a1 = a0;
 
     int64_t e[kStepUnroll];
-    Raw8 rx[kStepUnroll], ry[kStepUnroll];
+    Raw8 rx[kStepUnroll], ry[kStepUnroll], rz[kStepUnroll];
 #pragma unroll
     for (int u = 0; u < kStepUnroll; ++u) {
       e[u] = a0 + tt * kStepTile + (int64_t(u) * kThreads + threadIdx.x) * kStepVec;
       if (e[u] < a1) {
         rx[u] = load8(X, e[u]);
         if (OP == OP_ADD) ry[u] = load8(Y, e[u]);
+        if (two) rz[u] = load8(X2, e[u]);
       }
     }
 #pragma unroll
@@ -145,12 +152,18 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
             widen8(ry[u], Y.f32, g);
 #pragma unroll
             for (int w = 0; w < 8; ++w) f[w] = fadd(f[w], g[w]);
+            if (two) {
+              widen8(rz[u], X2.f32, g);
+#pragma unroll
+              for (int w = 0; w < 8; ++w) f[w] = fadd(f[w], g[w]);
+            }
           }
           if (fin) {
 #pragma unroll
             for (int w = 0; w < 8; ++w) f[w] = fmul(f[w], p.scale);
           }
           store8(D, e[u], f);
+          if (pair) store8(D2, e[u], f);
         }
       }
     }
@@ -167,8 +180,10 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
       if (es >= 0) {
         float v = load1(X, es);
         if (OP == OP_ADD) v = fadd(v, load1(Y, es));
+        if (two) v = fadd(v, load1(X2, es));
         if (OP != OP_COPY && fin) v = fmul(v, p.scale);
         store1(D, es, v);
+        if (pair) store1(D2, es, v);
       }
     }
   }

@@ -63,7 +63,34 @@ typedef enum { AR_F32 = 0, AR_BF16 = 1 } ar_dtype;
  * of every rank is read once and written once, the traffic of a rank that
  * sends its buffer once and receives the sum once (primer §4.4, "In-network
  * reduction"). */
-typedef enum { AR_RING = 0, AR_RABENSEIFNER = 1, AR_HIER = 2, AR_FUSED = 3, AR_AUTO = 4 } ar_algo;
+typedef enum {
+  AR_RING = 0,
+  AR_RABENSEIFNER = 1,
+  AR_HIER = 2,
+  AR_FUSED = 3,
+  AR_AUTO = 4,
+  AR_RECDOUBLING = 5, /* recursive doubling (primer §4.3, "Trees", Fig. 4.5):
+                         log2 N steps; in step k ranks i and i xor 2^(k-1)
+                         exchange whole buffers and both add. N a power of two.
+                         Its sum is the balanced tree of AR_ORDER_TREE. */
+  AR_DBTREE = 6,      /* double binary tree (primer §4.3, Fig. 4.6): tree 1 is
+                         root 0 over the in-order binary tree of ranks 1..N-1
+                         (rank r with lowest set bit b >= 2 has children
+                         r - b/2 and r + b/2, the right offset halved until the
+                         child is below N); tree 2 is its mirror, r -> N-1-r.
+                         Tree t carries half t of the buffer ([0, floor(L/2))
+                         and the rest): a reduce up the tree, level by level,
+                         inner nodes folding (own + first child) + second
+                         child in ascending rank order, then a broadcast down.
+                         About 2 log2 N steps. */
+  AR_TORUS = 7        /* dimension-ordered all-reduce on a torus (Scaling ML
+                         Systems, "Collective communication", torus section):
+                         ar_desc.torus_dims = {X, Y, Z} with X*Y*Z = N, rank
+                         (x, y, z) = x + X*(y + Y*z); a ring all-reduce along
+                         every X line, then every Y line, then every Z line,
+                         each over the whole buffer; partial sums stay fp32
+                         between dimensions. 2(X-1) + 2(Y-1) + 2(Z-1) steps. */
+} ar_algo;
 /* AR_AUTO: ar_plan picks the algorithm with ar_select under this GPU's own
  * fabric (virtual ranks in one HBM: every step costs AR_DEVICE_ALPHA_S plus
  * its HBM bytes at AR_DEVICE_BW, both measured on GB300) and records the
@@ -139,6 +166,8 @@ typedef struct {
                       the GPU, as a NCCL channel takes one SM (primer §4.5).
                       Results do not depend on it. */
   ar_kernel kernel; /* AR_KERNEL_AUTO (0) unless set */
+  int torus_dims[3]; /* AR_TORUS: {X, Y, Z}, a 0 counting as 1, product N
+                        (AR_EINVAL otherwise); ignored by the others */
 } ar_desc;
 
 /* Accounting of one ar_execute (primer §4.2 and §4.3 cost formulas). */
@@ -270,10 +299,12 @@ typedef struct {
 ar_status ar_plan_predict(const ar_plan_t* plan, const ar_fabric* fabric, double* seconds);
 
 /* The algorithm with the smallest predicted time for `desc` on `fabric`
- * among AR_RING, AR_RABENSEIFNER (N a power of two), AR_HIER with
+ * among AR_FUSED (in-network or shared memory), AR_RING, AR_RABENSEIFNER and
+ * AR_RECDOUBLING (N a power of two), AR_DBTREE, and AR_HIER with
  * group_size = ranks_per_server (when that divides N and lies strictly
- * between 1 and N) and AR_FUSED (in-network or shared memory); only AR_RING
- * and AR_FUSED for a reduce-scatter or all-gather. desc->algo is ignored.
+ * between 1 and N), in that order, an earlier one winning a tie; only
+ * AR_FUSED and AR_RING for a reduce-scatter or all-gather. AR_TORUS is never
+ * chosen (the fabric does not describe a torus). desc->algo is ignored.
  * Writes the choice to *algo (and its group size to *group_size if not NULL)
  * and its predicted time to *seconds (if not NULL). The choice NCCL makes per
  * call from its tables (primer §4.5), here from the model. */
@@ -285,7 +316,9 @@ ar_status ar_select(const ar_desc* desc, const ar_fabric* fabric, ar_algo* algo,
  * 1 = copy: the receiver overwrites) and *n_xfers, and, if xfers is not NULL,
  * up to max_xfers rows of 4 int64 values {src rank, dst rank, first element,
  * end element}: rank dst receives elements [first, end) from rank src. Empty
- * transfers (chunks with no elements) are omitted. AR_EINVAL for a NULL
+ * transfers (chunks with no elements) are omitted. An exchange (recursive
+ * doubling) is two rows, one per direction; a tree node receiving from two
+ * children in one step is two rows. AR_EINVAL for a NULL
  * plan/op/n_xfers, an AR_FUSED plan, or step out of range. */
 ar_status ar_plan_transfers(const ar_plan_t* plan, int step, int* op, int* n_xfers, int64_t* xfers,
                             int max_xfers);

@@ -28,7 +28,7 @@ def widened(x: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def expected(algo: str, order: str, x: np.ndarray, dtype: str, group_size: int = 0, scale: float = 1.0,
-             idx=None, L=None) -> np.ndarray:
+             idx=None, L=None, torus_dims=None) -> np.ndarray:
     """The oracle's result for one rank (all ranks are identical), as stored
     (fp32 values or bf16 bits)."""
     xf = widened(x, dtype)
@@ -42,6 +42,12 @@ def expected(algo: str, order: str, x: np.ndarray, dtype: str, group_size: int =
         out, _ = schedules.rabenseifner_allreduce(xf, idx=idx, L=L, finish=finish)
     elif algo == "hier":
         out, _ = schedules.hierarchical_allreduce(xf, group_size, idx=idx, L=L, finish=finish)
+    elif algo == "recdoubling":
+        out, _ = schedules.recursive_doubling_allreduce(xf, idx=idx, L=L, finish=finish)
+    elif algo == "dbtree":
+        out, _ = schedules.double_binary_tree_allreduce(xf, idx=idx, L=L, finish=finish)
+    elif algo == "torus":
+        out, _ = schedules.torus_allreduce(xf, torus_dims, idx=idx, L=L, finish=finish)
     else:
         raise ValueError(algo)
     for r in range(1, out.shape[0]):

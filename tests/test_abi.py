@@ -239,3 +239,72 @@ def test_kernel_choice_validation(g):
     with pytest.raises(g.ArError) as e:
         g.ar_bucket_allreduce(ok[:4], [10, 10, 10], 0, 3, "bf16", 0.5, stream=0, kernel=7)
     assert e.value.status == g.AR_EINVAL
+
+
+def _check_table(g, plan, st, steps, n_reduce):
+    stats = plan.stats
+    assert stats["steps"] == st.steps
+    for s in range(stats["steps"]):
+        op, rows = g.ar_plan_transfers(plan, s)
+        assert op == ("reduce" if s < n_reduce else "copy"), s
+        assert len(rows) == len(set(rows))
+        assert set(rows) == steps.get(s, set()), s
+    assert stats["bytes_sent_per_rank"] == 4 * int(st.elements_sent.max())
+
+
+@pytest.mark.parametrize("N,L", [(N, L) for N in (1, 2, 4, 8, 16, 64) for L in (0, 1, 7, 1001)])
+def test_recursive_doubling_table_matches_oracle(g, N, L):
+    plan = g.ar_plan(N, L, "f32", "recdoubling")
+    st, steps = _oracle_steps(schedules.recursive_doubling_allreduce, N, L)
+    K = N.bit_length() - 1
+    assert plan.stats["steps"] == K
+    _check_table(g, plan, st, steps, K)
+    # an exchange reads both copies and writes both once: 2 reads + 2 writes per pair
+    assert plan.stats["hbm_bytes"] == (4 * 4 * (N // 2) * L * K if N > 1 else 0)
+
+
+@pytest.mark.parametrize("N,L", [(N, L) for N in (1, 2, 3, 5, 8, 12, 16, 33, 64) for L in (0, 1, 2, 9, 1001)])
+def test_double_binary_tree_table_matches_oracle(g, N, L):
+    plan = g.ar_plan(N, L, "f32", "dbtree")
+    st, steps = _oracle_steps(schedules.double_binary_tree_allreduce, N, L)
+    _check_table(g, plan, st, steps, st.steps // 2)
+    assert plan.stats["hbm_bytes"] == 4 * (st.element_reads + st.element_writes)
+
+
+@pytest.mark.parametrize("dims,L", [((4, 4), 1000), ((2, 8), 77), ((8, 2), 4099), ((3, 5), 9), ((2, 3, 2), 100),
+                                    ((2, 2, 2), 0), ((1, 6), 31), ((5, 1), 5), ((4, 4, 4), 4096), ((1,), 8)])
+def test_torus_table_matches_oracle(g, dims, L):
+    N = int(np.prod(dims))
+    plan = g.ar_plan(N, L, "f32", "torus", torus_dims=dims)
+    st, steps = _oracle_steps(schedules.torus_allreduce, N, L, dims=dims, trace=lambda w: None)
+    assert plan.stats["steps"] == st.steps == sum(2 * (d - 1) for d in dims)
+    for s in range(plan.stats["steps"]):
+        op, rows = g.ar_plan_transfers(plan, s)
+        assert op == ("reduce" if "reduce-scatter" in st.trace[s][0] else "copy"), s
+        assert set(rows) == steps.get(s, set()), s
+    assert plan.stats["bytes_sent_per_rank"] == 4 * int(st.elements_sent.max())
+    assert plan.stats["hbm_bytes"] == 4 * (st.element_reads + st.element_writes)
+
+
+def test_variant_validation(g):
+    for N in (3, 6, 12):
+        with pytest.raises(g.ArError) as e:
+            g.ar_plan(N, 100, "f32", "recdoubling")
+        assert e.value.status == g.AR_EINVAL
+    for dims in ((4, 3), (0, 0, 0), (16, 2), (-1, 16), (65, 1, 1)):
+        with pytest.raises(g.ArError) as e:
+            g.ar_plan(16, 100, "f32", "torus", torus_dims=dims)
+        assert e.value.status == g.AR_EINVAL, dims
+    for algo in ("recdoubling", "dbtree"):
+        for coll in ("reduce_scatter", "allgather"):
+            with pytest.raises(g.ArError) as e:
+                g.ar_plan(8, 100, "f32", algo, collective=coll)
+            assert e.value.status == g.AR_EUNSUPPORTED
+    with pytest.raises(g.ArError) as e:
+        g.ar_plan(8, 100, "f32", 8)
+    assert e.value.status == g.AR_EINVAL
+    d = g.ar_plan_desc(g.ar_plan(16, 100, "f32", "torus", torus_dims=(4, 0, 4)))
+    assert d["torus_dims"] == (4, 0, 4)
+    assert g.ar_plan_desc(g.ar_plan(16, 100, "f32", "ring", torus_dims=(4, 4)))["torus_dims"] == (0, 0, 0)
+    # bf16 step plans keep fp32 partial sums in the workspace
+    assert g.ar_plan(16, 1000, "bf16", "torus", torus_dims=(4, 4)).stats["workspace_bytes"] == 16 * 1024 * 4

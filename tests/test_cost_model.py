@@ -67,17 +67,22 @@ def test_predictions_equal_the_oracle_round_model(g, N, L, G):
     fab = g.fabric(alpha, loc, net, ranks_per_server=G)
     bw = lambda s, d: loc if s // G == d // G else net  # noqa: E731
     algos = [("ring", schedules.ring_allreduce, {}), ("hier", schedules.hierarchical_allreduce, {"group_size": G})]
+    algos.append(("dbtree", schedules.double_binary_tree_allreduce, {}))
     if N & (N - 1) == 0:
         algos.append(("rabenseifner", schedules.rabenseifner_allreduce, {}))
+        algos.append(("recdoubling", schedules.recursive_doubling_allreduce, {}))
     for name, fn, kw in algos:
         got = g.ar_plan_predict(g.ar_plan(N, L, "f32", name, group_size=G), fab)
         assert got == pytest.approx(_oracle_round(fn, N, L, alpha, bw, **kw), rel=1e-12), name
+    dims = (G, N // G)
+    got = g.ar_plan_predict(g.ar_plan(N, L, "f32", "torus", torus_dims=dims), fab)
+    assert got == pytest.approx(_oracle_round(schedules.torus_allreduce, N, L, alpha, bw, dims=dims), rel=1e-12)
     for coll, fn in (("reduce_scatter", schedules.ring_reduce_scatter), ("allgather", schedules.ring_allgather)):
         got = g.ar_plan_predict(g.ar_plan(N, L, "f32", "ring", collective=coll), fab)
         assert got == pytest.approx(_oracle_round(fn, N, L, alpha, bw), rel=1e-12), coll
 
 
-def test_select_follows_the_model(g):
+def test_select_follows_the_model(g, golden):
     MiB_ = MiB
     book = g.fabric(ALPHA_BOOK, NVLINK, NIC, ranks_per_server=8)
     # 192 MiB on 2 x 8: distance-1-first halving keeps all but its last
@@ -89,9 +94,16 @@ def test_select_follows_the_model(g):
     # 12 ranks (no power of two): the hierarchy beats the flat ring
     algo, gs, _ = g.ar_select(12, 192 * MiB_ // 4, g.fabric(ALPHA_BOOK, NVLINK, NIC, ranks_per_server=6))
     assert (algo, gs) == ("hier", 6)
-    # small message on one server: fewer steps win (the primer's 1 MB example)
-    assert g.ar_select(8, 250_000, g.fabric(5e-6, NVLINK))[0] == "rabenseifner"
-    assert g.ar_select(6, 250_000, g.fabric(5e-6, NVLINK))[0] == "ring"
+    # small message on one server: fewer steps win. In the primer's 1 MB
+    # example recursive doubling's 3 rounds beat Rabenseifner's 6 and the
+    # ring's 14, at the time the page prints for doubling
+    algo, _, t = g.ar_select(8, 250_000, g.fabric(5e-6, NVLINK))
+    assert algo == "recdoubling"
+    check(golden("cost_model.txt"), "tp_doubling_s", t)
+    # 6 ranks (no doubling): the double binary tree's 6 rounds of S/2 beat
+    # the ring's 10 rounds of S/6 when alpha dominates
+    assert g.ar_select(6, 250_000, g.fabric(5e-6, NVLINK))[0] == "dbtree"
+    assert g.ar_select(6, 250_000_000, g.fabric(5e-6, NVLINK))[0] == "ring"
     # one shared memory: the single pass
     dev = g.fabric(g.AR_DEVICE_ALPHA_S, g.AR_DEVICE_BW, shared_memory=True)
     for N in (2, 3, 16, 64):
@@ -101,7 +113,7 @@ def test_select_follows_the_model(g):
 
 def test_device_model_is_launches_plus_bytes(g):
     dev = g.fabric(g.AR_DEVICE_ALPHA_S, g.AR_DEVICE_BW, shared_memory=True)
-    for algo in ("ring", "rabenseifner", "fused"):
+    for algo in ("ring", "rabenseifner", "fused", "recdoubling", "dbtree"):
         p = g.ar_plan(16, 50_331_648, "f32", algo)
         st = p.stats
         assert g.ar_plan_predict(p, dev) == pytest.approx(
