@@ -22,6 +22,9 @@ Modules:
                    ring reduce-scatter and all-gather, with per-rank mailboxes
                    and byte/step counters.
 * ``buckets``   -- DDP-style bucket assignment and the bucketed gradient sync.
+* ``compress``  -- blockwise INT8 quantization, error feedback, and the
+                   compressed all-reduce (every rank's message dequantized and
+                   summed in rank order).
 
 Parity pins: every function here is pinned by a test against a value the
 pages print, a closed form or brute force, except the bucket packing order
@@ -29,7 +32,7 @@ inside one bucket, which the pages do not fix (parity unpinned beyond the
 invariants listed in ``buckets``).
 """
 
-from . import buckets, chunks, numerics, schedules  # noqa: F401
+from . import buckets, chunks, compress, numerics, schedules  # noqa: F401
 from .chunks import chunk_bounds, chunk_of  # noqa: F401
 from .numerics import (bf16_to_f32, f32_to_bf16_rne, fused_sum, reference_sum_f64,  # noqa: F401
                        abs_sum_f64)

@@ -192,3 +192,63 @@ def test_mutant_torus_line_ring_starts_one_late(monkeypatch):
     _plant_ring_rule(monkeypatch, "dim X reduce-scatter", lambda p, s: p - 1 - s)
     with pytest.raises(AssertionError):
         variants.test_torus_order_closed_form((4, 4))
+
+
+# ---- blockwise INT8 compression and error feedback
+
+from oracle import compress  # noqa: E402
+import test_oracle_compress as comp  # noqa: E402
+
+
+def _plant_quantizer(monkeypatch, scale_of, round_fn=np.rint, whole_tensor=False):
+    def quantize(x, block):
+        x = np.asarray(x, np.float32)
+        b = x.size if whole_tensor else block
+        nb = compress.n_blocks(x.size, block)
+        codes = np.zeros(x.size, np.int8)
+        scales = np.zeros(nb, np.float32)
+        for k in range(compress.n_blocks(x.size, b)):
+            xb = x[k * b:(k + 1) * b]
+            s = scale_of(np.max(np.abs(xb)))
+            for j in range(k * b // block, min(nb, ((k + 1) * b + block - 1) // block)):
+                scales[j] = s
+            if s:
+                codes[k * b:(k + 1) * b] = np.clip(round_fn((xb / s).astype(np.float32)), -127, 127)
+        return codes, scales
+
+    monkeypatch.setattr(compress, "quantize_blockwise", quantize)
+
+
+def test_mutant_scale_over_128(monkeypatch):
+    _plant_quantizer(monkeypatch, lambda m: np.float32(np.float32(m) / np.float32(128)))
+    with pytest.raises(AssertionError):
+        comp.test_exact_grid_values()
+
+
+def test_mutant_one_scale_per_tensor(monkeypatch):
+    _plant_quantizer(monkeypatch, lambda m: np.float32(np.float32(m) / np.float32(127)), whole_tensor=True)
+    with pytest.raises(AssertionError):
+        comp.test_zero_tiny_and_ragged_blocks()
+
+
+def test_mutant_codes_truncated(monkeypatch):
+    _plant_quantizer(monkeypatch, lambda m: np.float32(np.float32(m) / np.float32(127)), round_fn=np.trunc)
+    with pytest.raises(AssertionError):
+        comp.test_codes_are_the_nearest_level_brute_force()
+
+
+def test_mutant_feedback_sign_flipped(monkeypatch):
+    def flipped(g, e, c):
+        x = g + e
+        v = c(x)
+        return v, v - x
+
+    monkeypatch.setattr(compress, "error_feedback_step", flipped)
+    with pytest.raises(AssertionError):
+        comp.test_error_feedback_worked_example(read_golden)
+
+
+def test_mutant_feedback_residual_dropped(monkeypatch):
+    monkeypatch.setattr(compress, "error_feedback_step", lambda g, e, c: (c(g), e * 0))
+    with pytest.raises(AssertionError):
+        comp.test_error_feedback_worked_example(read_golden)
