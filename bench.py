@@ -16,7 +16,9 @@ Reported (one JSON line from rank 0):
   roofline   the fused kernel's algorithmic bytes (2 N S) per launch / its
              CUDA-event launch time, against the measured HBM copy bandwidth
   executors  the step-by-step ring and Rabenseifner on the same workload,
-             each against its own byte count, 5(N-1) S
+             each against its own byte count, 5(N-1) S; and the blockwise
+             INT8 compressed all-reduce with error feedback (fused pass, and
+             compressor + reducer), each against its own byte count
   e2e        the same all-reduce from pinned host buffers through
              ar_execute_host, copies included
   cpu_baseline  the CPU oracle (step-by-step ring simulation) on a bounded
@@ -300,6 +302,36 @@ def run_ours(args):
                            "steps": pst["steps"], "launches": pst["launches"],
                            "hbm_bytes": pst["hbm_bytes"], "achieved_gbs": round(bw, 1),
                            "frac_of_hbm": round(bw / hbm_peak, 4)}
+
+    # blockwise INT8 compressed all-reduce with error feedback (block 128, sum
+    # scaled by 1/N) on the same gradients: the fused pass and the two calls
+    from gradient_sync_gb300.cases import compressed_hbm_bytes
+
+    block = 128
+    res = [torch.zeros(L, dtype=torch.float32, device=dev) for _ in range(N)]
+    n_sc, _ = g.ar_compress_sizes(L, block)
+    codes = [torch.empty(L, dtype=torch.int8, device=dev) for _ in range(N)]
+    scales = [torch.empty(n_sc, dtype=torch.float32, device=dev) for _ in range(N)]
+    handle = int(stream.cuda_stream)
+
+    def comp_fused():
+        g.ar_compressed_allreduce(bufs, block, residuals=res, scale=1.0 / N, outs=outs, stream=handle)
+
+    def comp_two():
+        g.ar_compress(bufs, codes, scales, block, residuals=res, stream=handle)
+        g.ar_compressed_reduce(codes, scales, outs, block, scale=1.0 / N, stream=handle)
+
+    for name, fn, path, launches in (("compressed_int8_fused", comp_fused, "fused", 1),
+                                     ("compressed_int8_two_calls", comp_two, "two", 2)):
+        k = max(5, args.steps // 20)
+        ms_c = timed(dist, fn, sync, k, args.warmup, local if dist else None, event_timer) / k
+        hb = compressed_hbm_bytes(N, L, "f32", block, path, True)
+        bw = hb / (ms_c * 1e-3) / 1e9
+        executors[name] = {"ms": round(ms_c, 4), "algbw": round(S / (ms_c * 1e-3) / 1e9, 2), "block": block,
+                           "error_feedback": True, "launches": launches, "hbm_bytes": hb,
+                           "achieved_gbs": round(bw, 1), "frac_of_hbm": round(bw / hbm_peak, 4)}
+    del res, codes, scales
+    torch.cuda.empty_cache()
 
     # end to end: pinned host buffers in and out through ar_execute_host
     host_in = [torch.from_numpy(h).pin_memory() for h in host]

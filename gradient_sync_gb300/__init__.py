@@ -245,6 +245,49 @@ def ar_bucket_allreduce(tensors, counts, t_begin: int, t_end: int, dtype, scale:
                                            _stream(stream)), "ar_bucket_allreduce")
 
 
+# ---------------------------------------------------------------- compression
+
+AR_COMPRESS_MIN_BLOCK, AR_COMPRESS_MAX_BLOCK = 16, 1024
+
+
+def ar_compress_sizes(count: int, block: int):
+    """(number of scales, message bytes) of one rank's compressed message."""
+    ns, mb = _lib.c_size_t(), _lib.c_size_t()
+    _check(_lib.load().ar_compress_sizes(int(count), int(block), ns, mb), "ar_compress_sizes")
+    return ns.value, mb.value
+
+
+def ar_compress(grads, codes, scales, block: int, dtype="f32", residuals=None, count=None, stream=None):
+    """Blockwise INT8 compression of every rank's gradient (with error feedback
+    when ``residuals`` is given: read as e, overwritten with the new residual)."""
+    n = len(grads)
+    count = grads[0].numel() if count is None else count
+    res = _ptrs(residuals) if residuals is not None else None
+    _check(_lib.load().ar_compress(n, int(count), int(block), DTYPES.get(dtype, dtype), _ptrs(grads), res,
+                                   _ptrs(codes), _ptrs(scales), _stream(stream)), "ar_compress")
+
+
+def ar_compressed_reduce(codes, scales, outs, block: int, scale: float = 1.0, out_dtype="f32", count=None,
+                         stream=None):
+    """Sum the ranks' compressed messages in rank order into every ``outs[r]``."""
+    n = len(codes)
+    count = codes[0].numel() if count is None else count
+    _check(_lib.load().ar_compressed_reduce(n, int(count), int(block), _ptrs(codes), _ptrs(scales), float(scale),
+                                            DTYPES.get(out_dtype, out_dtype), _ptrs(outs), _stream(stream)),
+           "ar_compressed_reduce")
+
+
+def ar_compressed_allreduce(grads, block: int, dtype="f32", residuals=None, scale: float = 1.0, outs=None,
+                            count=None, stream=None):
+    """Compression and reduction in one pass (in place unless ``outs``)."""
+    n = len(grads)
+    count = grads[0].numel() if count is None else count
+    res = _ptrs(residuals) if residuals is not None else None
+    o = _ptrs(outs) if outs is not None else None
+    _check(_lib.load().ar_compressed_allreduce(n, int(count), int(block), DTYPES.get(dtype, dtype), _ptrs(grads),
+                                               res, float(scale), o, _stream(stream)), "ar_compressed_allreduce")
+
+
 # ---------------------------------------------------------------- status
 
 

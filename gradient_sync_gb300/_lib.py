@@ -48,6 +48,11 @@ SIGNATURES = {
                                  c_void_p]),
     "ar_bucket_allreduce": (c_int, [c_int, VOIDPP, SIZEP, c_int, c_int, c_int, c_int, c_float, c_int, c_int,
                                     c_void_p]),
+    "ar_compress_sizes": (c_int, [c_size_t, c_int, SIZEP, SIZEP]),
+    "ar_compress": (c_int, [c_int, c_size_t, c_int, c_int, VOIDPP, VOIDPP, VOIDPP, VOIDPP, c_void_p]),
+    "ar_compressed_reduce": (c_int, [c_int, c_size_t, c_int, VOIDPP, VOIDPP, c_float, c_int, VOIDPP, c_void_p]),
+    "ar_compressed_allreduce": (c_int, [c_int, c_size_t, c_int, c_int, VOIDPP, VOIDPP, c_float, VOIDPP,
+                                        c_void_p]),
     "ar_device_status": (c_int, [c_int]),
     "ar_selftest_wait_timeout": (c_int, [ctypes.c_uint, c_void_p]),
     "ar_status_string": (ctypes.c_char_p, [c_int]),

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libar_gb300.so")
 
-CUDA_SOURCES = ["fused.cu", "fused_tma.cu", "step.cu", "pack.cu", "noalloc.cu"]
+CUDA_SOURCES = ["fused.cu", "fused_tma.cu", "step.cu", "pack.cu", "noalloc.cu", "compress.cu"]
 CXX_SOURCES = ["api.cpp"]
 HEADERS = ["internal.h", "common.cuh", "bulk.cuh"]
 

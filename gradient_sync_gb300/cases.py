@@ -4,6 +4,7 @@
     python -m gradient_sync_gb300.cases --sweep > sweep.jsonl
     python -m gradient_sync_gb300.cases --buckets fused|pack --iters 5
     python -m gradient_sync_gb300.cases --overlap --n 8 --tokens 4096 --sm-budget 32 --iters 5
+    python -m gradient_sync_gb300.cases --compressed fused|two --n 16 --count 50331648 --block 128
 
 Each timed case prints one JSON line: time per call (median of CUDA-event
 timings on the launching stream, after warm-up), algbw = S/T, busbw =
@@ -164,6 +165,72 @@ def time_buckets(n=8, path="fused", iters=5, warmup=2, cap_bytes=25 * MiB):
     return res
 
 
+def compressed_hbm_bytes(n, count, dtype="f32", block=128, path="fused", ef=True):
+    """Algorithmic HBM bytes of one compressed all-reduce: every element and
+    scale read or written counted once per access at its storage width. Fused:
+    gradients read, results written to every rank, residuals read and
+    rewritten. Two calls: the compressor reads gradients (and residuals) and
+    writes codes, scales (and residuals); the reducer reads codes and scales
+    and writes every rank's result."""
+    esz = 4 if dtype == "f32" else 2
+    nb = (count + block - 1) // block
+    res = 8 * n * count if ef else 0
+    if path == "fused":
+        return n * count * 2 * esz + res
+    return n * count * (esz + 1) + 4 * n * nb + res + n * count + 4 * n * nb + n * count * esz
+
+
+def time_compressed(n=16, count=50_331_648, dtype="f32", block=128, path="fused", ef=True, iters=10, warmup=3):
+    """Time the blockwise INT8 compressed all-reduce (error feedback on when
+    ``ef``; sum scaled by 1/n): the fused single pass, or the compressor and
+    the reducer as two calls with the messages in HBM between them."""
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    grads = [torch.randn(count, device="cuda").mul_(1e-3).to(tdt) for _ in range(n)]
+    outs = [torch.empty_like(t) for t in grads]
+    res = [torch.zeros(count, device="cuda") for _ in range(n)] if ef else None
+    nb, _ = g.ar_compress_sizes(count, block)
+    if path == "two":
+        codes = [torch.empty(count, dtype=torch.int8, device="cuda") for _ in range(n)]
+        scales = [torch.empty(nb, dtype=torch.float32, device="cuda") for _ in range(n)]
+        launches = 2
+
+        def call():
+            g.ar_compress(grads, codes, scales, block, dtype=dtype, residuals=res)
+            g.ar_compressed_reduce(codes, scales, outs, block, scale=1.0 / n, out_dtype=dtype)
+    else:
+        launches = 1
+
+        def call():
+            g.ar_compressed_allreduce(grads, block, dtype=dtype, residuals=res, scale=1.0 / n, outs=outs)
+    hbm = compressed_hbm_bytes(n, count, dtype, block, path, ef)
+    reps = max(1, min(200, (256 * MiB) // max(1, hbm)))
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(iters):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            call()
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b) / reps)
+    times.sort()
+    ms = times[len(times) // 2]
+    S = count * (4 if dtype == "f32" else 2)
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    bw = hbm / (ms * 1e-3) / 1e9
+    out = {"workload": "blockwise INT8 compressed all-reduce", "n": n, "count": count, "dtype": dtype,
+           "block": block, "path": path, "error_feedback": ef, "us": round(ms * 1e3, 2),
+           "algbw": round(S / (ms * 1e-3) / 1e9, 2), "launches": launches, "hbm_bytes": hbm,
+           "hbm_gbs": round(bw, 1), "hbm_frac": round(bw / hbm_peak(), 4) if hbm > 8 * l2 else None}
+    del grads, outs, res
+    torch.cuda.empty_cache()
+    return out
+
+
 def sweep(out=sys.stdout, max_total=64 * GiB, graph=False):
     for n in (2, 4, 8, 16, 64):
         for k in range(11):
@@ -196,12 +263,20 @@ def main(argv=None):
     ap.add_argument("--sm-budget", type=int, default=0)
     ap.add_argument("--kernel", default="auto", choices=["auto", "loads", "bulk"])
     ap.add_argument("--dims", default="0,0,0", help="torus dimensions X,Y[,Z] for --algo torus")
+    ap.add_argument("--compressed", choices=["fused", "two"], default=None,
+                    help="blockwise INT8 compressed all-reduce (fused pass or compressor + reducer)")
+    ap.add_argument("--block", type=int, default=128)
+    ap.add_argument("--no-ef", action="store_true", help="compressed all-reduce without error feedback")
     a = ap.parse_args(argv)
     from gradient_sync_gb300 import build
 
     build.build()
     if a.sweep:
         sweep(graph=a.graph)
+        return
+    if a.compressed:
+        print(json.dumps(time_compressed(a.n, a.count, a.dtype, a.block, a.compressed, not a.no_ef,
+                                         a.iters, a.warmup)))
         return
     if a.buckets:
         print(json.dumps(time_buckets(path=a.buckets, iters=a.iters, warmup=min(a.warmup, 3))))

@@ -1106,6 +1106,131 @@ ar_status ar_bucket_allreduce(int n_ranks, void* const* tensors, const size_t* c
   return flush();
 }
 
+// ---------------------------------------------------------------- compression
+
+namespace {
+
+bool valid_block(int block) {
+  return block >= AR_COMPRESS_MIN_BLOCK && block <= AR_COMPRESS_MAX_BLOCK && (block & (block - 1)) == 0;
+}
+
+size_t n_scale_blocks(size_t count, int block) { return (count + size_t(block) - 1) / size_t(block); }
+
+// Checks shared by the compression calls: ranks, block, the pointer arrays
+// (each pointer non-NULL and 16-byte aligned; residuals may be a NULL array).
+ar_status check_compress_common(int n_ranks, int block, const void* const* a, const void* const* b) {
+  if (n_ranks < 1 || n_ranks > AR_MAX_RANKS || !valid_block(block)) return AR_EINVAL;
+  if (a == nullptr || b == nullptr) return AR_EINVAL;
+  for (int r = 0; r < n_ranks; ++r)
+    if (check_ptr(a[r]) != AR_OK || check_ptr(b[r]) != AR_OK) return AR_EINVAL;
+  return AR_OK;
+}
+
+void add_ranges(std::vector<std::pair<uintptr_t, uintptr_t>>& iv, const void* const* ptrs, int n, size_t bytes) {
+  for (int r = 0; r < n; ++r) iv.push_back({uintptr_t(ptrs[r]), uintptr_t(ptrs[r]) + bytes});
+}
+
+CompressParams compress_params(int n_ranks, size_t count, int block, float scale) {
+  CompressParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.n = n_ranks;
+  p.block = block;
+  p.count = int64_t(count);
+  p.n_blocks = int64_t(n_scale_blocks(count, block));
+  p.scale = scale;
+  return p;
+}
+
+}  // namespace
+
+ar_status ar_compress_sizes(size_t count, int block, size_t* n_scales, size_t* message_bytes) {
+  if (!valid_block(block)) return AR_EINVAL;
+  const size_t nb = n_scale_blocks(count, block);
+  if (n_scales != nullptr) *n_scales = nb;
+  if (message_bytes != nullptr) *message_bytes = count + 4 * nb;
+  return AR_OK;
+}
+
+ar_status ar_compress(int n_ranks, size_t count, int block, ar_dtype dtype, const void* const* grads,
+                      void* const* residuals, void* const* codes, void* const* scales, void* stream) {
+  ar_status s = check_compress_common(n_ranks, block, grads, codes);
+  if (s != AR_OK) return s;
+  if (dtype != AR_F32 && dtype != AR_BF16) return AR_EINVAL;
+  if (scales == nullptr) return AR_EINVAL;
+  for (int r = 0; r < n_ranks; ++r) {
+    if (check_ptr(scales[r]) != AR_OK) return AR_EINVAL;
+    if (residuals != nullptr && check_ptr(residuals[r]) != AR_OK) return AR_EINVAL;
+  }
+  if (count == 0) return AR_OK;
+  std::vector<std::pair<uintptr_t, uintptr_t>> iv;
+  add_ranges(iv, grads, n_ranks, count * esize(dtype));
+  add_ranges(iv, codes, n_ranks, count);
+  add_ranges(iv, scales, n_ranks, 4 * n_scale_blocks(count, block));
+  if (residuals != nullptr) add_ranges(iv, residuals, n_ranks, 4 * count);
+  if (!disjoint(iv)) return AR_EINVAL;
+  CompressParams p = compress_params(n_ranks, count, block, 1.0f);
+  p.ef = residuals != nullptr;
+  for (int r = 0; r < n_ranks; ++r) {
+    p.g[r] = grads[r];
+    p.q[r] = static_cast<int8_t*>(codes[r]);
+    p.s[r] = static_cast<float*>(scales[r]);
+    p.e[r] = residuals != nullptr ? static_cast<float*>(residuals[r]) : nullptr;
+  }
+  return from_cuda(launch_compress(p, dtype, static_cast<cudaStream_t>(stream)));
+}
+
+ar_status ar_compressed_reduce(int n_ranks, size_t count, int block, const void* const* codes,
+                               const void* const* scales, float scale, ar_dtype out_dtype, void* const* outs,
+                               void* stream) {
+  ar_status s = check_compress_common(n_ranks, block, codes, scales);
+  if (s != AR_OK) return s;
+  if (out_dtype != AR_F32 && out_dtype != AR_BF16) return AR_EINVAL;
+  if (!std::isfinite(scale) || outs == nullptr) return AR_EINVAL;
+  for (int r = 0; r < n_ranks; ++r)
+    if (check_ptr(outs[r]) != AR_OK) return AR_EINVAL;
+  if (count == 0) return AR_OK;
+  std::vector<std::pair<uintptr_t, uintptr_t>> iv;
+  add_ranges(iv, codes, n_ranks, count);
+  add_ranges(iv, scales, n_ranks, 4 * n_scale_blocks(count, block));
+  add_ranges(iv, outs, n_ranks, count * esize(out_dtype));
+  if (!disjoint(iv)) return AR_EINVAL;
+  CompressParams p = compress_params(n_ranks, count, block, scale);
+  for (int r = 0; r < n_ranks; ++r) {
+    p.q[r] = static_cast<int8_t*>(const_cast<void*>(codes[r]));
+    p.s[r] = static_cast<float*>(const_cast<void*>(scales[r]));
+    p.out[r] = outs[r];
+  }
+  return from_cuda(launch_compressed_reduce(p, out_dtype, static_cast<cudaStream_t>(stream)));
+}
+
+ar_status ar_compressed_allreduce(int n_ranks, size_t count, int block, ar_dtype dtype, const void* const* grads,
+                                  void* const* residuals, float scale, void* const* outs, void* stream) {
+  if (outs == nullptr) outs = const_cast<void* const*>(grads);  // in place
+  ar_status s = check_compress_common(n_ranks, block, grads, outs);
+  if (s != AR_OK) return s;
+  if (dtype != AR_F32 && dtype != AR_BF16) return AR_EINVAL;
+  if (!std::isfinite(scale)) return AR_EINVAL;
+  if (residuals != nullptr)
+    for (int r = 0; r < n_ranks; ++r)
+      if (check_ptr(residuals[r]) != AR_OK) return AR_EINVAL;
+  if (count == 0) return AR_OK;
+  std::vector<std::pair<uintptr_t, uintptr_t>> iv;
+  const size_t bytes = count * esize(dtype);
+  add_ranges(iv, grads, n_ranks, bytes);
+  for (int r = 0; r < n_ranks; ++r)
+    if (outs[r] != grads[r]) iv.push_back({uintptr_t(outs[r]), uintptr_t(outs[r]) + bytes});
+  if (residuals != nullptr) add_ranges(iv, residuals, n_ranks, 4 * count);
+  if (!disjoint(iv)) return AR_EINVAL;
+  CompressParams p = compress_params(n_ranks, count, block, scale);
+  p.ef = residuals != nullptr;
+  for (int r = 0; r < n_ranks; ++r) {
+    p.g[r] = grads[r];
+    p.out[r] = outs[r];
+    p.e[r] = residuals != nullptr ? static_cast<float*>(residuals[r]) : nullptr;
+  }
+  return from_cuda(launch_compressed_allreduce(p, dtype, static_cast<cudaStream_t>(stream)));
+}
+
 // ---------------------------------------------------------------- status
 
 ar_status ar_device_status(int clear) {

@@ -106,6 +106,23 @@ struct PackParams {
   int32_t tile_start[AR_MAX_BUCKET_TENSORS + 1];  // tiles per tensor (one rank)
 };
 
+// Blockwise INT8 compression (compress.cu). One parameter block serves the
+// three kernels: compress (g, e -> q, s, e'), the message reducer (q, s ->
+// out) and the fused single pass (g, e -> e', out).
+struct CompressParams {
+  const void* g[AR_MAX_RANKS];  // gradients, in the call's dtype
+  float* e[AR_MAX_RANKS];       // residuals (error feedback), fp32; unused when !ef
+  int8_t* q[AR_MAX_RANKS];      // codes, one byte per element
+  float* s[AR_MAX_RANKS];       // scales, one fp32 per block
+  void* out[AR_MAX_RANKS];      // results, in the call's output dtype
+  int n;                        // ranks
+  int block;                    // elements per quantisation block (power of two, 16..1024)
+  int ef;                       // 1: residuals given
+  int64_t count;                // elements per rank
+  int64_t n_blocks;             // ceil(count / block)
+  float scale;                  // multiplies the complete fp32 sum once
+};
+
 // ---- launchers (defined in the .cu files) ----
 // Tile sizes the launchers and the host planner agree on (elements).
 constexpr int kThreads = 256;
@@ -128,5 +145,9 @@ cudaError_t launch_fused_tma(const FusedParams& p, ar_dtype dtype, int stages, i
 cudaError_t launch_bucket_tma(const BucketFusedParams& p, ar_dtype dtype, int stages, int tile_bytes, int sm_budget,
                               cudaStream_t stream);
 cudaError_t launch_wait_timeout(uint32_t polls, cudaStream_t stream);
+// Blockwise INT8 compression (compress.cu).
+cudaError_t launch_compress(const CompressParams& p, ar_dtype dtype, cudaStream_t stream);
+cudaError_t launch_compressed_reduce(const CompressParams& p, ar_dtype out_dtype, cudaStream_t stream);
+cudaError_t launch_compressed_allreduce(const CompressParams& p, ar_dtype dtype, cudaStream_t stream);
 
 }  // namespace ar

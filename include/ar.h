@@ -369,6 +369,75 @@ ar_status ar_bucket_allreduce(int n_ranks, void* const* tensors, const size_t* c
                               int t_begin, int t_end, ar_dtype dtype, float scale, int sm_budget,
                               ar_kernel kernel, void* stream);
 
+/* ---------------------------------------------------------------- compression
+ * Blockwise INT8 gradient compression with error feedback (Scaling ML
+ * Systems, "Collective communication", the section on gradient compression:
+ * "Quantization: reducing precision" gives the INT8 scale max|g| / 127 and the
+ * codes round(g / scale); "Blockwise quantization for gradient communication"
+ * gives one scale per block of b elements and a message of d one-byte codes
+ * plus 4 bytes of fp32 scale per block; "Error feedback and residual
+ * accumulation" gives x = g + e, transmit C(x), keep e' = x - C(x)).
+ *
+ * Arithmetic, per rank and block k = [k*block, min((k+1)*block, count)) (the
+ * last block may be short), every operation one IEEE fp32 operation rounded to
+ * nearest even:
+ *   x = g + e (x = g without error feedback; bf16 g widened exactly)
+ *   s = max|x| / 127
+ *   q = the nearest integer to x / s, ties to even, clamped to [-127, 127];
+ *       q = 0 for every element of a block whose s is 0
+ *   d = q * s (the value the receiver reconstructs)
+ *   e' = x - d
+ * The page writes round() without a tie rule; ties to even (the IEEE default)
+ * is this library's reading. The reduction sums the N ranks' d in rank order,
+ * ((d_0 + d_1) + ...) + d_{N-1}, multiplies by `scale` once and rounds once to
+ * the output type (bf16: nearest even); no partial sum is re-quantised (the
+ * page's interfaces that fuse quantisation and reduction).
+ *
+ * Layout: rank r's codes are `count` int8 values (codes[r][e] for element e),
+ * its scales ceil(count / block) fp32 values (scales[r][k] for block k), its
+ * residuals `count` fp32 values. block is a power of two from
+ * AR_COMPRESS_MIN_BLOCK to AR_COMPRESS_MAX_BLOCK (the page's typical sizes are
+ * 64 and 128). count == 0 enqueues nothing. Buffers follow the conventions at
+ * the top of this file (caller-owned device memory, 16-byte aligned, no
+ * overlaps unless stated). */
+#define AR_COMPRESS_MIN_BLOCK 16
+#define AR_COMPRESS_MAX_BLOCK 1024
+
+/* Sizes of one rank's message for `count` elements: *n_scales = ceil(count /
+ * block) and *message_bytes = count + 4 * ceil(count / block), the page's d +
+ * 4d/b (either output may be NULL). Host only. AR_EINVAL: block not a power of
+ * two in [AR_COMPRESS_MIN_BLOCK, AR_COMPRESS_MAX_BLOCK]. */
+ar_status ar_compress_sizes(size_t count, int block, size_t* n_scales, size_t* message_bytes);
+
+/* Compress every rank's gradient into its message (the sending side).
+ *  grads[r]:     count elements of dtype (AR_F32 or AR_BF16), read only.
+ *  residuals:    NULL for no error feedback, or residuals[r] = rank r's fp32
+ *                residual e (count values): read as e, overwritten with e'.
+ *  codes[r]:     count int8 codes, written.
+ *  scales[r]:    ceil(count / block) fp32 scales, written.
+ * AR_EINVAL: n_ranks outside 1..AR_MAX_RANKS; a bad block or dtype; a NULL
+ * array; a NULL or misaligned pointer; overlapping buffers. */
+ar_status ar_compress(int n_ranks, size_t count, int block, ar_dtype dtype, const void* const* grads,
+                      void* const* residuals, void* const* codes, void* const* scales, void* stream);
+
+/* Sum the N ranks' messages (the receiving side): every outs[r] (count
+ * elements of out_dtype) is written with round(scale * sum over ranks in rank
+ * order of codes[r'][e] * scales[r'][e / block]). codes and scales as written
+ * by ar_compress. AR_EINVAL as ar_compress, and for a non-finite scale. */
+ar_status ar_compressed_reduce(int n_ranks, size_t count, int block, const void* const* codes,
+                               const void* const* scales, float scale, ar_dtype out_dtype, void* const* outs,
+                               void* stream);
+
+/* ar_compress followed by ar_compressed_reduce in one pass, without message
+ * buffers: every element of every rank is read once (with its residual) and
+ * the result written once to every rank; with error feedback each residual is
+ * read and rewritten once. The results (outputs and residuals) are
+ * bit-identical to the two calls. outs: NULL for in place (results overwrite
+ * grads), else outs[r] may equal grads[r]. Output dtype = dtype.
+ * AR_EINVAL as ar_compress, and for a non-finite scale. */
+ar_status ar_compressed_allreduce(int n_ranks, size_t count, int block, ar_dtype dtype, const void* const* grads,
+                                  void* const* residuals, float scale, void* const* outs, void* stream);
+
 /* ---------------------------------------------------------------- status */
 
 /* Read (and clear, if clear != 0) the calling device's sticky status word,

@@ -308,3 +308,49 @@ def test_variant_validation(g):
     assert g.ar_plan_desc(g.ar_plan(16, 100, "f32", "ring", torus_dims=(4, 4)))["torus_dims"] == (0, 0, 0)
     # bf16 step plans keep fp32 partial sums in the workspace
     assert g.ar_plan(16, 1000, "bf16", "torus", torus_dims=(4, 4)).stats["workspace_bytes"] == 16 * 1024 * 4
+
+
+def test_compress_sizes_match_oracle(g):
+    from oracle import compress as ocomp
+
+    for count in (0, 1, 15, 16, 17, 1000, 4099, 1 << 20, 50_331_648):
+        for b in (16, 32, 64, 128, 256, 512, 1024):
+            ns, mb = g.ar_compress_sizes(count, b)
+            assert ns == ocomp.n_blocks(count, b)
+            assert mb == ocomp.message_bytes(count, b)
+    for b in (0, 8, 15, 48, 100, 2048, -64):
+        with pytest.raises(g.ArError) as e:
+            g.ar_compress_sizes(100, b)
+        assert e.value.status == g.AR_EINVAL
+
+
+def test_compression_calls_reject_without_touching_the_device(g):
+    N, L, b = 3, 1000, 64
+    base = [0x1000000 * (k + 1) for k in range(20)]
+    grads, codes, scales, res, outs = base[0:3], base[3:6], base[6:9], base[9:12], base[12:15]
+
+    def rejects(fn, *a, **kw):
+        with pytest.raises(g.ArError) as e:
+            fn(*a, count=L, stream=0, **kw)
+        assert e.value.status == g.AR_EINVAL
+
+    for blk in (8, 100, 2048):
+        rejects(g.ar_compress, grads, codes, scales, blk)
+        rejects(g.ar_compressed_reduce, codes, scales, outs, blk)
+        rejects(g.ar_compressed_allreduce, grads, blk)
+    rejects(g.ar_compress, grads, codes, scales, b, dtype=5)
+    rejects(g.ar_compress, [grads[0] + 4] + grads[1:], codes, scales, b)          # misaligned
+    rejects(g.ar_compress, grads, [0] + codes[1:], scales, b)                     # null
+    rejects(g.ar_compress, grads, codes, [codes[0] + 512] + scales[1:], b)        # scales overlap codes
+    rejects(g.ar_compress, grads, codes, scales, b, residuals=[grads[1]] + res[1:])  # residual = a gradient
+    rejects(g.ar_compressed_reduce, codes, scales, outs, b, scale=float("nan"))
+    rejects(g.ar_compressed_reduce, codes, scales, [codes[1]] + outs[1:], b)      # output over codes
+    rejects(g.ar_compressed_allreduce, grads, b, outs=[grads[1]] + outs[1:])      # output over another input
+    rejects(g.ar_compressed_allreduce, grads, b, scale=float("inf"))
+    rejects(g.ar_compressed_allreduce, grads, b, residuals=res[:2] + [res[2] + 8])
+    with pytest.raises(g.ArError):
+        g.ar_compressed_allreduce([grads[0]] * 65, b, count=L, stream=0)          # too many ranks
+    # count 0 validates and enqueues nothing (no device call on this GPU-less host)
+    g.ar_compress(grads, codes, scales, b, count=0, stream=0)
+    g.ar_compressed_reduce(codes, scales, outs, b, count=0, stream=0)
+    g.ar_compressed_allreduce(grads, b, residuals=res, outs=grads, count=0, stream=0)

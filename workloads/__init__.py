@@ -196,6 +196,18 @@ def tensor_grad(spec: Spec, rank: int, tensor: int, count: int, lo: int = 0, hi:
     return window(spec.dist, spec.dtype, spec.seed, (rank, tensor), lo, hi, spec.std, threads)
 
 
+RESIDUAL_KEY = 1 << 24  # second key component of the residual streams (distinct from tensor ids)
+
+
+def residual_buffer(spec: Spec, rank: int, lo: int = 0, hi: int | None = None, threads=None) -> np.ndarray:
+    """An fp32 error-feedback residual for rank ``rank`` of a flat workload (or
+    elements [lo, hi) of it): normal with 1/100 of the gradients' std, the
+    size of a residual left by a block of a few std (half a scale is about
+    2 std / 127)."""
+    hi = spec.count if hi is None else hi
+    return window("normal", "f32", spec.seed, (rank, RESIDUAL_KEY), lo, hi, spec.std * 1e-2, threads)
+
+
 def small_spec(n_ranks: int, count: int, dtype: str = "f32", dist: str = "uniform", seed: int = 0,
                group_size: int = 0, std: float = 1e-3) -> Spec:
     """An ad-hoc workload for tests (ragged sizes, tiny N, edge cases)."""
