@@ -25,6 +25,8 @@ CXX_SOURCES = ["api.cpp"]
 HEADERS = ["internal.h", "common.cuh", "bulk.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+# Per-file nvcc flags (none at present).
+CUDA_FLAGS: dict = {}
 
 
 def cuda_home() -> str:
@@ -80,7 +82,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, 
     objs = []
     for src in CUDA_SOURCES:
         obj = os.path.join(bdir, src + ".o")
-        cmd = [nvcc, *ARCH, "-lineinfo", *common, "-Xcompiler", "-fPIC", "-c",
+        cmd = [nvcc, *ARCH, "-lineinfo", *common, *CUDA_FLAGS.get(src, []), "-Xcompiler", "-fPIC", "-c",
                os.path.join(CSRC, src), "-o", obj]
         if ptxas_info:
             cmd += ["-Xptxas", "-v"]

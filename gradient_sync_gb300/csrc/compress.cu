@@ -22,15 +22,28 @@
 //  compressed_allreduce_kernel  g, e -> e', out             (both in one pass; no message
 //                                                            is materialised)
 //
-// Thread geometry of the block-wise kernels: a group of `lanes` threads of one
-// warp covers one quantisation block; each thread holds V vectors of 4
-// consecutive elements, vector v of lane l at block_base + (v * lanes + l) * 4,
-// so the lanes of a group read contiguous 16-byte pieces. Blocks of up to 128
-// elements take block / 4 lanes and V = 1 (several blocks per warp); larger
-// blocks take the whole warp and V = block / 128. The block maximum is a
-// butterfly of shuffles inside the group. The group loop is warp-uniform, so
-// every lane reaches every shuffle; lanes past the last block compute on zeros
-// and store nothing.
+// Tiling: a CTA of 256 threads takes a tile of 256 * E consecutive elements,
+// the same tile of every rank, E per thread (thread t: elements E*t..E*t+E-1;
+// E = 8: one 16-byte bf16 vector or two fp32 vectors; E = 4: one 8-byte bf16
+// or one 16-byte fp32 vector), ranks in order, NB ranks' values loaded before
+// any of them is used. A quantisation block (a power of two from 16 to 1024
+// elements) lies inside one tile: blocks of up to 32 * E elements are covered
+// by block / E lanes of one warp and their maximum is a butterfly of shuffles
+// among those lanes; larger blocks span block / (32 * E) warps, which combine
+// their warp maxima through shared memory after one CTA barrier.
+// Loops are uniform across the CTA, so every thread reaches every shuffle and
+// barrier; elements past the end of the buffer read as 0 (they do not change a
+// maximum) and are never stored.
+//
+// The code of an element is decided without a division in the common case:
+// with a normal scale s, y = x * RN(1/s) lies within 2^-15 of the correctly
+// rounded quotient RN(x / s) (|x / s| <= 127 + 2^-16, two roundings of
+// relative size 2^-24 each). When every y of a thread is farther than 2^-12
+// from a half-integer, rint(y) equals rint(RN(x / s)); otherwise (rarely: a
+// quotient near a tie) the thread takes the correctly rounded quotient
+// __fdiv_rn(x, s) itself, so ties are decided exactly as the definition says.
+// Codes are kept as integer-valued floats, normalised so that a zero code is
+// +0 (as an integer code converted to float is).
 #include "common.cuh"
 
 namespace ar {
@@ -38,23 +51,41 @@ namespace ar {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
+constexpr int kWarps = kThreads / 32;
 
-// Four consecutive elements starting at e (a multiple of 4) as fp32; elements
-// at or past `lim` read as 0. A whole vector is one 16-byte (fp32) or 8-byte
-// (bf16) load: the base is 16-byte aligned and e a multiple of 4.
+// Elements per thread per rank: 4 for fp32 (one 16-byte vector), 8 for bf16
+// (one 16-byte vector). Measured on GB300 with 16 ranks of 192 MiB: fp32 at 8
+// per thread needs 72 registers, fits 3 CTAs per SM and stalls on memory
+// latency (0.89-0.93 of HBM); at 4 per thread it reaches 0.96-0.97. bf16 at 4
+// per thread moves only 8 bytes per load and reaches 0.70 against 0.80.
 template <bool BF16>
-__device__ __forceinline__ void load4(const void* base, int64_t e, int64_t lim, float (&f)[4]) {
-  if (e + 4 <= lim) {
-    if constexpr (BF16) {
+__host__ __device__ constexpr int ept() { return BF16 ? 8 : 4; }
+
+// kEPT consecutive elements starting at e (a multiple of kEPT) as fp32;
+// elements at or past `lim` read as 0. The base is 16-byte aligned, so a whole
+// group is whole 16-byte fp32 vectors, or one 8- or 16-byte bf16 vector.
+template <bool BF16, int kEPT>
+__device__ __forceinline__ void load_group(const void* base, int64_t e, int64_t lim, float (&f)[kEPT]) {
+  if (e + kEPT <= lim) {
+    if constexpr (BF16 && kEPT == 8) {
+      const uint4 w = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + e));
+      const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { f[2 * i] = bf16lo(v[i]); f[2 * i + 1] = bf16hi(v[i]); }
+    } else if constexpr (BF16) {
       const uint2 w = __ldcs(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + e));
       f[0] = bf16lo(w.x); f[1] = bf16hi(w.x); f[2] = bf16lo(w.y); f[3] = bf16hi(w.y);
     } else {
-      const float4 v = __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(base) + e));
-      f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+      const float4* q = reinterpret_cast<const float4*>(static_cast<const float*>(base) + e);
+#pragma unroll
+      for (int i = 0; i < kEPT / 4; ++i) {
+        const float4 a = __ldcs(q + i);
+        f[4 * i] = a.x; f[4 * i + 1] = a.y; f[4 * i + 2] = a.z; f[4 * i + 3] = a.w;
+      }
     }
   } else {
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < kEPT; ++w) {
       f[w] = 0.0f;
       if (e + w < lim)
         f[w] = BF16 ? bf16_to_f32(static_cast<const uint16_t*>(base)[e + w]) : static_cast<const float*>(base)[e + w];
@@ -62,20 +93,26 @@ __device__ __forceinline__ void load4(const void* base, int64_t e, int64_t lim, 
   }
 }
 
-// Store four consecutive elements at e (bf16: rounded to nearest even);
+// Store kEPT consecutive elements at e (bf16: rounded to nearest even);
 // elements at or past `count` are not written.
-template <bool BF16>
-__device__ __forceinline__ void store4(void* base, int64_t e, int64_t count, const float (&f)[4]) {
-  if (e + 4 <= count) {
-    if constexpr (BF16) {
+template <bool BF16, int kEPT>
+__device__ __forceinline__ void store_group(void* base, int64_t e, int64_t count, const float (&f)[kEPT]) {
+  if (e + kEPT <= count) {
+    if constexpr (BF16 && kEPT == 8) {
+      __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(base) + e),
+             make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                        pack_bf16x2(f[6], f[7])));
+    } else if constexpr (BF16) {
       __stcs(reinterpret_cast<uint2*>(static_cast<uint16_t*>(base) + e),
              make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3])));
     } else {
-      __stcs(reinterpret_cast<float4*>(static_cast<float*>(base) + e), make_float4(f[0], f[1], f[2], f[3]));
+      float4* q = reinterpret_cast<float4*>(static_cast<float*>(base) + e);
+#pragma unroll
+      for (int i = 0; i < kEPT / 4; ++i) __stcs(q + i, make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]));
     }
   } else {
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < kEPT; ++w) {
       if (e + w >= count) continue;
       if (BF16)
         static_cast<uint16_t*>(base)[e + w] = f32_to_bf16(f[w]);
@@ -85,276 +122,280 @@ __device__ __forceinline__ void store4(void* base, int64_t e, int64_t count, con
   }
 }
 
-// The block's scale: the largest |x| over the group's lanes, divided by 127.
-// Every lane of the warp must call this (it shuffles across the warp).
-template <int V>
-__device__ __forceinline__ float group_scale(const float (&x)[V][4], int lanes) {
+// The block's scale s = max|x| / 127 for this thread's kEPT values.
+// `wmax` is this call's shared-memory slot; callers alternate two slots, so
+// one barrier per call suffices (a warp that writes the next call's slot has
+// passed this call's barrier, after every warp finished reading the slot of
+// the call before).
+template <int kEPT>
+__device__ __forceinline__ float block_scale(const float (&x)[kEPT], int block, float* wmax) {
   float m = 0.0f;
 #pragma unroll
-  for (int v = 0; v < V; ++v)
-#pragma unroll
-    for (int w = 0; w < 4; ++w) m = fmaxf(m, fabsf(x[v][w]));
+  for (int w = 0; w < kEPT; ++w) m = fmaxf(m, fabsf(x[w]));
+  constexpr int kWarpElems = 32 * kEPT;
+  const int lanes = block < kWarpElems ? block / kEPT : 32;
   for (int o = lanes >> 1; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  if (block > kWarpElems) {
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) wmax[warp] = m;
+    __syncthreads();
+    const int W = block / kWarpElems;
+    const int w0 = warp & ~(W - 1);
+    m = wmax[w0];
+    for (int i = 1; i < W; ++i) m = fmaxf(m, wmax[w0 + i]);
+  }
   return __fdiv_rn(m, 127.0f);
 }
 
-// The code of x in a block of scale s: the nearest integer to the fp32
-// quotient x / s (ties to even), clamped to [-127, 127]; 0 when s is 0.
-__device__ __forceinline__ int quant_code(float x, float s) {
-  if (!(s > 0.0f)) return 0;
-  const float t = fminf(fmaxf(rintf(__fdiv_rn(x, s)), -127.0f), 127.0f);
-  return int(t);
+// Element-wise fp32 arithmetic, one IEEE operation per element rounded to
+// nearest even and never contracted into an FMA (the definition rounds every
+// product before it is summed).
+template <int n>
+__device__ __forceinline__ void mul_each(float (&d)[n], const float (&a)[n], float b) {
+#pragma unroll
+  for (int w = 0; w < n; ++w) d[w] = __fmul_rn(a[w], b);
+}
+template <int n>
+__device__ __forceinline__ void add_each(float (&d)[n], const float (&a)[n], const float (&b)[n]) {
+#pragma unroll
+  for (int w = 0; w < n; ++w) d[w] = __fadd_rn(a[w], b[w]);
+}
+template <int n>
+__device__ __forceinline__ void sub_each(float (&d)[n], const float (&a)[n], const float (&b)[n]) {
+#pragma unroll
+  for (int w = 0; w < n; ++w) d[w] = __fsub_rn(a[w], b[w]);
 }
 
-__device__ __forceinline__ uint32_t pack_codes(const int (&c)[4]) {
-  return (uint32_t(c[0]) & 0xFFu) | ((uint32_t(c[1]) & 0xFFu) << 8) | ((uint32_t(c[2]) & 0xFFu) << 16) |
-         ((uint32_t(c[3]) & 0xFFu) << 24);
+// The codes of this thread's values in a block of scale s, as integer-valued
+// floats: the nearest integer to RN(x / s) (ties to even), clamped to
+// [-127, 127]; all 0 when s is 0. See the file comment for the screening.
+template <int kEPT>
+__device__ __forceinline__ void quant_group(const float (&x)[kEPT], float s, float (&c)[kEPT]) {
+  if (s >= 0x1p-126f) {
+    float y[kEPT], dev[kEPT];
+    mul_each(y, x, __frcp_rn(s));
+#pragma unroll
+    for (int w = 0; w < kEPT; ++w) c[w] = rintf(y[w]);
+    sub_each(dev, y, c);  // exact: y and its nearest integer are within a factor of 2 (or c = 0)
+    float worst = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kEPT; ++w) worst = fmaxf(worst, fabsf(dev[w]));
+    if (worst >= 0.5f - 0x1p-12f) {  // a quotient near a tie: the exact quotient decides
+#pragma unroll
+      for (int w = 0; w < kEPT; ++w) c[w] = rintf(__fdiv_rn(x[w], s));
+    }
+    // |x / s| < 127.5 for a normal s, so no clamp is needed here
+  } else if (s > 0.0f) {  // a subnormal scale: exact quotients, clamped
+#pragma unroll
+    for (int w = 0; w < kEPT; ++w) c[w] = fminf(fmaxf(rintf(__fdiv_rn(x[w], s)), -127.0f), 127.0f);
+  } else {
+#pragma unroll
+    for (int w = 0; w < kEPT; ++w) c[w] = 0.0f;
+  }
+#pragma unroll
+  for (int w = 0; w < kEPT; ++w) c[w] = __fadd_rn(c[w], 0.0f);  // -0 -> +0
+}
+
+// Four integer-valued codes in [-127, 127] (c[i..i+3]) as four
+// two's-complement bytes of one word.
+template <int kEPT>
+__device__ __forceinline__ uint32_t pack_codes4(const float (&c)[kEPT], int i) {
+  return (uint32_t(int(c[i])) & 0xFFu) | ((uint32_t(int(c[i + 1])) & 0xFFu) << 8) |
+         ((uint32_t(int(c[i + 2])) & 0xFFu) << 16) | ((uint32_t(int(c[i + 3])) & 0xFFu) << 24);
 }
 
 __device__ __forceinline__ float code_of(uint32_t word, int j) {
   return float(static_cast<int8_t>(static_cast<uint8_t>(word >> (8 * j))));
 }
 
-struct GroupGeom {
-  int lanes, sub, gpw;  // lanes per group, this lane's index in it, groups per warp
-  int64_t warp, n_warps;
-};
-
-template <int V>
-__device__ __forceinline__ GroupGeom group_geom(int block) {
-  GroupGeom g;
-  g.lanes = V > 1 ? 32 : block / 4;
-  const int lane = threadIdx.x & 31;
-  g.sub = lane & (g.lanes - 1);
-  g.gpw = 32 / g.lanes;
-  g.warp = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-  g.n_warps = (int64_t(gridDim.x) * kThreads) >> 5;
-  return g;
-}
-
 // ---------------------------------------------------------------- compress
-// One group per (rank, block): codes, the block's scale and (with error
-// feedback) the new residual of that rank's block.
-template <bool BF16, int V, bool EF>
+// Each tile of every rank: codes (kEPT bytes per thread), the scale of each block
+// (written by the block's first thread) and, with error feedback, the new
+// residual.
+template <bool BF16, bool EF>
 __global__ void __launch_bounds__(kThreads) compress_kernel(const __grid_constant__ CompressParams p) {
+  constexpr int kEPT = ept<BF16>();
+  constexpr int kTileElems = kEPT * kThreads;
+  constexpr int NB = (EF && BF16) ? 2 : 4;
+  __shared__ float wmax[2][kWarps];
   grid_dependency_wait();
   grid_dependents_launch();
-  const GroupGeom gg = group_geom<V>(p.block);
-  const int64_t total = p.n_blocks * p.n;
-  for (int64_t g0 = gg.warp * gg.gpw; g0 < total; g0 += gg.n_warps * gg.gpw) {
-    const int64_t gid = g0 + (threadIdx.x & 31) / gg.lanes;
-    const bool live = gid < total;
-    const int r = live ? int(gid / p.n_blocks) : 0;
-    const int64_t k = live ? gid - int64_t(r) * p.n_blocks : 0;
-    const int64_t base = k * p.block;
-    const int64_t lim = live ? p.count : 0;  // lanes past the last block read nothing
-    float x[V][4];
+  const int64_t n_tiles = (p.count + kTileElems - 1) / kTileElems;
+  const int shift = __ffs(p.block) - 1;  // block is a power of two
+  int phase = 0;
+  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const int64_t e = tile * kTileElems + int64_t(kEPT) * threadIdx.x;
+#pragma unroll 1
+    for (int r0 = 0; r0 < p.n; r0 += NB) {
+      float xg[NB][kEPT], xe[NB][kEPT];
 #pragma unroll
-    for (int v = 0; v < V; ++v) {
-      const int64_t e = base + (int64_t(v) * gg.lanes + gg.sub) * 4;
-      load4<BF16>(p.g[r], e, lim, x[v]);
-      if (EF) {
-        float ev[4];
-        load4<false>(p.e[r], e, lim, ev);
-#pragma unroll
-        for (int w = 0; w < 4; ++w) x[v][w] = fadd(x[v][w], ev[w]);
+      for (int b = 0; b < NB; ++b) {
+        if (r0 + b >= p.n) continue;
+        load_group<BF16, kEPT>(p.g[r0 + b], e, p.count, xg[b]);
+        if (EF) load_group<false, kEPT>(p.e[r0 + b], e, p.count, xe[b]);
       }
-    }
-    const float s = group_scale<V>(x, gg.lanes);
-    if (!live) continue;
-    if (gg.sub == 0) p.s[r][k] = s;
 #pragma unroll
-    for (int v = 0; v < V; ++v) {
-      const int64_t e = base + (int64_t(v) * gg.lanes + gg.sub) * 4;
-      if (e >= p.count) continue;
-      int c[4];
+      for (int b = 0; b < NB; ++b) {
+        const int r = r0 + b;
+        if (r >= p.n) continue;  // uniform across the CTA
+        float x[kEPT], c[kEPT];
+        if (EF)
+          add_each(x, xg[b], xe[b]);
+        else
 #pragma unroll
-      for (int w = 0; w < 4; ++w) c[w] = quant_code(x[v][w], s);
-      int8_t* q = p.q[r];
-      if (e + 4 <= p.count) {
-        __stcs(reinterpret_cast<unsigned int*>(q + e), pack_codes(c));
-      } else {
+          for (int w = 0; w < kEPT; ++w) x[w] = xg[b][w];
+        const float s = block_scale<kEPT>(x, p.block, wmax[phase]);
+        phase ^= 1;
+        if (e >= p.count) continue;
+        if ((e & (p.block - 1)) == 0) p.s[r][e >> shift] = s;
+        quant_group<kEPT>(x, s, c);
+        int8_t* q = p.q[r];
+        if (e + kEPT <= p.count) {
+          if constexpr (kEPT == 8)
+            __stcs(reinterpret_cast<uint2*>(q + e), make_uint2(pack_codes4<kEPT>(c, 0), pack_codes4<kEPT>(c, 4)));
+          else
+            __stcs(reinterpret_cast<unsigned int*>(q + e), pack_codes4<kEPT>(c, 0));
+        } else {
 #pragma unroll
-        for (int w = 0; w < 4; ++w)
-          if (e + w < p.count) q[e + w] = static_cast<int8_t>(c[w]);
-      }
-      if (EF) {
-        float res[4];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) res[w] = __fsub_rn(x[v][w], fmul(float(c[w]), s));
-        store4<false>(p.e[r], e, p.count, res);
+          for (int w = 0; w < kEPT; ++w)
+            if (e + w < p.count) q[e + w] = static_cast<int8_t>(int(c[w]));
+        }
+        if (EF) {
+          float d[kEPT], res[kEPT];
+          mul_each(d, c, s);
+          sub_each(res, x, d);
+          store_group<false, kEPT>(p.e[r], e, p.count, res);
+        }
       }
     }
   }
 }
 
 // ---------------------------------------------------------------- reduce
-// The receiving side: each thread takes 16 consecutive elements (one 16-byte
-// vector of codes per rank; a block is a multiple of 16 elements, so the 16
-// share one scale), reconstructs every rank's values, sums them in rank order,
-// scales once and writes the result to every rank. Loads are issued NB ranks
-// at a time before any arithmetic.
+// The receiving side: for each tile, every rank's codes (kEPT bytes per thread)
+// and the scale of the thread's block are loaded NB ranks at a time, the
+// reconstructions summed in rank order, scaled once, and the result written to
+// every rank.
 template <bool BF16OUT>
 __global__ void __launch_bounds__(kThreads) compressed_reduce_kernel(const __grid_constant__ CompressParams p) {
+  constexpr int NB = 8;
+  constexpr int kEPT = ept<BF16OUT>();
+  constexpr int kTileElems = kEPT * kThreads;
   grid_dependency_wait();
   grid_dependents_launch();
-  constexpr int NB = 8;
-  const int64_t n16 = (p.count + 15) >> 4;
-  const int64_t stride = int64_t(gridDim.x) * kThreads;
-  for (int64_t t = int64_t(blockIdx.x) * kThreads + threadIdx.x; t < n16; t += stride) {
-    const int64_t e = t << 4;
-    const int64_t kb = e / p.block;
-    if (e + 16 <= p.count) {
-      float acc[16];
+  const int64_t n_tiles = (p.count + kTileElems - 1) / kTileElems;
+  const int shift = __ffs(p.block) - 1;
+  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const int64_t e = tile * kTileElems + int64_t(kEPT) * threadIdx.x;
+    if (e >= p.count) continue;
+    const int64_t kb = e >> shift;
+    const bool whole = e + kEPT <= p.count;
+    float acc[kEPT];
 #pragma unroll 1
-      for (int r0 = 0; r0 < p.n; r0 += NB) {
-        uint4 c[NB];
-        float s[NB];
+    for (int r0 = 0; r0 < p.n; r0 += NB) {
+      uint2 c[NB];
+      float s[NB];
 #pragma unroll
-        for (int b = 0; b < NB; ++b)
-          if (r0 + b < p.n) {
-            c[b] = __ldcs(reinterpret_cast<const uint4*>(p.q[r0 + b] + e));
-            s[b] = __ldg(p.s[r0 + b] + kb);
-          }
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          if (r0 + b >= p.n) continue;
-          const uint32_t wd[4] = {c[b].x, c[b].y, c[b].z, c[b].w};
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float d = fmul(code_of(wd[i >> 2], i & 3), s[b]);
-            acc[i] = (r0 + b == 0) ? d : fadd(acc[i], d);
-          }
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 16; ++i) acc[i] = fmul(acc[i], p.scale);
-#pragma unroll 1
-      for (int r = 0; r < p.n; ++r) {
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const float f[4] = {acc[4 * h], acc[4 * h + 1], acc[4 * h + 2], acc[4 * h + 3]};
-          store4<BF16OUT>(p.out[r], e + 4 * h, p.count, f);
-        }
-      }
-    } else {  // the ragged end of the buffer, one element at a time
-      for (int64_t x = e; x < p.count; ++x) {
-        float a = 0.0f;
-        for (int r = 0; r < p.n; ++r) {
-          const float d = fmul(float(p.q[r][x]), p.s[r][kb]);
-          a = r == 0 ? d : fadd(a, d);
-        }
-        a = fmul(a, p.scale);
-        for (int r = 0; r < p.n; ++r) {
-          if (BF16OUT)
-            static_cast<uint16_t*>(p.out[r])[x] = f32_to_bf16(a);
+      for (int b = 0; b < NB; ++b) {
+        if (r0 + b >= p.n) continue;
+        const int8_t* q = p.q[r0 + b];
+        if (whole) {
+          if constexpr (kEPT == 8)
+            c[b] = __ldcs(reinterpret_cast<const uint2*>(q + e));
           else
-            static_cast<float*>(p.out[r])[x] = a;
+            c[b] = make_uint2(__ldcs(reinterpret_cast<const unsigned int*>(q + e)), 0u);
+        } else {  // the ragged end: bytes past count read as code 0 and are never stored
+          uint32_t lo = 0, hi = 0;
+          for (int w = 0; w < kEPT; ++w)
+            if (e + w < p.count) {
+              const uint32_t v = uint32_t(static_cast<uint8_t>(q[e + w]));
+              if (w < 4) lo |= v << (8 * w); else hi |= v << (8 * (w - 4));
+            }
+          c[b] = make_uint2(lo, hi);
+        }
+        s[b] = __ldg(p.s[r0 + b] + kb);
+      }
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        if (r0 + b >= p.n) continue;
+        float q[kEPT], d[kEPT];
+#pragma unroll
+        for (int w = 0; w < kEPT; ++w) q[w] = code_of(w < 4 ? c[b].x : c[b].y, w & 3);
+        mul_each(d, q, s[b]);
+        if (r0 + b == 0) {
+#pragma unroll
+          for (int w = 0; w < kEPT; ++w) acc[w] = d[w];
+        } else {
+          add_each(acc, acc, d);
         }
       }
     }
+    mul_each(acc, acc, p.scale);
+#pragma unroll 1
+    for (int r = 0; r < p.n; ++r) store_group<BF16OUT, kEPT>(p.out[r], e, p.count, acc);
   }
 }
 
 // ---------------------------------------------------------------- fused
-// One group per block index k, over all ranks in rank order: quantise rank
-// r's block, add its reconstruction to the running sum, store its residual;
-// then write the scaled sum to every rank. No message leaves the registers.
-// For small V the next rank's block is loaded before this rank's shuffles.
-template <bool BF16, int V, bool EF>
+// Each tile, ranks in order: quantise rank r's block, add its reconstruction
+// to the running sum and store its residual; then write the scaled sum to
+// every rank. No message leaves the registers.
+template <bool BF16, bool EF>
 __global__ void __launch_bounds__(kThreads) compressed_allreduce_kernel(const __grid_constant__ CompressParams p) {
+  constexpr int kEPT = ept<BF16>();
+  constexpr int kTileElems = kEPT * kThreads;
+  constexpr int NB = EF ? 2 : 4;
+  __shared__ float wmax[2][kWarps];
   grid_dependency_wait();
   grid_dependents_launch();
-  constexpr bool kPrefetch = V <= 2;
-  const GroupGeom gg = group_geom<V>(p.block);
-  const int64_t total = p.n_blocks;
-  for (int64_t g0 = gg.warp * gg.gpw; g0 < total; g0 += gg.n_warps * gg.gpw) {
-    const int64_t k = g0 + (threadIdx.x & 31) / gg.lanes;
-    const bool live = k < total;
-    const int64_t base = live ? k * p.block : 0;
-    const int64_t lim = live ? p.count : 0;
-    int64_t ev_at[V];
-#pragma unroll
-    for (int v = 0; v < V; ++v) ev_at[v] = base + (int64_t(v) * gg.lanes + gg.sub) * 4;
-    float acc[V][4];
-    float ng[V][4], ne[V][4];  // the next rank's gradient and residual (prefetch)
-    if (kPrefetch) {
-#pragma unroll
-      for (int v = 0; v < V; ++v) {
-        load4<BF16>(p.g[0], ev_at[v], lim, ng[v]);
-        if (EF) load4<false>(p.e[0], ev_at[v], lim, ne[v]);
-      }
-    }
+  const int64_t n_tiles = (p.count + kTileElems - 1) / kTileElems;
+  int phase = 0;
+  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const int64_t e = tile * kTileElems + int64_t(kEPT) * threadIdx.x;
+    float acc[kEPT];
 #pragma unroll 1
-    for (int r = 0; r < p.n; ++r) {
-      float x[V][4];
+    for (int r0 = 0; r0 < p.n; r0 += NB) {
+      float xg[NB][kEPT], xe[NB][kEPT];
 #pragma unroll
-      for (int v = 0; v < V; ++v) {
-        float gv[4], evv[4];
-        if (kPrefetch) {
+      for (int b = 0; b < NB; ++b) {
+        if (r0 + b >= p.n) continue;
+        load_group<BF16, kEPT>(p.g[r0 + b], e, p.count, xg[b]);
+        if (EF) load_group<false, kEPT>(p.e[r0 + b], e, p.count, xe[b]);
+      }
 #pragma unroll
-          for (int w = 0; w < 4; ++w) { gv[w] = ng[v][w]; evv[w] = EF ? ne[v][w] : 0.0f; }
+      for (int b = 0; b < NB; ++b) {
+        const int r = r0 + b;
+        if (r >= p.n) continue;  // uniform across the CTA
+        float x[kEPT], c[kEPT];
+        if (EF)
+          add_each(x, xg[b], xe[b]);
+        else
+#pragma unroll
+          for (int w = 0; w < kEPT; ++w) x[w] = xg[b][w];
+        const float s = block_scale<kEPT>(x, p.block, wmax[phase]);
+        phase ^= 1;
+        quant_group<kEPT>(x, s, c);
+        float d[kEPT];
+        mul_each(d, c, s);
+        if (r == 0) {
+#pragma unroll
+          for (int w = 0; w < kEPT; ++w) acc[w] = d[w];
         } else {
-          load4<BF16>(p.g[r], ev_at[v], lim, gv);
-          if (EF) load4<false>(p.e[r], ev_at[v], lim, evv);
+          add_each(acc, acc, d);
         }
-#pragma unroll
-        for (int w = 0; w < 4; ++w) x[v][w] = EF ? fadd(gv[w], evv[w]) : gv[w];
-      }
-      if (kPrefetch && r + 1 < p.n) {
-#pragma unroll
-        for (int v = 0; v < V; ++v) {
-          load4<BF16>(p.g[r + 1], ev_at[v], lim, ng[v]);
-          if (EF) load4<false>(p.e[r + 1], ev_at[v], lim, ne[v]);
-        }
-      }
-      const float s = group_scale<V>(x, gg.lanes);
-#pragma unroll
-      for (int v = 0; v < V; ++v) {
-        float res[4];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const float d = fmul(float(quant_code(x[v][w], s)), s);
-          acc[v][w] = r == 0 ? d : fadd(acc[v][w], d);
-          res[w] = __fsub_rn(x[v][w], d);
-        }
-        if (EF && live && ev_at[v] < p.count) store4<false>(p.e[r], ev_at[v], p.count, res);
+        float res[kEPT];
+        if (EF) sub_each(res, x, d);
+        if (EF && e < p.count) store_group<false, kEPT>(p.e[r], e, p.count, res);
       }
     }
-    if (!live) continue;
-#pragma unroll
-    for (int v = 0; v < V; ++v)
-#pragma unroll
-      for (int w = 0; w < 4; ++w) acc[v][w] = fmul(acc[v][w], p.scale);
+    if (e >= p.count) continue;
+    mul_each(acc, acc, p.scale);
 #pragma unroll 1
-    for (int r = 0; r < p.n; ++r)
-#pragma unroll
-      for (int v = 0; v < V; ++v)
-        if (ev_at[v] < p.count) store4<BF16>(p.out[r], ev_at[v], p.count, acc[v]);
+    for (int r = 0; r < p.n; ++r) store_group<BF16, kEPT>(p.out[r], e, p.count, acc);
   }
 }
 
 using Kern = void (*)(CompressParams);
-
-template <bool BF16, bool EF>
-Kern pick_compress(int V) {
-  switch (V) {
-    case 1: return compress_kernel<BF16, 1, EF>;
-    case 2: return compress_kernel<BF16, 2, EF>;
-    case 4: return compress_kernel<BF16, 4, EF>;
-    default: return compress_kernel<BF16, 8, EF>;
-  }
-}
-
-template <bool BF16, bool EF>
-Kern pick_fused(int V) {
-  switch (V) {
-    case 1: return compressed_allreduce_kernel<BF16, 1, EF>;
-    case 2: return compressed_allreduce_kernel<BF16, 2, EF>;
-    case 4: return compressed_allreduce_kernel<BF16, 4, EF>;
-    default: return compressed_allreduce_kernel<BF16, 8, EF>;
-  }
-}
 
 cudaError_t launch(Kern k, int64_t tiles, const CompressParams& p, cudaStream_t stream) {
   if (tiles <= 0) return cudaSuccess;
@@ -370,38 +411,30 @@ cudaError_t launch(Kern k, int64_t tiles, const CompressParams& p, cudaStream_t 
   return cudaLaunchKernelEx(&cfg, k, p);
 }
 
-// Groups of one CTA: 8 warps, each 32 / lanes groups.
-int64_t groups_per_cta(int block) {
-  const int lanes = block > 128 ? 32 : block / 4;
-  return int64_t(kThreads / 32) * (32 / lanes);
+int64_t n_tiles(int64_t count, bool bf16) {
+  const int64_t tile = int64_t(bf16 ? ept<true>() : ept<false>()) * kThreads;
+  return (count + tile - 1) / tile;
 }
-
-int vectors_per_lane(int block) { return block > 128 ? block / 128 : 1; }
 
 }  // namespace
 
 cudaError_t launch_compress(const CompressParams& p, ar_dtype dtype, cudaStream_t stream) {
-  const int V = vectors_per_lane(p.block);
   const bool bf = dtype == AR_BF16;
-  const Kern k = bf ? (p.ef ? pick_compress<true, true>(V) : pick_compress<true, false>(V))
-                    : (p.ef ? pick_compress<false, true>(V) : pick_compress<false, false>(V));
-  const int64_t per = groups_per_cta(p.block);
-  return launch(k, (p.n_blocks * p.n + per - 1) / per, p, stream);
+  const Kern k = bf ? (p.ef ? compress_kernel<true, true> : compress_kernel<true, false>)
+                    : (p.ef ? compress_kernel<false, true> : compress_kernel<false, false>);
+  return launch(k, n_tiles(p.count, bf), p, stream);
 }
 
 cudaError_t launch_compressed_reduce(const CompressParams& p, ar_dtype out_dtype, cudaStream_t stream) {
   const Kern k = out_dtype == AR_BF16 ? compressed_reduce_kernel<true> : compressed_reduce_kernel<false>;
-  const int64_t n16 = (p.count + 15) / 16;
-  return launch(k, (n16 + kThreads - 1) / kThreads, p, stream);
+  return launch(k, n_tiles(p.count, out_dtype == AR_BF16), p, stream);
 }
 
 cudaError_t launch_compressed_allreduce(const CompressParams& p, ar_dtype dtype, cudaStream_t stream) {
-  const int V = vectors_per_lane(p.block);
   const bool bf = dtype == AR_BF16;
-  const Kern k = bf ? (p.ef ? pick_fused<true, true>(V) : pick_fused<true, false>(V))
-                    : (p.ef ? pick_fused<false, true>(V) : pick_fused<false, false>(V));
-  const int64_t per = groups_per_cta(p.block);
-  return launch(k, (p.n_blocks + per - 1) / per, p, stream);
+  const Kern k = bf ? (p.ef ? compressed_allreduce_kernel<true, true> : compressed_allreduce_kernel<true, false>)
+                    : (p.ef ? compressed_allreduce_kernel<false, true> : compressed_allreduce_kernel<false, false>);
+  return launch(k, n_tiles(p.count, bf), p, stream);
 }
 
 }  // namespace ar

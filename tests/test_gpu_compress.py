@@ -136,6 +136,31 @@ def test_compress_exact_grid_and_ties(g):
     assert np.all(got[0][0][half].astype(int) % 2 == 0)
 
 
+@pytest.mark.parametrize("block", [16, 128, 1024])
+def test_compress_near_ties_with_arbitrary_scales(g, block):
+    """Values a few ulps either side of (k + 1/2) * s for scales that are not
+    powers of two: the quotients x / s fall next to half-integers, where only
+    the correctly rounded quotient decides the code."""
+    rng = np.random.default_rng(block + 1)
+    nb = 64
+    m = (rng.uniform(0.5, 2.0, nb) * np.exp2(rng.integers(-30, 10, nb))).astype(F32)
+    s = (m / F32(127)).astype(F32)
+    k = rng.integers(-126, 126, (nb, block)) + 0.5
+    x = (k * s[:, None].astype(np.float64)).astype(F32)  # the fp32 nearest to (k + 1/2) * s
+    step = rng.integers(-2, 3, x.shape)  # then 0, 1 or 2 ulps up or down
+    for _ in range(2):
+        x = np.where(step > 0, np.nextafter(x, F32(np.inf)), np.where(step < 0, np.nextafter(x, F32(-np.inf)), x))
+        step = step - np.sign(step)
+    x = x.astype(F32)
+    x[:, 0] = m * rng.choice([-1, 1], nb)
+    x = x.reshape(1, -1)
+    got = _compress_on_gpu(g, x, None, "f32", block)
+    _check_messages(got, _oracle_messages(x, None, block), False)
+    e = (rng.standard_normal(x.shape) * 1e-9).astype(F32)
+    got = _compress_on_gpu(g, x, e, "f32", block)
+    _check_messages(got, _oracle_messages(x, e, block), True)
+
+
 @pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("block", [16, 128, 1024])
 @pytest.mark.parametrize("N", [1, 2, 5, 8, 16, 64])
