@@ -299,11 +299,17 @@ cudaError_t launch_persistent(void (*kernel)(P), const P& p, int64_t tiles, int 
 
 }  // namespace
 
-// Vectors per thread for N ranks: about eight 16-byte loads in flight per
-// thread whatever N is (N loads per vector).
-// (An all-gather folds one rank per element, so it takes the most vectors.)
+// Vectors per thread: about eight 16-byte loads in flight per thread for the
+// all-reduce whatever N is (N loads per vector). The reduce-scatter writes one
+// vector per N loaded and needs twice that: 8 ranks x 2 vectors measured 1.02
+// of HBM at 16 x 192 MiB fp32 on GB300, against 0.87 with one vector. The
+// all-gather folds one rank per element and is bound by its N stores per load
+// (0.85 with 4 vectors; 8 measured the same).
+constexpr int kRsNB = 8, kRsVPT = 2, kAgVPT = 4;
+
 int fused_vpt(int n, int order, int collective) {
-  if (collective == AR_ALLGATHER) return 4;
+  if (collective == AR_ALLGATHER) return kAgVPT;
+  if (collective == AR_REDUCE_SCATTER && order != AR_ORDER_TREE && n > 4) return kRsVPT;
   if (order == AR_ORDER_TREE) return 1;
   return n <= 2 ? 4 : n <= 4 ? 2 : 1;
 }
@@ -316,6 +322,10 @@ template <bool BF16>
 cudaError_t launch_fused_t(const FusedParams& p, int64_t tiles, int sm_budget, cudaStream_t stream) {
   if (p.order == AR_ORDER_TREE && p.collective != AR_ALLGATHER)
     return launch_persistent(fused_flat_kernel<BF16, true, 8, 1>, p, tiles, sm_budget, stream);
+  if (p.collective == AR_REDUCE_SCATTER && p.n > 4)
+    return launch_persistent(fused_flat_kernel<BF16, false, kRsNB, kRsVPT>, p, tiles, sm_budget, stream);
+  if (p.collective == AR_ALLGATHER)
+    return launch_persistent(fused_flat_kernel<BF16, false, 1, kAgVPT>, p, tiles, sm_budget, stream);
   switch (fused_vpt(p.n, p.order, p.collective)) {
     case 4: return launch_persistent(fused_flat_kernel<BF16, false, 2, 4>, p, tiles, sm_budget, stream);
     case 2: return launch_persistent(fused_flat_kernel<BF16, false, 4, 2>, p, tiles, sm_budget, stream);
