@@ -180,6 +180,39 @@ def ar_execute_noalloc(plan: Plan, bufs, outs=None, stream=None):
     _check(_lib.load().ar_execute_noalloc(plan.handle, _ptrs(bufs), o, _stream(stream)), "ar_execute_noalloc")
 
 
+class Bound:
+    """An ar_bound_t*: a plan bound to its buffers (a persistent collective).
+    Keeps the buffers alive; destroyed with the object."""
+
+    def __init__(self, handle: int, keep):
+        self.handle = handle
+        self._keep = keep
+
+    def __del__(self):
+        h, self.handle = getattr(self, "handle", None), None
+        if h:
+            try:
+                _lib.load().ar_bound_destroy(h)
+            except Exception:
+                pass
+
+    def execute(self, stream=None):
+        ar_execute_bound(self, stream)
+
+
+def ar_bind(plan: Plan, bufs, outs=None, workspace=None) -> Bound:
+    """Validate the buffers once and record the plan's launches (see include/ar.h)."""
+    o = _ptrs(outs) if outs is not None else None
+    h = _lib.c_void_p()
+    _check(_lib.load().ar_bind(plan.handle, _ptrs(bufs), o, _ptr(workspace), h), "ar_bind")
+    return Bound(h.value, (list(bufs), None if outs is None else list(outs), workspace))
+
+
+def ar_execute_bound(bound: Bound, stream=None):
+    """Replay a bound all-reduce on ``stream`` (an int handle skips the torch lookup)."""
+    _check(_lib.load().ar_execute_bound(bound.handle, _stream(stream)), "ar_execute_bound")
+
+
 # ---------------------------------------------------------------- buckets
 
 

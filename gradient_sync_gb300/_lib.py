@@ -37,6 +37,9 @@ SIGNATURES = {
     "ar_execute": (c_int, [c_void_p, VOIDPP, VOIDPP, c_void_p, c_void_p]),
     "ar_execute_host": (c_int, [c_void_p, VOIDPP, VOIDPP, VOIDPP, c_void_p, c_void_p]),
     "ar_execute_noalloc": (c_int, [c_void_p, VOIDPP, VOIDPP, c_void_p]),
+    "ar_bind": (c_int, [c_void_p, VOIDPP, VOIDPP, c_void_p, ctypes.POINTER(c_void_p)]),
+    "ar_execute_bound": (c_int, [c_void_p, c_void_p]),
+    "ar_bound_destroy": (None, [c_void_p]),
     "ar_plan_destroy": (None, [c_void_p]),
     "ar_plan_predict": (c_int, [c_void_p, ctypes.POINTER(ArFabric), ctypes.POINTER(ctypes.c_double)]),
     "ar_select": (c_int, [ctypes.POINTER(ArDesc), ctypes.POINTER(ArFabric), INTP, INTP,

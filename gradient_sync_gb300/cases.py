@@ -39,7 +39,8 @@ def hbm_peak():
 
 
 def time_case(n, count, dtype="f32", algo="fused", order="ring", group_size=0, iters=20, warmup=5,
-              reps=None, graph=False, collective="allreduce", sm_budget=0, kernel="auto", torus_dims=(0, 0, 0)):
+              reps=None, graph=False, collective="allreduce", sm_budget=0, kernel="auto", torus_dims=(0, 0, 0),
+              bound=False):
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
     esz = 4 if dtype == "f32" else 2
     bufs = [torch.rand(count, device="cuda").to(tdt) for _ in range(n)]
@@ -56,6 +57,15 @@ def time_case(n, count, dtype="f32", algo="fused", order="ring", group_size=0, i
         g.ar_execute(plan, bufs, outs=outs, workspace=ws)
     torch.cuda.synchronize()
     run = None
+    if bound:  # a persistent collective: bound once, replayed from Python with one call each
+        bnd = g.ar_bind(plan, bufs, outs=outs, workspace=ws)
+        handle = int(stream.cuda_stream)
+
+        def run():
+            for _ in range(reps):
+                g.ar_execute_bound(bnd, stream=handle)
+        run()
+        torch.cuda.synchronize()
     if graph:  # the reps calls captured once into a CUDA graph: device time without host launch cost
         side = torch.cuda.Stream()
         side.wait_stream(stream)
@@ -90,7 +100,7 @@ def time_case(n, count, dtype="f32", algo="fused", order="ring", group_size=0, i
     factor = 2 * (n - 1) / n if collective == "allreduce" else (n - 1) / n  # busbw (primer §4.8)
     res = {"n": n, "collective": collective, "sm_budget": sm_budget, "kernel": kernel, "bytes_per_rank": S, "dtype": dtype, "algo": algo,
            "order": order if algo == "fused" else None,
-           "timing": "cuda graph" if graph else "launched from python",
+           "timing": "cuda graph" if graph else ("bound, replayed from python" if bound else "launched from python"),
            "group_size": group_size or None, "torus_dims": list(torus_dims) if algo == "torus" else None,
            "us": round(ms * 1e3, 2), "algbw": round(algbw, 2),
            "busbw": round(algbw * factor, 2), "steps": st["steps"], "launches": st["launches"],
@@ -257,6 +267,7 @@ def main(argv=None):
     ap.add_argument("--reps", type=int, default=None)
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--graph", action="store_true", help="replay the timed calls from a CUDA graph")
+    ap.add_argument("--bound", action="store_true", help="bind the plan once (ar_bind) and time ar_execute_bound")
     ap.add_argument("--buckets", choices=["fused", "pack"], default=None)
     ap.add_argument("--overlap", action="store_true", help="bucketed sync overlapped with a synthetic backward")
     ap.add_argument("--tokens", type=int, default=4096)
@@ -289,7 +300,8 @@ def main(argv=None):
         return
     print(json.dumps(time_case(a.n, a.count, a.dtype, a.algo, a.order, a.group_size, a.iters, a.warmup, a.reps,
                                graph=a.graph, collective=a.collective, sm_budget=a.sm_budget,
-                               kernel=a.kernel, torus_dims=tuple(int(v) for v in a.dims.split(",")))))
+                               kernel=a.kernel, torus_dims=tuple(int(v) for v in a.dims.split(",")),
+                               bound=a.bound)))
 
 
 if __name__ == "__main__":

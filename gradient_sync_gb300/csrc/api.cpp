@@ -762,6 +762,98 @@ ar_status ar_execute(const ar_plan_t* plan, void* const* bufs, void* const* outs
   return execute_steps(plan, bufs, outs, workspace, st);
 }
 
+}  // extern "C"
+
+// A plan bound to its buffers. Step plans: the launches of one ar_execute
+// recorded once into a CUDA graph (ar_bind) and replayed by ar_execute_bound.
+// Single-pass plans are one kernel, which a direct launch starts sooner than
+// a one-node graph (measured on GB300: 3.8 against 6.2 us per call back to
+// back), so they keep the validated plan and buffers and launch directly.
+struct ar_bound {
+  int device = -1;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  struct ar_plan plan;          // fused: a copy of the plan (its descriptor and stats)
+  std::vector<void*> bufs, outs;
+  bool direct = false;
+};
+
+namespace {
+
+void release(ar_bound* b) {
+  if (b == nullptr) return;
+  if (b->exec != nullptr) cudaGraphExecDestroy(b->exec);
+  if (b->graph != nullptr) cudaGraphDestroy(b->graph);
+  delete b;
+}
+
+}  // namespace
+
+extern "C" {
+
+ar_status ar_bind(const ar_plan_t* plan, void* const* bufs, void* const* outs, void* workspace, ar_bound_t** out) {
+  if (plan == nullptr || out == nullptr) return AR_EINVAL;
+  *out = nullptr;
+  const ar_status chk = check_buffers(plan, bufs, outs, workspace);
+  if (chk != AR_OK) return chk;
+  ar_bound* b = new (std::nothrow) ar_bound;
+  if (b == nullptr) return AR_ENOMEM;
+  if (plan->desc.count == 0) {  // nothing to launch: no graph, no CUDA call
+    *out = b;
+    return AR_OK;
+  }
+  if (cudaGetDevice(&b->device) != cudaSuccess) {
+    release(b);
+    return AR_ECUDA;
+  }
+  if (plan->desc.algo == AR_FUSED) {
+    b->plan = *plan;
+    const int N = plan->desc.n_ranks;
+    b->bufs.assign(bufs, bufs + N);
+    if (outs != nullptr) b->outs.assign(outs, outs + N);
+    b->direct = true;
+    *out = b;
+    return AR_OK;
+  }
+  // Record on a private stream. Relaxed mode: the launchers' first-use
+  // occupancy queries are allowed while capturing.
+  cudaStream_t cap = nullptr;
+  if (cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking) != cudaSuccess) {
+    release(b);
+    return AR_ECUDA;
+  }
+  ar_status s = AR_OK;
+  if (cudaStreamBeginCapture(cap, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
+    s = AR_ECUDA;
+  } else {
+    s = execute_steps(plan, bufs, outs, workspace, cap);
+    const cudaError_t e = cudaStreamEndCapture(cap, &b->graph);  // ends the capture even after an error
+    if (s == AR_OK && e != cudaSuccess) s = AR_ECUDA;
+  }
+  cudaStreamDestroy(cap);
+  if (s == AR_OK && cudaGraphInstantiate(&b->exec, b->graph, 0) != cudaSuccess) s = AR_ECUDA;
+  if (s != AR_OK) {
+    release(b);
+    return s;
+  }
+  *out = b;
+  return AR_OK;
+}
+
+ar_status ar_execute_bound(const ar_bound_t* bound, void* stream) {
+  if (bound == nullptr) return AR_EINVAL;
+  if (bound->exec == nullptr && !bound->direct) return AR_OK;  // count == 0
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return AR_ECUDA;
+  if (dev != bound->device) return AR_EINVAL;
+  if (bound->direct)
+    return execute_fused(&bound->plan, bound->bufs.data(), bound->outs.empty() ? nullptr : bound->outs.data(), 0,
+                         int64_t(bound->plan.desc.count), static_cast<cudaStream_t>(stream));
+  return from_cuda(cudaGraphLaunch(bound->exec, static_cast<cudaStream_t>(stream)));
+}
+
+void ar_bound_destroy(ar_bound_t* bound) { release(bound); }
+
 ar_status ar_execute_host(const ar_plan_t* plan, const void* const* host_in, void* const* host_out,
                           void* const* dev_bufs, void* workspace, void* stream) {
   if (plan == nullptr || host_in == nullptr || host_out == nullptr) return AR_EINVAL;

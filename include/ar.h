@@ -268,6 +268,36 @@ ar_status ar_execute_host(const ar_plan_t* plan, const void* const* host_in, voi
  * Other arguments and errors as ar_execute. */
 ar_status ar_execute_noalloc(const ar_plan_t* plan, void* const* bufs, void* const* outs, void* stream);
 
+/* ---------------------------------------------------------------- persistent collectives
+ * A plan bound to its buffers (Scaling ML Systems, "Collective communication":
+ * persistent, pre-registered collectives amortise the set-up of a collective
+ * that is issued again and again on the same buffers, as DDP does every
+ * step). ar_bind validates the buffers once. For a step-by-step plan it
+ * records every launch of one ar_execute(plan, bufs, outs, workspace) into a
+ * CUDA graph, which ar_execute_bound replays with one host call: 2(N-1) ring
+ * steps cost one graph launch on the host instead of 2(N-1) kernel launches.
+ * A single-pass (AR_FUSED) plan is one kernel, launched directly without the
+ * argument checks. The results are those of ar_execute, bit for bit. */
+typedef struct ar_bound ar_bound_t;
+
+/* Bind `plan` to its buffers (arguments and errors as ar_execute; nothing is
+ * launched). The plan may be destroyed afterwards; the buffers must stay
+ * allocated, at the same addresses, until ar_bound_destroy. The graph belongs
+ * to the device current at this call. count == 0 makes no CUDA call. Errors:
+ * AR_EINVAL (as ar_execute, or NULL out), AR_ENOMEM, AR_ECUDA (a CUDA call
+ * failed while recording; nothing is left behind). Recording a step plan
+ * creates CUDA graph objects (driver-managed); no buffer is allocated. */
+ar_status ar_bind(const ar_plan_t* plan, void* const* bufs, void* const* outs, void* workspace,
+                  ar_bound_t** out);
+
+/* Enqueue the bound all-reduce on `stream` (asynchronous, as ar_execute).
+ * AR_EINVAL: NULL bound, or a current device other than the one at ar_bind.
+ * Calls on one bound collective that overlap on the GPU (two streams at once)
+ * race on its buffers, as ar_execute calls would. */
+ar_status ar_execute_bound(const ar_bound_t* bound, void* stream);
+
+void ar_bound_destroy(ar_bound_t* bound);
+
 void ar_plan_destroy(ar_plan_t* plan);
 
 /* ---------------------------------------------------------------- cost model

@@ -354,3 +354,22 @@ def test_compression_calls_reject_without_touching_the_device(g):
     g.ar_compress(grads, codes, scales, b, count=0, stream=0)
     g.ar_compressed_reduce(codes, scales, outs, b, count=0, stream=0)
     g.ar_compressed_allreduce(grads, b, residuals=res, outs=grads, count=0, stream=0)
+
+
+def test_bind_validates_without_touching_the_device(g):
+    plan = g.ar_plan(4, 1024, "f32", "ring")
+    good = [0x100000 * (r + 1) for r in range(4)]
+    for bufs in ([0] + good[1:], [good[0] + 4] + good[1:], [good[0]] * 4):
+        with pytest.raises(g.ArError) as e:
+            g.ar_bind(plan, bufs)
+        assert e.value.status == g.AR_EINVAL
+    wplan = g.ar_plan(4, 1024, "bf16", "ring")
+    with pytest.raises(g.ArError) as e:  # bf16 step plans need a workspace
+        g.ar_bind(wplan, good)
+    assert e.value.status == g.AR_EINVAL
+    empty = g.ar_plan(4, 0, "f32", "ring")
+    b = g.ar_bind(empty, good)  # count 0: no graph, no CUDA call
+    g.ar_execute_bound(b, stream=0)
+    del b
+    with pytest.raises(g.ArError):
+        g._check(g._lib.load().ar_execute_bound(None, None), "ar_execute_bound")
