@@ -47,18 +47,29 @@ if ROOT not in sys.path:
 METRIC = "all-reduce algbw/busbw GB/s (N virtual ranks, 1 GB300) and % of HBM roofline"
 UNIT = "GB/s"
 PROFILE = os.path.join(ROOT, "profiles", "fused_ring_n16_192mib.md")
-KERNEL_SOURCES = ["gradient_sync_gb300/csrc/fused.cu", "gradient_sync_gb300/csrc/common.cuh",
-                  "gradient_sync_gb300/csrc/internal.h"]
+KERNEL_SOURCES = ["gradient_sync_gb300/csrc/fused.cu", "gradient_sync_gb300/csrc/common.cuh"]
+# From internal.h only what the fused kernel compiles from: its parameter
+# block and the block size (other declarations there do not change it).
+KERNEL_HEADER = "gradient_sync_gb300/csrc/internal.h"
 
 
 # ------------------------------------------------------------------ helpers
 
 
 def kernel_sources_hash() -> str:
+    """Hash of the fused kernel's sources: fused.cu, common.cuh, and from
+    internal.h the FusedParams struct and the kThreads constant."""
+    import re
+
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
+    with open(os.path.join(ROOT, KERNEL_HEADER)) as f:
+        text = f.read()
+    for pattern in (r"struct FusedParams \{.*?\n\};", r"constexpr int kThreads = \d+;"):
+        m = re.search(pattern, text, flags=re.S)
+        h.update((m.group(0) if m else "").encode())
     return h.hexdigest()[:16]
 
 

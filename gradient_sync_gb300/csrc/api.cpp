@@ -553,6 +553,7 @@ ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs
   sp.ws = static_cast<float*>(workspace);
   sp.ws_stride = p->ws_stride;
   sp.scale = d.scale;
+  sp.interleave = d.algo == AR_DBTREE ? 1 : 0;  // see the tile order in step.cu
   if (N == 1) {
     const bool in_place = outs == nullptr || outs[0] == bufs[0];
     const float scale = d.collective == AR_ALLGATHER ? 1.0f : d.scale;

@@ -59,6 +59,7 @@ struct StepParams {
   int64_t ws_stride;
   float scale;
   int n_xfer;
+  int interleave;  // 1: tiles dealt round-robin over the transfers; 0: transfer by transfer
   Transfer x[kMaxXfers];
   int32_t tile_start[kMaxXfers + 1];  // prefix sums of tiles per transfer
 };

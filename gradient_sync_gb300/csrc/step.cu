@@ -43,14 +43,32 @@ struct Raw8 {
   uint4 a, b;
 };
 
+// Loads and stores: streaming (evict-first) for the add steps, whose results
+// are read again only a step or more later; ordinary caching for the copy
+// steps, whose chunk the next step forwards (ring all-gather: 0.82 of its
+// bytes against 0.79 with streaming hints, measured on GB300 at 16 x 192 MiB).
+template <bool STREAM>
+__device__ __forceinline__ uint4 ld16(const uint4* q) {
+  if (STREAM) return __ldcs(q);
+  return *q;
+}
+template <bool STREAM>
+__device__ __forceinline__ void st16(uint4* q, const uint4& v) {
+  if (STREAM)
+    __stcs(q, v);
+  else
+    *q = v;
+}
+
+template <bool STREAM>
 __device__ __forceinline__ Raw8 load8(const Operand& o, int64_t e) {
   Raw8 r;
   if (o.f32) {
     const uint4* q = reinterpret_cast<const uint4*>(o.base + e * 4);
-    r.a = __ldcs(q);
-    r.b = __ldcs(q + 1);
+    r.a = ld16<STREAM>(q);
+    r.b = ld16<STREAM>(q + 1);
   } else {
-    r.a = __ldcs(reinterpret_cast<const uint4*>(o.base + e * 2));
+    r.a = ld16<STREAM>(reinterpret_cast<const uint4*>(o.base + e * 2));
     r.b = make_uint4(0, 0, 0, 0);
   }
   return r;
@@ -96,20 +114,38 @@ __device__ __forceinline__ void store1(const Operand& o, int64_t e, float v) {
 
 template <bool BF16, int OP>
 __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ StepParams p) {
+  constexpr bool kStream = OP != OP_COPY;
   grid_dependency_wait();
   grid_dependents_launch();
-  const int total = p.tile_start[p.n_xfer];
+  // Tile order: transfer by transfer (tile t of the prefix sums), or dealt
+  // round-robin over the transfers (tile t is tile t / n_xfer of transfer
+  // t % n_xfer, skipped past that transfer's end). The double binary tree's
+  // steps run faster interleaved (1.00 of their bytes against 0.95 at 16 x
+  // 192 MiB on GB300); the ring, Rabenseifner and hierarchical steps run 2-4 %
+  // slower interleaved, so the host picks per plan.
+  int max_tiles = 0;
+  if (p.interleave)
+    for (int x = 0; x < p.n_xfer; ++x) max_tiles = max(max_tiles, p.tile_start[x + 1] - p.tile_start[x]);
+  const int total = p.interleave ? max_tiles * p.n_xfer : p.tile_start[p.n_xfer];
   for (int t = blockIdx.x; t < total; t += gridDim.x) {
-    int lo_i = 0, hi_i = p.n_xfer;  // find x with tile_start[x] <= t < tile_start[x+1]
-    while (hi_i - lo_i > 1) {
-      const int mid = (lo_i + hi_i) >> 1;
-      if (p.tile_start[mid] <= t)
-        lo_i = mid;
-      else
-        hi_i = mid;
+    int lo_i = 0;
+    int64_t tt = 0;
+    if (p.interleave) {  // uniform across the grid
+      lo_i = t % p.n_xfer;
+      tt = t / p.n_xfer;
+      if (tt >= p.tile_start[lo_i + 1] - p.tile_start[lo_i]) continue;
+    } else {
+      int hi_i = p.n_xfer;  // find x with tile_start[x] <= t < tile_start[x+1]
+      while (hi_i - lo_i > 1) {
+        const int mid = (lo_i + hi_i) >> 1;
+        if (p.tile_start[mid] <= t)
+          lo_i = mid;
+        else
+          hi_i = mid;
+      }
+      tt = t - p.tile_start[lo_i];
     }
     const Transfer tr = p.x[lo_i];
-    const int64_t tt = t - p.tile_start[lo_i];
     const Operand X = operand<BF16>(p, tr.xs, tr.src);
     const Operand Y = operand<BF16>(p, tr.ys, tr.dst);
     const Operand D = operand<BF16>(p, tr.ds, tr.dst);
@@ -128,9 +164,9 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
     for (int u = 0; u < kStepUnroll; ++u) {
       e[u] = a0 + tt * kStepTile + (int64_t(u) * kThreads + threadIdx.x) * kStepVec;
       if (e[u] < a1) {
-        rx[u] = load8(X, e[u]);
-        if (OP == OP_ADD) ry[u] = load8(Y, e[u]);
-        if (two) rz[u] = load8(X2, e[u]);
+        rx[u] = load8<kStream>(X, e[u]);
+        if (OP == OP_ADD) ry[u] = load8<kStream>(Y, e[u]);
+        if (two) rz[u] = load8<kStream>(X2, e[u]);
       }
     }
 #pragma unroll
@@ -139,10 +175,10 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
         if (OP == OP_COPY) {  // same type on both sides: move the bytes
           if (X.f32) {
             uint4* q = reinterpret_cast<uint4*>(D.base + e[u] * 4);
-            __stcs(q, rx[u].a);
-            __stcs(q + 1, rx[u].b);
+            st16<kStream>(q, rx[u].a);
+            st16<kStream>(q + 1, rx[u].b);
           } else {
-            __stcs(reinterpret_cast<uint4*>(D.base + e[u] * 2), rx[u].a);
+            st16<kStream>(reinterpret_cast<uint4*>(D.base + e[u] * 2), rx[u].a);
           }
         } else {
           float f[8];
