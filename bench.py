@@ -197,13 +197,19 @@ def dist_env():
     return world, rank, local
 
 
-def init_dist(world: int, backend: str):
+def init_dist(world: int, backend: str, timeout_s: float | None = None):
+    """The process group of a multi-GPU run (None for one process). With
+    `timeout_s`, a collective that waits longer (a rank that never arrives)
+    raises instead of blocking."""
     if world <= 1:
         return None
+    import datetime
+
     import torch.distributed as dist
 
     if not dist.is_initialized():
-        dist.init_process_group(backend=backend)
+        kw = {} if timeout_s is None else {"timeout": datetime.timedelta(seconds=timeout_s)}
+        dist.init_process_group(backend=backend, **kw)
     return dist
 
 
