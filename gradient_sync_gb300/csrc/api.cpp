@@ -513,8 +513,12 @@ void fused_tiling(const ar_desc& d, FusedParams& fp, int64_t tile) {
   fp.tiles_per_seg = tps;
 }
 
+// `host_memory`: the buffers are pinned host memory read and written over the
+// host link; only the register pipeline, whose plain loads and stores are
+// known to work there, runs on them (the bulk-copy kernels are kept to device
+// memory).
 ar_status execute_fused(const ar_plan_t* p, void* const* bufs, void* const* outs, int64_t e_lo,
-                        int64_t e_hi, cudaStream_t stream) {
+                        int64_t e_hi, cudaStream_t stream, bool host_memory = false) {
   const ar_desc& d = p->desc;
   FusedParams fp;
   std::memset(&fp, 0, sizeof(fp));
@@ -532,7 +536,11 @@ ar_status execute_fused(const ar_plan_t* p, void* const* bufs, void* const* outs
   fp.e_hi = e_hi;
   fp.scale = d.collective == AR_ALLGATHER ? 1.0f : d.scale;  // an all-gather only copies
   int stages = 0, tile_bytes = 0;
-  if (d.kernel == AR_KERNEL_BULK && tma_shape(d.n_ranks, stages, tile_bytes)) {  // checked at plan time
+  if (!host_memory && d.kernel != AR_KERNEL_LOADS && d.collective == AR_ALLGATHER && d.n_ranks > 1) {  // bulk: faster
+    fused_tiling(d, fp, allgather_bulk_tile_elems(d.dtype));
+    return from_cuda(launch_allgather_bulk(fp, d.dtype, d.sm_budget, stream));
+  }
+  if (!host_memory && d.kernel == AR_KERNEL_BULK && tma_shape(d.n_ranks, stages, tile_bytes)) {  // checked at plan time
     fused_tiling(d, fp, tile_bytes / int64_t(esize(d.dtype)));
     return from_cuda(launch_fused_tma(fp, d.dtype, stages, tile_bytes, d.sm_budget, stream));
   }
@@ -669,7 +677,8 @@ ar_status ar_plan(const ar_desc* desc, ar_plan_t** out) {
   if (d.kernel < AR_KERNEL_AUTO || d.kernel > AR_KERNEL_BULK) return AR_EINVAL;
   if (d.kernel == AR_KERNEL_BULK && d.algo == AR_FUSED && N > 1) {
     int stages = 0, tile_bytes = 0;
-    if (d.collective != AR_ALLREDUCE || !tma_shape(N, stages, tile_bytes)) return AR_EUNSUPPORTED;
+    const bool ok = d.collective == AR_ALLGATHER || (d.collective == AR_ALLREDUCE && tma_shape(N, stages, tile_bytes));
+    if (!ok) return AR_EUNSUPPORTED;
   }
   if (d.algo == AR_TORUS) {
     int prod = 1;
@@ -891,7 +900,7 @@ ar_status ar_execute_host(const ar_plan_t* plan, const void* const* host_in, voi
     if (direct) {
       const ar_status e = check_buffers(plan, in_dev.data(), out_dev.data(), nullptr);
       if (e != AR_OK) return e;
-      const ar_status x = execute_fused(plan, in_dev.data(), out_dev.data(), 0, L, st);
+      const ar_status x = execute_fused(plan, in_dev.data(), out_dev.data(), 0, L, st, true);
       if (x != AR_OK) return x;
       return from_cuda(cudaStreamSynchronize(st));
     }

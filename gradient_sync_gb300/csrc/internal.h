@@ -146,6 +146,9 @@ cudaError_t launch_fused_tma(const FusedParams& p, ar_dtype dtype, int stages, i
 cudaError_t launch_bucket_tma(const BucketFusedParams& p, ar_dtype dtype, int stages, int tile_bytes, int sm_budget,
                               cudaStream_t stream);
 cudaError_t launch_wait_timeout(uint32_t polls, cudaStream_t stream);
+// The all-gather with bulk copies (fused_tma.cu): tile size in elements, launch.
+int64_t allgather_bulk_tile_elems(ar_dtype dtype);
+cudaError_t launch_allgather_bulk(const FusedParams& p, ar_dtype dtype, int sm_budget, cudaStream_t stream);
 // Blockwise INT8 compression (compress.cu).
 cudaError_t launch_compress(const CompressParams& p, ar_dtype dtype, cudaStream_t stream);
 cudaError_t launch_compressed_reduce(const CompressParams& p, ar_dtype out_dtype, cudaStream_t stream);

@@ -137,18 +137,24 @@ typedef enum { AR_ALLREDUCE = 0, AR_REDUCE_SCATTER = 1, AR_ALLGATHER = 2 } ar_co
 /* Which kernel runs the single pass (AR_FUSED all-reduce and
  * ar_bucket_allreduce). Both compute the same result, bit for bit; they differ
  * in how bytes move between HBM and the SM.
- *  AR_KERNEL_AUTO:  the library's choice (currently AR_KERNEL_LOADS, the
- *                   faster of the two at every SM budget measured).
+ *  AR_KERNEL_AUTO:  the library's choice, the faster one measured: the
+ *                   register pipeline for the all-reduce and reduce-scatter
+ *                   (at every SM budget measured), bulk copies for the
+ *                   all-gather (0.89 of HBM against 0.86).
  *  AR_KERNEL_LOADS: persistent register pipeline, 2 CTAs per SM; each thread
  *                   keeps a batch of 16-byte loads in flight.
- *  AR_KERNEL_BULK:  one CTA per SM; a producer warp stages every rank's slice
- *                   of a tile in shared memory with bulk copies (TMA) through a
- *                   ring of mbarrier-guarded stages; consumer warps fold from
- *                   shared memory and the result leaves through bulk stores.
- *                   All-reduce only, N <= 24 (the stages must fit in shared
- *                   memory); otherwise ar_plan returns AR_EUNSUPPORTED. Its
- *                   waits are bounded: a wait that runs out sets the device
- *                   status word (ar_device_status) instead of hanging.
+ *  AR_KERNEL_BULK:  bulk copies (TMA) through shared memory.
+ *                   All-reduce: one CTA per SM; a producer warp stages every
+ *                   rank's slice of a tile in shared memory through a ring of
+ *                   mbarrier-guarded stages; consumer warps fold from shared
+ *                   memory and the result leaves through bulk stores; N <= 24
+ *                   (the stages must fit in shared memory).
+ *                   All-gather: each tile of a chunk is bulk-loaded once from
+ *                   its owner and bulk-stored to the N ranks; any N.
+ *                   The reduce-scatter has no bulk variant. Unsupported
+ *                   requests make ar_plan return AR_EUNSUPPORTED. The waits are
+ *                   bounded: a wait that runs out sets the device status word
+ *                   (ar_device_status) instead of hanging.
  * The step executors (AR_RING, AR_RABENSEIFNER, AR_HIER) ignore it. */
 typedef enum { AR_KERNEL_AUTO = 0, AR_KERNEL_LOADS = 1, AR_KERNEL_BULK = 2 } ar_kernel;
 

@@ -222,12 +222,14 @@ def test_kernel_choice_validation(g):
     with pytest.raises(g.ArError) as e:
         g.ar_plan(8, 100, "f32", "fused", kernel=3)
     assert e.value.status == g.AR_EINVAL
-    for bad in (dict(n_ranks=25), dict(collective="reduce_scatter"), dict(collective="allgather")):
+    for bad in (dict(n_ranks=25), dict(collective="reduce_scatter")):
         args = dict(n_ranks=8, count=100, dtype="f32", algo="fused", kernel="bulk")
         args.update(bad)
-        with pytest.raises(g.ArError) as e:  # the stages must fit in shared memory; all-reduce only
+        with pytest.raises(g.ArError) as e:  # the all-reduce's stages must fit in shared memory; no RS
             g.ar_plan(**args)
         assert e.value.status == g.AR_EUNSUPPORTED, bad
+    for n in (2, 25, 64):  # the all-gather stages one rank's tile: any N
+        assert g.ar_plan_desc(g.ar_plan(n, 100, "f32", "fused", kernel="bulk", collective="allgather"))["kernel"] == "bulk"
     for n in (1, 2, 16, 24):
         assert g.ar_plan_desc(g.ar_plan(n, 100, "bf16", "fused", kernel="bulk"))["kernel"] == "bulk"
     assert g.ar_plan_desc(g.ar_plan(64, 100, "f32", "ring", kernel="bulk"))["kernel"] == "bulk"  # ignored

@@ -27,11 +27,12 @@ def g():
 SIZES = [(1, 9), (2, 7), (3, 1000), (4, 4099), (8, 20003), (16, 100003), (64, 5000)]
 
 
-def _run(g, x, dtype, algo, coll, order="ring", scale=1.0, out_of_place=False):
+def _run(g, x, dtype, algo, coll, order="ring", scale=1.0, out_of_place=False, kernel="auto", sm_budget=0):
     N, L = x.shape
     devs = [to_device(x[r], dtype) for r in range(N)]
     outs = [torch.full_like(d, 7.0) for d in devs] if out_of_place else None
-    plan = g.ar_plan(N, L, dtype, algo, order=order, scale=scale, collective=coll)
+    plan = g.ar_plan(N, L, dtype, algo, order=order, scale=scale, collective=coll, kernel=kernel,
+                     sm_budget=sm_budget)
     ws = g.workspace_for(plan)
     if ws is not None:
         ws.fill_(0xFF)
@@ -68,17 +69,66 @@ def test_reduce_scatter(g, dtype, algo, order, N, L):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("algo", ["ring", "fused"])
+@pytest.mark.parametrize("algo,kernel", [("ring", "auto"), ("fused", "auto"), ("fused", "loads")])
 @pytest.mark.parametrize("N,L", SIZES)
 @pytest.mark.parametrize("out_of_place", [False, True])
-def test_allgather(g, dtype, algo, N, L, out_of_place):
+def test_allgather(g, dtype, algo, kernel, N, L, out_of_place):
     x = workloads.all_ranks(workloads.small_spec(N, L, dtype, "uniform", seed=N * 5 + L))
-    got = _run(g, x, dtype, algo, "allgather", scale=3.0, out_of_place=out_of_place)  # scale is ignored
+    got = _run(g, x, dtype, algo, "allgather", scale=3.0, out_of_place=out_of_place,  # scale is ignored
+               kernel=kernel)
     want, _ = schedules.ring_allgather(x)
     b = chunk_bounds(L, N)
     assert np.array_equal(want[0], np.concatenate([x[c, b[c]:b[c + 1]] for c in range(N)]))
     for r in range(N):
         assert_bits_equal(got[r], want[r], f"rank {r}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N,L", SIZES + [(5, 1), (7, 3), (16, 37), (12, (1 << 20) + 13)])
+@pytest.mark.parametrize("out_of_place", [False, True])
+def test_allgather_bulk_copies(g, dtype, N, L, out_of_place):
+    """The all-gather through bulk copies (one load, N stores per tile) gives
+    the oracle's result, ragged chunk heads and tails included, under an SM
+    budget too."""
+    x = workloads.all_ranks(workloads.small_spec(N, L, dtype, "uniform", seed=N * 7 + L))
+    want, _ = schedules.ring_allgather(x)
+    for sm_budget in (0, 5):
+        got = _run(g, x, dtype, "fused", "allgather", out_of_place=out_of_place, kernel="bulk", sm_budget=sm_budget)
+        for r in range(N):
+            assert_bits_equal(got[r], want[r], f"rank {r} (sm_budget {sm_budget})")
+
+
+def test_allgather_bulk_from_host_slabs(g):
+    """ar_execute_host on pageable memory runs the all-gather in element-range
+    slabs: each slab's chunk pieces go through the bulk pipeline."""
+    N, L = 6, (3 << 20) + 17
+    x = workloads.all_ranks(workloads.small_spec(N, L, "f32", "uniform", seed=11))
+    want, _ = schedules.ring_allgather(x)
+    plan = g.ar_plan(N, L, "f32", "fused", collective="allgather", kernel="bulk")
+    host_in = [torch.from_numpy(x[r].copy()) for r in range(N)]
+    host_out = [torch.zeros(L) for _ in range(N)]
+    dev = [torch.empty(L, device="cuda") for _ in range(N)]
+    g.ar_execute_host(plan, host_in, host_out, dev)
+    for r in range(N):
+        assert_bits_equal(host_out[r].numpy(), want[r], f"rank {r}")
+
+
+def test_allgather_bulk_full_size(g):
+    """16 ranks x 192 MiB fp32, in the launch configuration the timings use:
+    every output chunk is a bit-for-bit copy of its owner's chunk (the
+    definition), checked on the device over the whole buffers."""
+    N, L = 16, 50_331_648
+    b = chunk_bounds(L, N)
+    devs = [torch.randn(L, device="cuda") for _ in range(N)]
+    outs = [torch.zeros_like(d) for d in devs]
+    plan = g.ar_plan(N, L, "f32", "fused", collective="allgather", kernel="bulk")
+    g.ar_execute(plan, devs, outs=outs)
+    torch.cuda.synchronize()
+    for r in range(N):
+        for c in range(N):
+            assert torch.equal(outs[r][b[c]:b[c + 1]].view(torch.int32), devs[c][b[c]:b[c + 1]].view(torch.int32))
+    del devs, outs
+    torch.cuda.empty_cache()
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
