@@ -562,6 +562,12 @@ ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs
   sp.ws_stride = p->ws_stride;
   sp.scale = d.scale;
   sp.interleave = d.algo == AR_DBTREE ? 1 : 0;  // see the tile order in step.cu
+  // 256-bit accesses when every base pointer is 32-byte aligned (see step.cu)
+  bool v8 = workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 32 == 0;
+  for (int r = 0; r < N; ++r) {
+    v8 = v8 && reinterpret_cast<uintptr_t>(bufs[r]) % 32 == 0;
+    if (outs != nullptr) v8 = v8 && reinterpret_cast<uintptr_t>(outs[r]) % 32 == 0;
+  }
   if (N == 1) {
     const bool in_place = outs == nullptr || outs[0] == bufs[0];
     const float scale = d.collective == AR_ALLGATHER ? 1.0f : d.scale;
@@ -572,7 +578,7 @@ ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs
     sp.tile_start[0] = 0;
     const int64_t body = std::max<int64_t>(rdown(d.count, kStepVec), 0);
     sp.tile_start[1] = int32_t(std::max<int64_t>(1, (body + kStepTile - 1) / kStepTile));
-    return from_cuda(launch_step(sp, d.dtype, OP_FINISH, sp.tile_start[1], false, d.sm_budget, stream));
+    return from_cuda(launch_step(sp, d.dtype, OP_FINISH, sp.tile_start[1], false, d.sm_budget, v8, stream));
   }
   if (d.collective == AR_ALLGATHER && outs != nullptr) {
     // out of place: every rank's own chunk is copied to its output first (the
@@ -592,7 +598,7 @@ ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs
         tiles += int(std::max<int64_t>(1, (body + kStepTile - 1) / kStepTile));
       }
       sp.tile_start[sp.n_xfer] = tiles;
-      const ar_status s = from_cuda(launch_step(sp, d.dtype, OP_COPY, tiles, true, d.sm_budget, stream));
+      const ar_status s = from_cuda(launch_step(sp, d.dtype, OP_COPY, tiles, true, d.sm_budget, v8, stream));
       if (s != AR_OK) return s;
     }
   }
@@ -610,7 +616,7 @@ ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs
         tiles += int(std::max<int64_t>(1, (body + kStepTile - 1) / kStepTile));
       }
       sp.tile_start[sp.n_xfer] = tiles;
-      const ar_status s = from_cuda(launch_step(sp, d.dtype, st.op, tiles, true, d.sm_budget, stream));
+      const ar_status s = from_cuda(launch_step(sp, d.dtype, st.op, tiles, true, d.sm_budget, v8, stream));
       if (s != AR_OK) return s;
     }
   }

@@ -132,8 +132,10 @@ constexpr int kStepUnroll = 2;
 constexpr int64_t kStepTile = kThreads * kStepVec * kStepUnroll;  // 4096
 constexpr int kPackTile = kThreads * 8;                   // 2048 elements
 
+// v8: every base pointer of the call is 32-byte aligned, so the fp32 vectors
+// may move as 256-bit accesses.
 cudaError_t launch_step(const StepParams& p, ar_dtype dtype, StepOp op, int total_tiles, bool pdl,
-                        int sm_budget, cudaStream_t stream);
+                        int sm_budget, bool v8, cudaStream_t stream);
 cudaError_t launch_fused(const FusedParams& p, ar_dtype dtype, int sm_budget, cudaStream_t stream);
 int64_t fused_tile_elems(ar_dtype dtype, int n, int order, int collective);
 cudaError_t launch_bucket_fused(const BucketFusedParams& p, ar_dtype dtype, int sm_budget, cudaStream_t stream);

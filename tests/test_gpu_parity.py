@@ -274,3 +274,28 @@ def test_bucket_paths_with_sm_budget(g, sm_budget, kernel):
         for t in b:
             for r in range(N):
                 assert_bits_equal(to_host(dev[r][t], "bf16"), want[(t, 0)][r], f"t={t} r={r}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("algo", ["ring", "rabenseifner", "dbtree", "recdoubling"])
+def test_step_executor_on_16_byte_aligned_buffers(g, dtype, algo):
+    """Buffers that are 16- but not 32-byte aligned (views 16 bytes into a
+    larger allocation) take the 16-byte access path of the step kernel; the
+    result is the same bits."""
+    N, L = 8, 20011
+    x = workloads.all_ranks(workloads.small_spec(N, L, dtype, "normal", seed=41))
+    esz = 2 if dtype == "bf16" else 4
+    shift = 16 // esz
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    big = [torch.empty(L + 64, dtype=tdt, device="cuda") for _ in range(N)]
+    devs = [b[shift:shift + L] for b in big]
+    for r in range(N):
+        devs[r].copy_(to_device(x[r], dtype))
+        assert devs[r].data_ptr() % 32 == 16
+    plan = g.ar_plan(N, L, dtype, algo, scale=0.5)
+    ws = g.workspace_for(plan)
+    g.ar_execute(plan, devs, workspace=ws)
+    torch.cuda.synchronize()
+    want = expected(algo, "ring", x, dtype, scale=0.5)
+    for r in range(N):
+        assert_bits_equal(to_host(devs[r].contiguous(), dtype), want, f"rank {r}")
