@@ -483,8 +483,9 @@ ar_status check_buffers(const ar_plan_t* p, void* const* bufs, void* const* outs
 ar_status from_cuda(cudaError_t e) { return e == cudaSuccess ? AR_OK : AR_ECUDA; }
 
 // Segment count and tiles per segment of a fused launch over [e_lo, e_hi),
-// for tiles of `tile` elements.
-void fused_tiling(const ar_desc& d, FusedParams& fp, int64_t tile) {
+// for tiles of `tile` elements whose segment bodies start and end on
+// multiples of W elements (the kernel's vector).
+void fused_tiling(const ar_desc& d, FusedParams& fp, int64_t tile, int64_t W) {
   const int N = d.n_ranks;
   const int64_t L = int64_t(d.count);
   std::vector<std::pair<int64_t, int64_t>> segs;
@@ -501,7 +502,6 @@ void fused_tiling(const ar_desc& d, FusedParams& fp, int64_t tile) {
   } else {
     segs.push_back({0, L});
   }
-  const int64_t W = d.dtype == AR_BF16 ? 8 : 4;
   int64_t tps = 1;
   for (auto& s : segs) {
     const int64_t lo = std::max(s.first, fp.e_lo), hi = std::min(s.second, fp.e_hi);
@@ -537,14 +537,15 @@ ar_status execute_fused(const ar_plan_t* p, void* const* bufs, void* const* outs
   fp.scale = d.collective == AR_ALLGATHER ? 1.0f : d.scale;  // an all-gather only copies
   int stages = 0, tile_bytes = 0;
   if (!host_memory && d.kernel != AR_KERNEL_LOADS && d.collective == AR_ALLGATHER && d.n_ranks > 1) {  // bulk: faster
-    fused_tiling(d, fp, allgather_bulk_tile_elems(d.dtype));
+    fused_tiling(d, fp, allgather_bulk_tile_elems(d.dtype), d.dtype == AR_BF16 ? 8 : 4);
     return from_cuda(launch_allgather_bulk(fp, d.dtype, d.sm_budget, stream));
   }
   if (!host_memory && d.kernel == AR_KERNEL_BULK && tma_shape(d.n_ranks, stages, tile_bytes)) {  // checked at plan time
-    fused_tiling(d, fp, tile_bytes / int64_t(esize(d.dtype)));
+    fused_tiling(d, fp, tile_bytes / int64_t(esize(d.dtype)), d.dtype == AR_BF16 ? 8 : 4);
     return from_cuda(launch_fused_tma(fp, d.dtype, stages, tile_bytes, d.sm_budget, stream));
   }
-  fused_tiling(d, fp, fused_tile_elems(d.dtype, d.n_ranks, d.order, d.collective));
+  fused_tiling(d, fp, fused_tile_elems(d.dtype, d.n_ranks, d.order, d.collective, false),
+               fused_vec_elems(d.dtype, false));
   return from_cuda(launch_fused(fp, d.dtype, d.sm_budget, stream));
 }
 
@@ -1160,11 +1161,15 @@ ar_status ar_bucket_allreduce(int n_ranks, void* const* tensors, const size_t* c
   for (int t = t_begin; t < t_end; ++t) Lb += int64_t(counts[t]);
   if (Lb == 0) return AR_OK;
   const auto b = cuts(0, Lb, N);
-  const int64_t W = dtype == AR_BF16 ? 8 : 4;
   int stages = 0, tile_bytes = 0;
   const bool tma = kernel == AR_KERNEL_BULK;
+  bool v8 = !tma && N > 4;  // 32-byte vectors when every tensor of the bucket is 32-byte aligned
+  for (int t = t_begin; t < t_end && v8; ++t)
+    for (int r = 0; r < N; ++r)
+      if (reinterpret_cast<uintptr_t>(tensors[size_t(r) * n_tensors + t]) % 32 != 0) v8 = false;
+  const int64_t W = tma ? (dtype == AR_BF16 ? 8 : 4) : fused_vec_elems(dtype, v8);  // the kernel's vector
   if (tma && !tma_shape(N, stages, tile_bytes)) return AR_EUNSUPPORTED;
-  const int64_t tile = tma ? tile_bytes / int64_t(esize(dtype)) : fused_tile_elems(dtype, N, AR_ORDER_RING, AR_ALLREDUCE);
+  const int64_t tile = tma ? tile_bytes / int64_t(esize(dtype)) : fused_tile_elems(dtype, N, AR_ORDER_RING, AR_ALLREDUCE, v8);
   const int max_group = std::min(AR_MAX_BUCKET_TENSORS, kMaxBucketPtrs / N);
   static thread_local BucketFusedParams bp;
   std::memset(&bp, 0, sizeof(bp));
@@ -1178,7 +1183,7 @@ ar_status ar_bucket_allreduce(int n_ranks, void* const* tensors, const size_t* c
     bp.scale = scale;
     bp.tile_start[bp.n_seg] = tiles;
     const cudaError_t e = tma ? launch_bucket_tma(bp, dtype, stages, tile_bytes, sm_budget, static_cast<cudaStream_t>(stream))
-                              : launch_bucket_fused(bp, dtype, sm_budget, static_cast<cudaStream_t>(stream));
+                              : launch_bucket_fused(bp, dtype, sm_budget, v8, static_cast<cudaStream_t>(stream));
     std::memset(&bp, 0, sizeof(bp));
     nt = 0;
     tiles = 0;

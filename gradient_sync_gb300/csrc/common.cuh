@@ -118,6 +118,47 @@ struct Lane<true, false> {  // 1 x bf16
   }
 };
 
+// A 32-byte lane: 8 fp32 or 16 bf16 elements moved by one 256-bit access
+// (ld/st.global.cs.v8.b32, sm_100 and later). Addresses must be 32-byte
+// aligned: kernels use it only when the host has checked every base pointer.
+template <bool BF16>
+struct Lane32 {
+  static constexpr int W = BF16 ? 16 : 8;
+  struct raw_t {
+    uint32_t w[8];
+  };
+  static __device__ __forceinline__ raw_t load(const char* base, int64_t e) {
+    raw_t r;
+    asm volatile("ld.global.cs.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]), "=r"(r.w[5]), "=r"(r.w[6]),
+                   "=r"(r.w[7])
+                 : "l"(base + e * (BF16 ? 2 : 4)));
+    return r;
+  }
+  static __device__ __forceinline__ void widen(const raw_t& r, float (&f)[W]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (BF16) {
+        f[2 * i] = bf16lo(r.w[i]);
+        f[2 * i + 1] = bf16hi(r.w[i]);
+      } else {
+        f[i] = __uint_as_float(r.w[i]);
+      }
+    }
+  }
+  static __device__ __forceinline__ raw_t narrow(const float (&f)[W]) {
+    raw_t r;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) r.w[i] = BF16 ? pack_bf16x2(f[2 * i], f[2 * i + 1]) : __float_as_uint(f[i]);
+    return r;
+  }
+  static __device__ __forceinline__ void store(char* base, int64_t e, const raw_t& r) {
+    asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(base + e * (BF16 ? 2 : 4)), "r"(r.w[0]),
+                 "r"(r.w[1]), "r"(r.w[2]), "r"(r.w[3]), "r"(r.w[4]), "r"(r.w[5]), "r"(r.w[6]), "r"(r.w[7])
+                 : "memory");
+  }
+};
+
 // ---------------------------------------------------------------------------
 // Summation folds over the ranks of one element position.
 //

@@ -137,8 +137,11 @@ constexpr int kPackTile = kThreads * 8;                   // 2048 elements
 cudaError_t launch_step(const StepParams& p, ar_dtype dtype, StepOp op, int total_tiles, bool pdl,
                         int sm_budget, bool v8, cudaStream_t stream);
 cudaError_t launch_fused(const FusedParams& p, ar_dtype dtype, int sm_budget, cudaStream_t stream);
-int64_t fused_tile_elems(ar_dtype dtype, int n, int order, int collective);
-cudaError_t launch_bucket_fused(const BucketFusedParams& p, ar_dtype dtype, int sm_budget, cudaStream_t stream);
+// Register pipeline: elements per vector (v8: 32-byte vectors, bucket kernel
+// only, N > 4 and every pointer 32-byte aligned) and per tile.
+int fused_vec_elems(ar_dtype dtype, bool v8);
+int64_t fused_tile_elems(ar_dtype dtype, int n, int order, int collective, bool v8);
+cudaError_t launch_bucket_fused(const BucketFusedParams& p, ar_dtype dtype, int sm_budget, bool v8, cudaStream_t stream);
 cudaError_t launch_pack(const PackParams& p, ar_dtype dtype, bool unpack, cudaStream_t stream);
 cudaError_t read_device_status(unsigned int* value, bool clear);
 // The bulk-copy variant of the fused all-reduce (fused_tma.cu).

@@ -299,3 +299,39 @@ def test_step_executor_on_16_byte_aligned_buffers(g, dtype, algo):
     want = expected(algo, "ring", x, dtype, scale=0.5)
     for r in range(N):
         assert_bits_equal(to_host(devs[r].contiguous(), dtype), want, f"rank {r}")
+
+
+@pytest.mark.parametrize("aligned32", [True, False])
+def test_bucket_allreduce_vector_widths(g, aligned32):
+    """The fused bucket pass moves 32-byte vectors when every tensor is
+    32-byte aligned (8 ranks) and 16-byte vectors otherwise (tensors placed 16
+    bytes into larger allocations); both give the oracle's bits, ragged tensor
+    sizes included."""
+    from oracle import buckets as ob
+
+    N, dtype = 8, "bf16"
+    counts = [5, 1000, 37, 4096, 9, 2051, 777, 64, 3, 30_011]
+    scale = 1.0 / N
+    rng = np.random.default_rng(17)
+    host = [[numerics.f32_to_bf16_rne((rng.standard_normal(c) * 1e-3).astype(np.float32)) for c in counts]
+            for _ in range(N)]
+    tdt = torch.bfloat16
+    shift = 0 if aligned32 else 8  # 16 bytes of bf16
+    keep, dev = [], []
+    for r in range(N):
+        row = []
+        for t, c in enumerate(counts):
+            big = torch.empty(c + 64, dtype=tdt, device="cuda")
+            keep.append(big)
+            v = big[shift:shift + c]
+            v.copy_(to_device(host[r][t], dtype))
+            assert (v.data_ptr() % 32 == 0) == aligned32
+            row.append(v)
+        dev.append(row)
+    lo, hi = 0, len(counts)
+    g.ar_bucket_allreduce(dev, counts, lo, hi, dtype, scale)
+    torch.cuda.synchronize()
+    want = ob.sync_bucket(host, list(range(lo, hi)), counts, scale)
+    for t in range(lo, hi):
+        for r in range(N):
+            assert_bits_equal(to_host(dev[r][t].contiguous(), dtype), want[(t, 0)][r], f"t={t} r={r}")
