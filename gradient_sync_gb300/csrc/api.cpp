@@ -1361,7 +1361,7 @@ const char* ar_status_string(ar_status status) {
   switch (status) {
     case AR_OK: return "AR_OK: success";
     case AR_EINVAL: return "AR_EINVAL: invalid argument";
-    case AR_EUNSUPPORTED: return "AR_EUNSUPPORTED: not supported by this build";
+    case AR_EUNSUPPORTED: return "AR_EUNSUPPORTED: not supported by the library";
     case AR_ENOMEM: return "AR_ENOMEM: host allocation failed";
     case AR_ECUDA: return "AR_ECUDA: CUDA runtime error";
     case AR_ETIMEOUT: return "AR_ETIMEOUT: a device-side wait ran out of time";

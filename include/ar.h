@@ -47,7 +47,7 @@ extern "C" {
 typedef enum {
   AR_OK = 0,
   AR_EINVAL = 1,        /* bad argument: see each call */
-  AR_EUNSUPPORTED = 2,  /* valid request this build does not implement */
+  AR_EUNSUPPORTED = 2,  /* valid request the library does not implement */
   AR_ENOMEM = 3,        /* host allocation failed */
   AR_ECUDA = 4,         /* a CUDA runtime call failed */
   AR_ETIMEOUT = 5       /* a device-side bounded wait ran out (sticky) */
