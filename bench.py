@@ -22,7 +22,8 @@ Reported (one JSON line from rank 0):
   e2e        the same all-reduce from pinned host buffers through
              ar_execute_host, copies included
   cpu_baseline  the CPU oracle (step-by-step ring simulation) on a bounded
-             sample of the same workload, on the host cores
+             sample of the same workload: one process per host core (value,
+             cores) and one core alone (value_one_core)
 
 With --gpus N > 1 (torchrun, one process per GPU) every GPU all-reduces its
 own copy of the workload (weak scaling, no collective on the data path); the
@@ -159,32 +160,59 @@ class ClockSampler:
                 "samples": len(loaded), "power_w_max": max(r["power"] for r in rows)}
 
 
-def cpu_baseline(seconds: float = 10.0):
-    """The oracle (step-by-step ring simulation in numpy) on a bounded sample of
-    the workload: one 16 Ki-element window per chunk of every rank."""
+def _oracle_sample(win: int):
+    """The cpu_baseline sample: one `win`-element window per chunk of every
+    rank of the 16 x 192 MiB workload, and the element indices it covers."""
     import numpy as np
 
     import workloads
-    from oracle import schedules
 
     spec = workloads.RING_N16_192MIB
     N, L = spec.n_ranks, spec.count
-    win = 16 * 1024
     idx = np.concatenate([np.arange((c * L) // N, (c * L) // N + win) for c in range(N)]).astype(np.int64)
     x = np.stack([np.concatenate([workloads.rank_buffer(spec, r, (c * L) // N, (c * L) // N + win, threads=1)
                                   for c in range(N)]) for r in range(N)])
+    return x, idx, L
+
+
+def _oracle_loop(args):
+    """Run the oracle's step-by-step ring on the sample for `seconds`; returns
+    (repetitions, elapsed seconds, sampled bytes per rank)."""
+    x, idx, L, seconds = args
+    from oracle import schedules
+
     reps, t0 = 0, time.perf_counter()
     while True:
         schedules.ring_allreduce(x, idx=idx, L=L)
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds:
-            break
-    per_rank_bytes = idx.size * 4
-    return {"value": round(per_rank_bytes * reps / el / 1e9, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{N} ranks x {idx.size} fp32 elements ({win} per chunk, all {N} chunks) of the "
-                      f"192 MiB workload, step-by-step ring simulation repeated {reps} times in {el:.1f} s; "
-                      f"algbw = sampled per-rank bytes / time"}
+            return reps, el, idx.size * 4
+
+
+def cpu_baseline(seconds: float = 10.0):
+    """The oracle (step-by-step ring simulation in numpy) on a bounded sample of
+    the workload, one 16 Ki-element window per chunk of every rank: on one core,
+    then as one process per host core, each running the same sample (elements
+    are independent, so cores multiply the throughput)."""
+    import multiprocessing as mp
+
+    win = 16 * 1024
+    x, idx, L = _oracle_sample(win)
+    reps, el, per_rank = _oracle_loop((x, idx, L, seconds))
+    one = per_rank * reps / el / 1e9
+    procs = max(1, os.cpu_count() or 1)
+    ctx = mp.get_context("spawn")  # this process has initialised CUDA: no fork
+    with ctx.Pool(procs) as pool:
+        res = pool.map(_oracle_loop, [(x, idx, L, seconds)] * procs)
+    wall = max(e for _, e, _ in res)
+    many = sum(r * b for r, _, b in res) / wall / 1e9
+    return {"value": round(many, 6), "unit": UNIT, "cores": procs, "kind": "oracle",
+            "value_one_core": round(one, 6),
+            "sample": f"16 ranks x {idx.size} fp32 elements ({win} per chunk, all 16 chunks) of the 192 MiB "
+                      f"workload, step-by-step ring simulation; {procs} processes each repeating it for "
+                      f"{seconds:.0f} s (one core alone: {reps} repetitions in {el:.1f} s); algbw = sampled "
+                      f"per-rank bytes / time"}
 
 
 # ------------------------------------------------------------------ distributed harness
