@@ -335,3 +335,25 @@ def test_bucket_allreduce_vector_widths(g, aligned32):
     for t in range(lo, hi):
         for r in range(N):
             assert_bits_equal(to_host(dev[r][t].contiguous(), dtype), want[(t, 0)][r], f"t={t} r={r}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("algo,order", [("fused", "ring"), ("fused", "tree"), ("ring", "ring"),
+                                        ("rabenseifner", "ring"), ("hier", "ring"), ("dbtree", "ring")])
+def test_mixed_in_and_out_of_place(g, dtype, algo, order):
+    """outs[r] may equal bufs[r] rank by rank: even ranks in place, odd ranks
+    into separate outputs, in one call. Every rank gets the oracle's bits and
+    the odd ranks' inputs are untouched."""
+    N, L = 8, 50_021
+    x = workloads.all_ranks(workloads.small_spec(N, L, dtype, "normal", seed=23))
+    devs = [to_device(x[r], dtype) for r in range(N)]
+    outs = [devs[r] if r % 2 == 0 else torch.empty_like(devs[r]) for r in range(N)]
+    plan = g.ar_plan(N, L, dtype, algo, order=order, group_size=4 if algo == "hier" else 0, scale=0.25)
+    ws = g.workspace_for(plan)
+    g.ar_execute(plan, devs, outs=outs, workspace=ws)
+    torch.cuda.synchronize()
+    want = expected(algo, order, x, dtype, group_size=4 if algo == "hier" else 0, scale=0.25)
+    for r in range(N):
+        assert_bits_equal(to_host(outs[r], dtype), want, f"rank {r}")
+        if r % 2:
+            np.testing.assert_array_equal(to_host(devs[r], dtype), x[r])
