@@ -42,8 +42,8 @@
 // from a half-integer, rint(y) equals rint(RN(x / s)); otherwise (rarely: a
 // quotient near a tie) the thread takes the correctly rounded quotient
 // __fdiv_rn(x, s) itself, so ties are decided exactly as the definition says.
-// Codes are kept as integer-valued floats, normalised so that a zero code is
-// +0 (as an integer code converted to float is).
+// Codes are kept as integer-valued floats; a zero code is +0 (as an integer
+// code converted to float is).
 #include "common.cuh"
 
 namespace ar {
@@ -181,34 +181,44 @@ __device__ __forceinline__ void sub_each(float (&d)[n], const float (&a)[n], con
   for (int w = 0; w < n; ++w) d[w] = __fsub_rn(a[w], b[w]);
 }
 
+// The nearest integer to y (ties to even) as a float, for |y| < 2^22, by the
+// classic rounding-to-integer addition: y + 1.5 * 2^23 lands in a binade whose
+// spacing is 1, so the sum is rounded to an integer (nearest, ties to even),
+// and subtracting 1.5 * 2^23 back is exact. Two full-rate adds, and a zero
+// result is +0 (as an integer code converted to float is), never -0.
+__device__ __forceinline__ float round_int(float y) {
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  return __fsub_rn(__fadd_rn(y, kMagic), kMagic);
+}
+
 // The codes of this thread's values in a block of scale s, as integer-valued
 // floats: the nearest integer to RN(x / s) (ties to even), clamped to
 // [-127, 127]; all 0 when s is 0. See the file comment for the screening.
+// Every quotient here is below 255 in magnitude (a subnormal scale loses at
+// most half its value to rounding), well inside round_int's range.
 template <int kEPT>
 __device__ __forceinline__ void quant_group(const float (&x)[kEPT], float s, float (&c)[kEPT]) {
   if (s >= 0x1p-126f) {
     float y[kEPT], dev[kEPT];
     mul_each(y, x, __frcp_rn(s));
 #pragma unroll
-    for (int w = 0; w < kEPT; ++w) c[w] = rintf(y[w]);
+    for (int w = 0; w < kEPT; ++w) c[w] = round_int(y[w]);
     sub_each(dev, y, c);  // exact: y and its nearest integer are within a factor of 2 (or c = 0)
     float worst = 0.0f;
 #pragma unroll
     for (int w = 0; w < kEPT; ++w) worst = fmaxf(worst, fabsf(dev[w]));
     if (worst >= 0.5f - 0x1p-12f) {  // a quotient near a tie: the exact quotient decides
 #pragma unroll
-      for (int w = 0; w < kEPT; ++w) c[w] = rintf(__fdiv_rn(x[w], s));
+      for (int w = 0; w < kEPT; ++w) c[w] = round_int(__fdiv_rn(x[w], s));
     }
     // |x / s| < 127.5 for a normal s, so no clamp is needed here
   } else if (s > 0.0f) {  // a subnormal scale: exact quotients, clamped
 #pragma unroll
-    for (int w = 0; w < kEPT; ++w) c[w] = fminf(fmaxf(rintf(__fdiv_rn(x[w], s)), -127.0f), 127.0f);
+    for (int w = 0; w < kEPT; ++w) c[w] = fminf(fmaxf(round_int(__fdiv_rn(x[w], s)), -127.0f), 127.0f);
   } else {
 #pragma unroll
     for (int w = 0; w < kEPT; ++w) c[w] = 0.0f;
   }
-#pragma unroll
-  for (int w = 0; w < kEPT; ++w) c[w] = __fadd_rn(c[w], 0.0f);  // -0 -> +0
 }
 
 // Four integer-valued codes in [-127, 127] (c[i..i+3]) as four
