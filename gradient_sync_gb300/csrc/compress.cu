@@ -229,8 +229,13 @@ __device__ __forceinline__ uint32_t pack_codes4(const float (&c)[kEPT], int i) {
          ((uint32_t(int(c[i + 2])) & 0xFFu) << 16) | ((uint32_t(int(c[i + 3])) & 0xFFu) << 24);
 }
 
+// Code j (a two's-complement byte) of a word of four codes as a float, with
+// full-rate integer and add instructions: flipping the sign bit gives c + 128
+// in 0..255, placed as the low byte under the exponent of 2^23 it is the float
+// 2^23 + 128 + c exactly, and subtracting 2^23 + 128 leaves c exactly.
 __device__ __forceinline__ float code_of(uint32_t word, int j) {
-  return float(static_cast<int8_t>(static_cast<uint8_t>(word >> (8 * j))));
+  const uint32_t biased = __byte_perm(word ^ 0x80808080u, 0x4B000000u, 0x7540u | uint32_t(j));
+  return __fsub_rn(__uint_as_float(biased), 8388736.0f);  // 2^23 + 128
 }
 
 // ---------------------------------------------------------------- compress
