@@ -328,6 +328,12 @@ def ar_device_status(clear: bool = True) -> int:
     return _lib.load().ar_device_status(1 if clear else 0)
 
 
+def ar_plan_query(plan: Plan) -> int:
+    """The plan's sticky asynchronous status (AR_OK or AR_ETIMEOUT), read
+    without synchronising; see include/ar.h."""
+    return _lib.load().ar_plan_query(plan.handle)
+
+
 def ar_selftest_wait_timeout(polls: int = 1000, stream=None):
     """Run the bounded-wait self-test kernel (see include/ar.h)."""
     _check(_lib.load().ar_selftest_wait_timeout(int(polls), _stream(stream)), "ar_selftest_wait_timeout")

@@ -57,6 +57,7 @@ SIGNATURES = {
     "ar_compressed_allreduce": (c_int, [c_int, c_size_t, c_int, c_int, VOIDPP, VOIDPP, c_float, VOIDPP,
                                         c_void_p]),
     "ar_device_status": (c_int, [c_int]),
+    "ar_plan_query": (c_int, [c_void_p]),
     "ar_selftest_wait_timeout": (c_int, [ctypes.c_uint, c_void_p]),
     "ar_status_string": (ctypes.c_char_p, [c_int]),
     "ar_version": (c_int, []),

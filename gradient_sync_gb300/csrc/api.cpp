@@ -482,6 +482,20 @@ ar_status check_buffers(const ar_plan_t* p, void* const* bufs, void* const* outs
 
 ar_status from_cuda(cudaError_t e) { return e == cudaSuccess ? AR_OK : AR_ECUDA; }
 
+// Before an executing call enqueues anything: publish the current device's
+// host-visible status word (once per device) and refuse with AR_ETIMEOUT
+// while a bounded device-side wait that ran out is still recorded in it
+// (sticky until ar_device_status(1) clears it). Records the device on `p`.
+ar_status status_guard(const ar_plan_t* p, int* device = nullptr) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return AR_ECUDA;
+  volatile unsigned int* word = nullptr;
+  if (host_status_word(dev, &word) != cudaSuccess) return AR_ECUDA;
+  if (p != nullptr) p->last_device.v.store(dev, std::memory_order_relaxed);
+  if (device != nullptr) *device = dev;
+  return *word != 0 ? AR_ETIMEOUT : AR_OK;
+}
+
 // Segment count and tiles per segment of a fused launch over [e_lo, e_hi),
 // for tiles of `tile` elements whose segment bodies start and end on
 // multiples of W elements (the kernel's vector).
@@ -773,6 +787,8 @@ ar_status ar_execute(const ar_plan_t* plan, void* const* bufs, void* const* outs
   const ar_status s = check_buffers(plan, bufs, outs, workspace);
   if (s != AR_OK) return s;
   if (plan->desc.count == 0) return AR_OK;
+  const ar_status g = status_guard(plan);
+  if (g != AR_OK) return g;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (plan->desc.algo == AR_FUSED)
     return execute_fused(plan, bufs, outs, 0, int64_t(plan->desc.count), st);
@@ -819,9 +835,10 @@ ar_status ar_bind(const ar_plan_t* plan, void* const* bufs, void* const* outs, v
     *out = b;
     return AR_OK;
   }
-  if (cudaGetDevice(&b->device) != cudaSuccess) {
+  const ar_status g = status_guard(plan, &b->device);  // also publishes the word before any capture
+  if (g != AR_OK) {
     release(b);
-    return AR_ECUDA;
+    return g;
   }
   if (plan->desc.algo == AR_FUSED) {
     b->plan = *plan;
@@ -863,6 +880,9 @@ ar_status ar_execute_bound(const ar_bound_t* bound, void* stream) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return AR_ECUDA;
   if (dev != bound->device) return AR_EINVAL;
+  const volatile unsigned int* word = host_status_word_if_ready(dev);  // published by ar_bind
+  if (word == nullptr) return AR_ECUDA;
+  if (*word != 0) return AR_ETIMEOUT;
   if (bound->direct)
     return execute_fused(&bound->plan, bound->bufs.data(), bound->outs.empty() ? nullptr : bound->outs.data(), 0,
                          int64_t(bound->plan.desc.count), static_cast<cudaStream_t>(stream));
@@ -881,6 +901,8 @@ ar_status ar_execute_host(const ar_plan_t* plan, const void* const* host_in, voi
     if (host_in[r] == nullptr || host_out[r] == nullptr) return AR_EINVAL;
   const int64_t L = int64_t(plan->desc.count);
   if (L == 0) return AR_OK;
+  const ar_status g = status_guard(plan);
+  if (g != AR_OK) return g;
   const size_t es = esize(plan->desc.dtype);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   std::lock_guard<std::mutex> lock(g_host_mu);
@@ -1169,6 +1191,8 @@ ar_status ar_bucket_allreduce(int n_ranks, void* const* tensors, const size_t* c
       if (reinterpret_cast<uintptr_t>(tensors[size_t(r) * n_tensors + t]) % 32 != 0) v8 = false;
   const int64_t W = tma ? (dtype == AR_BF16 ? 8 : 4) : fused_vec_elems(dtype, v8);  // the kernel's vector
   if (tma && !tma_shape(N, stages, tile_bytes)) return AR_EUNSUPPORTED;
+  s = status_guard(nullptr);
+  if (s != AR_OK) return s;
   const int64_t tile = tma ? tile_bytes / int64_t(esize(dtype)) : fused_tile_elems(dtype, N, AR_ORDER_RING, AR_ALLREDUCE, v8);
   const int max_group = std::min(AR_MAX_BUCKET_TENSORS, kMaxBucketPtrs / N);
   static thread_local BucketFusedParams bp;
@@ -1352,8 +1376,18 @@ ar_status ar_device_status(int clear) {
   return v != 0 ? AR_ETIMEOUT : AR_OK;
 }
 
+ar_status ar_plan_query(const ar_plan_t* plan) {
+  if (plan == nullptr) return AR_EINVAL;
+  const volatile unsigned int* word = host_status_word_if_ready(plan->last_device.v.load(std::memory_order_relaxed));
+  return word != nullptr && *word != 0 ? AR_ETIMEOUT : AR_OK;
+}
+
 ar_status ar_selftest_wait_timeout(unsigned int polls, void* stream) {
   if (polls == 0) return AR_EINVAL;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return AR_ECUDA;
+  volatile unsigned int* word = nullptr;
+  if (host_status_word(dev, &word) != cudaSuccess) return AR_ECUDA;  // so that the timeout reaches the host copy
   return from_cuda(launch_wait_timeout(polls, static_cast<cudaStream_t>(stream)));
 }
 

@@ -3,9 +3,10 @@
 //
 // Every wait here is bounded: after `limit` unsuccessful polls (each poll may
 // suspend the thread for a while in hardware) it gives up, records the
-// timeout in the device status word and returns false. A kernel that sees a
-// failed wait raises its abort flag and winds down; the host reads the word
-// with ar_device_status.
+// timeout in the device status word (and in its host-visible copy) and
+// returns false. A kernel that sees a failed wait raises its abort flag and
+// winds down; the host reads the word with ar_device_status, or the copy with
+// ar_plan_query and before every execution.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -19,6 +20,11 @@ enum : unsigned int { kStatusTimeout = 1u };
 // The library's sticky per-device status word (read by ar_device_status).
 // Defined here: only one translation unit (fused_tma.cu) includes this file.
 __device__ unsigned int g_ar_status_word;
+
+// Host-visible copy of the status word: one word of page-locked, mapped host
+// memory per device, which the host reads without synchronising. Null until
+// the host has published it (the first executing call on the device).
+__device__ unsigned int* g_ar_status_host;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -67,6 +73,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
     if (*abort) return false;
   }
   atomicOr(&g_ar_status_word, kStatusTimeout);
+  if (unsigned int* h = g_ar_status_host) {
+    // Only one bit exists, so a plain store of it loses nothing to racing
+    // writers; the fence makes it visible to the host before the kernel ends.
+    *reinterpret_cast<volatile unsigned int*>(h) = kStatusTimeout;
+    __threadfence_system();
+  }
   *abort = 1;
   return false;
 }

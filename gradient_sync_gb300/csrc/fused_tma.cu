@@ -27,6 +27,8 @@
 // Every mbarrier wait is bounded (bulk.cuh); a timeout sets the library's
 // device status word, raises the CTA's abort flag, and the CTA winds down
 // after its outstanding copies.
+#include <atomic>
+
 #include "bulk.cuh"
 #include "common.cuh"
 
@@ -765,13 +767,70 @@ cudaError_t launch_wait_timeout(uint32_t polls, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+namespace {
+
+constexpr int kMaxStatusDevices = 64;
+// Per device ordinal: the host-visible status word, once published.
+std::atomic<unsigned int*> g_host_word[kMaxStatusDevices];
+std::mutex g_host_word_mu;
+
+}  // namespace
+
+volatile unsigned int* host_status_word_if_ready(int device) {
+  if (device < 0 || device >= kMaxStatusDevices) return nullptr;
+  return g_host_word[device].load(std::memory_order_acquire);
+}
+
+cudaError_t host_status_word(int device, volatile unsigned int** word) {
+  *word = host_status_word_if_ready(device);
+  if (*word != nullptr) return cudaSuccess;
+  if (device < 0 || device >= kMaxStatusDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_host_word_mu);
+  unsigned int* h = g_host_word[device].load(std::memory_order_acquire);
+  if (h == nullptr) {
+    // Relaxed capture mode for this thread: the one-time set-up may run while
+    // another thread captures a stream. The pointer goes to the device on a
+    // private non-blocking stream, which joins no capture.
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    cudaError_t err = cudaThreadExchangeStreamCaptureMode(&mode);
+    if (err != cudaSuccess) return err;
+    void* dptr = nullptr;
+    cudaStream_t s = nullptr;
+    err = cudaHostAlloc(reinterpret_cast<void**>(&h), sizeof(unsigned int),
+                        cudaHostAllocMapped | cudaHostAllocPortable);
+    if (err == cudaSuccess) {
+      *reinterpret_cast<volatile unsigned int*>(h) = 0;
+      err = cudaHostGetDevicePointer(&dptr, h, 0);
+    }
+    if (err == cudaSuccess) err = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+    if (err == cudaSuccess)
+      err = cudaMemcpyToSymbolAsync(g_ar_status_host, &dptr, sizeof(dptr), 0, cudaMemcpyHostToDevice, s);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(s);
+    if (s != nullptr) cudaStreamDestroy(s);
+    cudaThreadExchangeStreamCaptureMode(&mode);  // restore the caller's mode
+    if (err != cudaSuccess) {
+      if (h != nullptr) cudaFreeHost(h);
+      return err;
+    }
+    g_host_word[device].store(h, std::memory_order_release);
+  }
+  *word = h;
+  return cudaSuccess;
+}
+
 cudaError_t read_device_status(unsigned int* value, bool clear) {
   cudaError_t err = cudaDeviceSynchronize();
   if (err != cudaSuccess) return err;
   err = cudaMemcpyFromSymbol(value, g_ar_status_word, sizeof(unsigned int));
   if (err != cudaSuccess || !clear) return err;
   const unsigned int zero = 0;
-  return cudaMemcpyToSymbol(g_ar_status_word, &zero, sizeof(unsigned int));
+  err = cudaMemcpyToSymbol(g_ar_status_word, &zero, sizeof(unsigned int));
+  if (err != cudaSuccess) return err;
+  int dev = 0;
+  err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (volatile unsigned int* h = host_status_word_if_ready(dev)) *h = 0;
+  return cudaSuccess;
 }
 
 }  // namespace ar

@@ -2,6 +2,7 @@
 // launchers (*.cu). Not part of the public ABI.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <vector>
@@ -39,11 +40,29 @@ struct Step {
 
 }  // namespace ar
 
+namespace ar {
+
+// The device a plan last ran on (-1: never), written by the executing calls
+// and read by ar_plan_query, possibly from other threads. Copyable, so that
+// a plan can still be copied by value.
+struct DeviceTag {
+  std::atomic<int> v{-1};
+  DeviceTag() = default;
+  DeviceTag(const DeviceTag& o) : v(o.v.load(std::memory_order_relaxed)) {}
+  DeviceTag& operator=(const DeviceTag& o) {
+    v.store(o.v.load(std::memory_order_relaxed), std::memory_order_relaxed);
+    return *this;
+  }
+};
+
+}  // namespace ar
+
 struct ar_plan {
   ar_desc desc;
   std::vector<ar::Step> steps;  // empty for AR_FUSED
   ar_stats stats;
   int64_t ws_stride;  // fp32 elements per rank in the workspace (multiple of 64)
+  mutable ar::DeviceTag last_device;
 };
 
 namespace ar {
@@ -144,6 +163,13 @@ int64_t fused_tile_elems(ar_dtype dtype, int n, int order, int collective, bool 
 cudaError_t launch_bucket_fused(const BucketFusedParams& p, ar_dtype dtype, int sm_budget, bool v8, cudaStream_t stream);
 cudaError_t launch_pack(const PackParams& p, ar_dtype dtype, bool unpack, cudaStream_t stream);
 cudaError_t read_device_status(unsigned int* value, bool clear);
+// Host-visible copy of a device's status word (page-locked, mapped host
+// memory that the bounded waits also set). host_status_word publishes it on
+// first use (a one-time pinned host allocation, no device memory);
+// host_status_word_if_ready returns it only if already published, else null,
+// and makes no CUDA call.
+cudaError_t host_status_word(int device, volatile unsigned int** word);
+volatile unsigned int* host_status_word_if_ready(int device);
 // The bulk-copy variant of the fused all-reduce (fused_tma.cu).
 bool tma_shape(int n, int& stages, int& tile_bytes);
 cudaError_t launch_fused_tma(const FusedParams& p, ar_dtype dtype, int stages, int tile_bytes, int sm_budget,

@@ -28,7 +28,9 @@
  *    an error has enqueued nothing. AR_ECUDA reports a CUDA error at launch.
  *  - No call allocates device memory, and no call synchronises the device,
  *    except ar_execute_host (which waits for its own copies) and
- *    ar_device_status (which reads a status word).
+ *    ar_device_status (which reads a status word). The first executing call
+ *    on each device pins one 4-byte host word, the host-visible copy of the
+ *    device's status word (see "status" below); nothing else is allocated.
  *  - The library never reads environment variables.
  */
 #ifndef AR_GB300_H
@@ -218,7 +220,9 @@ ar_status ar_plan_desc(const ar_plan_t* plan, ar_desc* desc);
  *             when that size is 0. Its contents on entry do not matter.
  * Every rank ends with bitwise identical results. Errors (AR_EINVAL): NULL
  * plan or bufs; a NULL or misaligned buffer; overlapping buffers; workspace
- * NULL or misaligned when one is needed. count == 0 enqueues nothing. */
+ * NULL or misaligned when one is needed. count == 0 enqueues nothing.
+ * AR_ETIMEOUT, enqueuing nothing, while the current device's status word
+ * records a device-side wait that ran out (sticky: see ar_plan_query). */
 ar_status ar_execute(const ar_plan_t* plan, void* const* bufs, void* const* outs, void* workspace,
                      void* stream);
 
@@ -254,8 +258,9 @@ ar_status ar_execute_host(const ar_plan_t* plan, const void* const* host_in, voi
  * does, with the workspace taken from a fixed array of
  * AR_STATIC_WORKSPACE_BYTES bytes inside the library's device memory (every
  * GPU that loads the library holds that array until the process exits). It
- * calls no cudaMalloc, cudaFree or other allocating routine. The caller still
- * passes the input and output buffers.
+ * calls no cudaMalloc, cudaFree or other device-allocating routine (like
+ * every executing call, the first one on a device pins the 4-byte host status
+ * word). The caller still passes the input and output buffers.
  *
  * Limits and rules:
  *  - A plan whose ar_stats.workspace_bytes exceeds AR_STATIC_WORKSPACE_BYTES
@@ -476,11 +481,28 @@ ar_status ar_compressed_allreduce(int n_ranks, size_t count, int block, ar_dtype
 
 /* ---------------------------------------------------------------- status */
 
-/* Read (and clear, if clear != 0) the calling device's sticky status word,
- * set by a kernel whose bounded device-side wait ran out (the bulk-copy
- * all-reduce's mbarrier waits). Synchronises the device. Returns AR_OK or
- * AR_ETIMEOUT (or AR_ECUDA). */
+/* Every device-side wait in the library is bounded. One that runs out (for
+ * example an mbarrier wait of a bulk-copy kernel) sets the device's sticky
+ * status word, both in device memory and in a host-visible copy (page-locked
+ * mapped host memory). The error surfaces after the call that enqueued the
+ * work has returned, since initiation is non-blocking (Scaling ML Systems,
+ * "Collective communication"). From then on the executing calls
+ * (ar_execute, ar_execute_host, ar_execute_noalloc, ar_bind,
+ * ar_execute_bound, ar_bucket_allreduce) on that device return AR_ETIMEOUT
+ * and enqueue nothing, until ar_device_status(1) clears the word. */
+
+/* Read (and clear, if clear != 0) the calling device's sticky status word.
+ * Synchronises the device. Returns AR_OK or AR_ETIMEOUT (or AR_ECUDA). */
 ar_status ar_device_status(int clear);
+
+/* The plan's asynchronous error, without synchronising and without any CUDA
+ * call: AR_ETIMEOUT if the host-visible status word of the device that last
+ * executed `plan` (ar_execute, ar_execute_host, ar_execute_noalloc or
+ * ar_bind) records a wait that ran out, else AR_OK (also for a plan never
+ * executed). A kernel still running has not reported yet: after the stream
+ * has drained, the answer covers all of the plan's work. Does not clear the
+ * word. AR_EINVAL if plan is NULL. */
+ar_status ar_plan_query(const ar_plan_t* plan);
 
 /* Failure-path self-test: launches one thread that waits, with a bound of
  * `polls` polls, on an mbarrier that nothing will ever complete. The wait gives

@@ -375,3 +375,14 @@ def test_bind_validates_without_touching_the_device(g):
     del b
     with pytest.raises(g.ArError):
         g._check(g._lib.load().ar_execute_bound(None, None), "ar_execute_bound")
+
+
+def test_plan_query_makes_no_device_call(g):
+    # A plan that never ran reports nothing, without any CUDA call (there is
+    # no GPU here); an empty execution does not count as running.
+    plan = g.ar_plan(4, 1024, "f32", "ring")
+    assert g.ar_plan_query(plan) == g.AR_OK
+    empty = g.ar_plan(4, 0, "f32", "fused")
+    g.ar_execute(empty, [0x100000 * (r + 1) for r in range(4)], stream=0)
+    assert g.ar_plan_query(empty) == g.AR_OK
+    assert g._lib.load().ar_plan_query(None) == g.AR_EINVAL
