@@ -20,7 +20,10 @@
 //  compress_kernel              g, e -> codes, scales, e'   (the message of every rank)
 //  compressed_reduce_kernel     codes, scales -> out        (the receiving side)
 //  compressed_allreduce_kernel  g, e -> e', out             (both in one pass; no message
-//                                                            is materialised)
+//                                                            is materialised; bf16 without
+//                                                            feedback: the register-
+//                                                            pipelined
+//                                                            compressed_allreduce_bf16_kernel)
 //
 // Tiling: a CTA of 256 threads takes a tile of 256 * E consecutive elements,
 // the same tile of every rank, E per thread (thread t: elements E*t..E*t+E-1;
@@ -104,6 +107,23 @@ __device__ __forceinline__ void load_group(const void* base, int64_t e, int64_t 
         f[w] = BF16 ? bf16_to_f32(static_cast<const uint16_t*>(base)[e + w]) : static_cast<const float*>(base)[e + w];
     }
   }
+}
+
+// Eight bf16 values starting at e (a multiple of 8) as four raw words, two
+// values per word, low half first; values at or past `lim` read as +0.
+__device__ __forceinline__ uint4 load_bf16x8_raw(const void* base, int64_t e, int64_t lim) {
+  const uint16_t* b = static_cast<const uint16_t*>(base);
+  if (e + 8 <= lim) return __ldcs(reinterpret_cast<const uint4*>(b + e));
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (e + i < lim) w[i / 2] |= uint32_t(b[e + i]) << (16 * (i & 1));
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ void widen_bf16x8(const uint4 w, float (&f)[8]) {
+  f[0] = bf16lo(w.x); f[1] = bf16hi(w.x); f[2] = bf16lo(w.y); f[3] = bf16hi(w.y);
+  f[4] = bf16lo(w.z); f[5] = bf16hi(w.z); f[6] = bf16lo(w.w); f[7] = bf16hi(w.w);
 }
 
 // Store kEPT consecutive elements at e (bf16: rounded to nearest even);
@@ -370,6 +390,79 @@ __global__ void __launch_bounds__(kThreads) compressed_reduce_kernel(const __gri
 }
 
 // ---------------------------------------------------------------- fused
+// One rank's step of the fused pass for this thread's values x: quantise the
+// block, add the reconstruction d to the running sum (acc = d for rank 0)
+// and, with error feedback, return the residual x - d.
+template <int kEPT, bool EF>
+__device__ __forceinline__ void fold_rank(const float (&x)[kEPT], int r, int block, float* wmax, float (&acc)[kEPT],
+                                          float (&res)[kEPT]) {
+  float c[kEPT], d[kEPT];
+  const float s = block_scale<kEPT>(x, block, wmax);
+  quant_group<kEPT>(x, s, c);
+  mul_each(d, c, s);
+  if (r == 0) {
+#pragma unroll
+    for (int w = 0; w < kEPT; ++w) acc[w] = d[w];
+  } else {
+    add_each(acc, acc, d);
+  }
+  if (EF) sub_each(res, x, d);
+}
+
+// bf16 without error feedback moves only 2 bytes in and 2 out per element
+// and rank, so a thread that loads one rank and then quantises it has little
+// in flight. Here every thread keeps the raw words of the next kAhead
+// (tile, rank) pairs of its visiting order in flight while it works on the
+// current one (tiles blockIdx.x, + gridDim.x, ...; ranks 0..n-1 within each).
+// Measured on GB300 at 16 ranks x 96 Mi bf16, block 128: 0.615 of its bytes
+// with 2 ahead, 0.611 with 1, 0.595 with 3, 0.586 with 4, against 0.54 for
+// the load-then-quantise loop. A bulk L2 prefetch of the tiles ahead, one
+// thread per CTA, reached 0.596 here and cost 7-25 % on the paths that
+// already have enough in flight (fp32, error feedback), so it is not used.
+constexpr int kAhead = 2;
+
+__global__ void __launch_bounds__(kThreads) compressed_allreduce_bf16_kernel(const __grid_constant__ CompressParams p) {
+  constexpr int kEPT = 8;
+  constexpr int kTileElems = kEPT * kThreads;
+  __shared__ float wmax[2][kWarps];
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int64_t n_tiles = (p.count + kTileElems - 1) / kTileElems;
+  const int64_t lane_off = int64_t(kEPT) * threadIdx.x;
+  // The pair k positions ahead of (tile, r), loaded into w (+0 past the end).
+  auto fetch = [&](int64_t tile, int r, int k, uint4& w) {
+    r += k;
+    while (r >= p.n) {
+      r -= p.n;
+      tile += gridDim.x;
+    }
+    w = tile < n_tiles ? load_bf16x8_raw(p.g[r], tile * kTileElems + lane_off, p.count) : make_uint4(0u, 0u, 0u, 0u);
+  };
+  uint4 ring[kAhead];
+#pragma unroll
+  for (int k = 0; k < kAhead; ++k) fetch(blockIdx.x, 0, k, ring[k]);
+  int phase = 0;
+  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const int64_t e = tile * kTileElems + lane_off;
+    float acc[kEPT];
+#pragma unroll 1
+    for (int r = 0; r < p.n; ++r) {
+      const uint4 w = ring[0];
+#pragma unroll
+      for (int k = 0; k + 1 < kAhead; ++k) ring[k] = ring[k + 1];
+      fetch(tile, r, kAhead, ring[kAhead - 1]);
+      float x[kEPT], res[kEPT];
+      widen_bf16x8(w, x);
+      fold_rank<kEPT, false>(x, r, p.block, wmax[phase], acc, res);
+      phase ^= 1;
+    }
+    if (e >= p.count) continue;
+    mul_each(acc, acc, p.scale);
+#pragma unroll 1
+    for (int r = 0; r < p.n; ++r) store_group<true, kEPT>(p.out[r], e, p.count, acc);
+  }
+}
+
 // Each tile, ranks in order: quantise rank r's block, add its reconstruction
 // to the running sum and store its residual; then write the scaled sum to
 // every rank. No message leaves the registers.
@@ -377,10 +470,10 @@ template <bool BF16, bool EF>
 __global__ void __launch_bounds__(kThreads) compressed_allreduce_kernel(const __grid_constant__ CompressParams p) {
   constexpr int kEPT = ept<BF16>();
   constexpr int kTileElems = kEPT * kThreads;
-  // Ranks per load batch. bf16 takes one: fewer registers, more resident warps
-  // (measured at 16 x 96 Mi: 0.97 of its bytes with error feedback against
-  // 0.81 with two, 0.51 without against 0.43 with four). fp32 keeps 2 / 4 (one
-  // or two measured 0-3 % slower).
+  // Ranks per load batch. bf16 (with error feedback here; without, the
+  // pipelined kernel above runs) takes one: fewer registers, more resident
+  // warps (measured at 16 x 96 Mi: 0.97 of its bytes against 0.81 with two).
+  // fp32 keeps 2 / 4 (one or two measured 0-3 % slower).
   constexpr int NB = BF16 ? 1 : (EF ? 2 : 4);
   __shared__ float wmax[2][kWarps];
   grid_dependency_wait();
@@ -403,25 +496,14 @@ __global__ void __launch_bounds__(kThreads) compressed_allreduce_kernel(const __
       for (int b = 0; b < NB; ++b) {
         const int r = r0 + b;
         if (r >= p.n) continue;  // uniform across the CTA
-        float x[kEPT], c[kEPT];
+        float x[kEPT], res[kEPT];
         if (EF)
           add_each(x, xg[b], xe[b]);
         else
 #pragma unroll
           for (int w = 0; w < kEPT; ++w) x[w] = xg[b][w];
-        const float s = block_scale<kEPT>(x, p.block, wmax[phase]);
+        fold_rank<kEPT, EF>(x, r, p.block, wmax[phase], acc, res);
         phase ^= 1;
-        quant_group<kEPT>(x, s, c);
-        float d[kEPT];
-        mul_each(d, c, s);
-        if (r == 0) {
-#pragma unroll
-          for (int w = 0; w < kEPT; ++w) acc[w] = d[w];
-        } else {
-          add_each(acc, acc, d);
-        }
-        float res[kEPT];
-        if (EF) sub_each(res, x, d);
         if (EF && e < p.count) store_group<false, kEPT>(p.e[r], e, p.count, res);
       }
     }
@@ -469,7 +551,7 @@ cudaError_t launch_compressed_reduce(const CompressParams& p, ar_dtype out_dtype
 
 cudaError_t launch_compressed_allreduce(const CompressParams& p, ar_dtype dtype, cudaStream_t stream) {
   const bool bf = dtype == AR_BF16;
-  const Kern k = bf ? (p.ef ? compressed_allreduce_kernel<true, true> : compressed_allreduce_kernel<true, false>)
+  const Kern k = bf ? (p.ef ? compressed_allreduce_kernel<true, true> : compressed_allreduce_bf16_kernel)
                     : (p.ef ? compressed_allreduce_kernel<false, true> : compressed_allreduce_kernel<false, false>);
   return launch(k, n_tiles(p.count, bf ? ept<true>() : ept<false>()), p, stream);
 }
