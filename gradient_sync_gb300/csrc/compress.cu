@@ -16,14 +16,15 @@
 // to nearest even, never contracted, so the results are bit-identical to the
 // step-by-step definition.
 //
-// Three kernels:
+// Kernels:
 //  compress_kernel              g, e -> codes, scales, e'   (the message of every rank)
+//  compress_pipe_kernel         g -> codes, scales          (the same without feedback)
 //  compressed_reduce_kernel     codes, scales -> out        (the receiving side)
 //  compressed_allreduce_kernel  g, e -> e', out             (both in one pass; no message
-//                                                            is materialised; bf16 without
-//                                                            feedback: the register-
-//                                                            pipelined
-//                                                            compressed_allreduce_bf16_kernel)
+//                                                            is materialised)
+//  compressed_allreduce_bf16_kernel  g -> out               (the same, bf16 without feedback)
+// The two kernels without feedback keep the loads of the ranks ahead in
+// flight (pipelined loads, below).
 //
 // Tiling: a CTA of 256 threads takes a tile of 256 * E consecutive elements,
 // the same tile of every rank, E per thread (thread t: elements E*t..E*t+E-1;
@@ -70,6 +71,12 @@ __host__ __device__ constexpr int ept() { return BF16 ? 8 : 4; }
 // The fused pass keeps 8 (16 measured 0.75 against 0.81).
 template <bool BF16>
 __host__ __device__ constexpr int compress_ept() { return BF16 ? 16 : 4; }
+// The compressor without error feedback (pipelined loads) takes 8 elements
+// per thread of either type. Measured at 16 ranks x 192 MiB, block 128, two
+// calls: bf16 0.621 of its bytes (0.615 with 16 per thread), fp32 0.874
+// (0.674 with 4), against 0.513 and 0.729 without the pipeline.
+template <bool BF16>
+__host__ __device__ constexpr int compress_pipe_ept() { return 8; }
 // The reducer reads codes, not gradients: 8 (bf16 out) or 4 (fp32 out) per thread.
 template <bool BF16>
 __host__ __device__ constexpr int reduce_ept() { return BF16 ? 8 : 4; }
@@ -109,21 +116,56 @@ __device__ __forceinline__ void load_group(const void* base, int64_t e, int64_t 
   }
 }
 
-// Eight bf16 values starting at e (a multiple of 8) as four raw words, two
-// values per word, low half first; values at or past `lim` read as +0.
-__device__ __forceinline__ uint4 load_bf16x8_raw(const void* base, int64_t e, int64_t lim) {
-  const uint16_t* b = static_cast<const uint16_t*>(base);
-  if (e + 8 <= lim) return __ldcs(reinterpret_cast<const uint4*>(b + e));
-  uint32_t w[4] = {0u, 0u, 0u, 0u};
+// kEPT consecutive elements starting at e (a multiple of kEPT) as raw words
+// (bf16: two values per word, low half first); elements at or past `lim`
+// read as +0. Loaded by the pipelined kernels ahead of use and widened only
+// when used.
+template <bool BF16, int kEPT>
+struct RawGroup {
+  static constexpr int kWords = BF16 ? kEPT / 2 : kEPT;
+  static_assert(kWords % 4 == 0, "whole 16-byte vectors");
+  uint4 v[kWords / 4];
+};
+
+template <bool BF16, int kEPT>
+__device__ __forceinline__ void load_raw(const void* base, int64_t e, int64_t lim, RawGroup<BF16, kEPT>& g) {
+  constexpr int kVecs = RawGroup<BF16, kEPT>::kWords / 4;
+  const uint4* q = reinterpret_cast<const uint4*>(static_cast<const char*>(base) + e * (BF16 ? 2 : 4));
+  if (e + kEPT <= lim) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    if (e + i < lim) w[i / 2] |= uint32_t(b[e + i]) << (16 * (i & 1));
-  return make_uint4(w[0], w[1], w[2], w[3]);
+    for (int i = 0; i < kVecs; ++i) g.v[i] = __ldcs(q + i);
+    return;
+  }
+  uint32_t u[4 * kVecs];
+#pragma unroll
+  for (int i = 0; i < 4 * kVecs; ++i) u[i] = 0u;
+#pragma unroll
+  for (int i = 0; i < kEPT; ++i) {
+    if (e + i >= lim) continue;
+    if (BF16)
+      u[i / 2] |= uint32_t(static_cast<const uint16_t*>(base)[e + i]) << (16 * (i & 1));
+    else
+      u[i] = static_cast<const uint32_t*>(base)[e + i];
+  }
+#pragma unroll
+  for (int i = 0; i < kVecs; ++i) g.v[i] = make_uint4(u[4 * i], u[4 * i + 1], u[4 * i + 2], u[4 * i + 3]);
 }
 
-__device__ __forceinline__ void widen_bf16x8(const uint4 w, float (&f)[8]) {
-  f[0] = bf16lo(w.x); f[1] = bf16hi(w.x); f[2] = bf16lo(w.y); f[3] = bf16hi(w.y);
-  f[4] = bf16lo(w.z); f[5] = bf16hi(w.z); f[6] = bf16lo(w.w); f[7] = bf16hi(w.w);
+template <bool BF16, int kEPT>
+__device__ __forceinline__ void widen_raw(const RawGroup<BF16, kEPT>& g, float (&f)[kEPT]) {
+#pragma unroll
+  for (int i = 0; i < RawGroup<BF16, kEPT>::kWords / 4; ++i) {
+    const uint32_t u[4] = {g.v[i].x, g.v[i].y, g.v[i].z, g.v[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (BF16) {
+        f[8 * i + 2 * j] = bf16lo(u[j]);
+        f[8 * i + 2 * j + 1] = bf16hi(u[j]);
+      } else {
+        f[4 * i + j] = __uint_as_float(u[j]);
+      }
+    }
+  }
 }
 
 // Store kEPT consecutive elements at e (bf16: rounded to nearest even);
@@ -258,7 +300,58 @@ __device__ __forceinline__ float code_of(uint32_t word, int j) {
   return __fsub_rn(__uint_as_float(biased), 8388736.0f);  // 2^23 + 128
 }
 
+// ---------------------------------------------------------------- pipelined loads
+// Without error feedback a rank's slice is only 2 or 4 bytes per element, so
+// a thread that loads one rank and then works on it has little in flight.
+// The pipelined kernels keep the raw words of the next kAhead (tile, rank)
+// pairs in flight while they work on the current one. A CTA visits the pairs
+// in a fixed order: tiles blockIdx.x, + gridDim.x, ...; ranks 0..n-1 within
+// each tile. Measured on GB300 at 16 ranks x 96 Mi bf16, block 128 (fused
+// pass): 0.615 of its bytes with 2 ahead, 0.611 with 1, 0.595 with 3, 0.586
+// with 4, against 0.54 for the load-then-quantise loop. A bulk L2 prefetch of
+// the tiles ahead, one thread per CTA, reached 0.596 there and cost 7-25 % on
+// the paths that already have enough in flight (fp32, error feedback), so it
+// is not used.
+constexpr int kAhead = 2;
+
+// Load the gradient words of the pair k positions after (tile, r) into w
+// (+0 past the last tile).
+template <bool BF16, int kEPT>
+__device__ __forceinline__ void fetch_ahead(const CompressParams& p, int64_t n_tiles, int64_t lane_off, int64_t tile,
+                                            int r, int k, RawGroup<BF16, kEPT>& w) {
+  constexpr int64_t kTileElems = int64_t(kEPT) * kThreads;
+  r += k;
+  while (r >= p.n) {
+    r -= p.n;
+    tile += gridDim.x;
+  }
+  if (tile < n_tiles) {
+    load_raw<BF16, kEPT>(p.g[r], tile * kTileElems + lane_off, p.count, w);
+  } else {
+#pragma unroll
+    for (int i = 0; i < RawGroup<BF16, kEPT>::kWords / 4; ++i) w.v[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 // ---------------------------------------------------------------- compress
+// kEPT codes at e, one byte each; codes at or past `count` are not written.
+template <int kEPT>
+__device__ __forceinline__ void store_codes(int8_t* q, int64_t e, int64_t count, const float (&c)[kEPT]) {
+  if (e + kEPT <= count) {
+    if constexpr (kEPT == 16)
+      __stcs(reinterpret_cast<uint4*>(q + e), make_uint4(pack_codes4<kEPT>(c, 0), pack_codes4<kEPT>(c, 4),
+                                                         pack_codes4<kEPT>(c, 8), pack_codes4<kEPT>(c, 12)));
+    else if constexpr (kEPT == 8)
+      __stcs(reinterpret_cast<uint2*>(q + e), make_uint2(pack_codes4<kEPT>(c, 0), pack_codes4<kEPT>(c, 4)));
+    else
+      __stcs(reinterpret_cast<unsigned int*>(q + e), pack_codes4<kEPT>(c, 0));
+  } else {
+#pragma unroll
+    for (int w = 0; w < kEPT; ++w)
+      if (e + w < count) q[e + w] = static_cast<int8_t>(int(c[w]));
+  }
+}
+
 // Each tile of every rank: codes (kEPT bytes per thread), the scale of each block
 // (written by the block's first thread) and, with error feedback, the new
 // residual.
@@ -266,7 +359,7 @@ template <bool BF16, bool EF>
 __global__ void __launch_bounds__(kThreads) compress_kernel(const __grid_constant__ CompressParams p) {
   constexpr int kEPT = compress_ept<BF16>();
   constexpr int kTileElems = kEPT * kThreads;
-  constexpr int NB = BF16 ? (EF ? 1 : 2) : 4;  // ranks per load batch (fp32: 1 or 2 measured slower)
+  constexpr int NB = BF16 ? 1 : 4;  // ranks per load batch (fp32: 1 or 2 measured slower)
   __shared__ float wmax[2][kWarps];
   grid_dependency_wait();
   grid_dependents_launch();
@@ -299,20 +392,7 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const __grid_constan
         if (e >= p.count) continue;
         if ((e & (p.block - 1)) == 0) p.s[r][e >> shift] = s;
         quant_group<kEPT>(x, s, c);
-        int8_t* q = p.q[r];
-        if (e + kEPT <= p.count) {
-          if constexpr (kEPT == 16)
-            __stcs(reinterpret_cast<uint4*>(q + e), make_uint4(pack_codes4<kEPT>(c, 0), pack_codes4<kEPT>(c, 4),
-                                                               pack_codes4<kEPT>(c, 8), pack_codes4<kEPT>(c, 12)));
-          else if constexpr (kEPT == 8)
-            __stcs(reinterpret_cast<uint2*>(q + e), make_uint2(pack_codes4<kEPT>(c, 0), pack_codes4<kEPT>(c, 4)));
-          else
-            __stcs(reinterpret_cast<unsigned int*>(q + e), pack_codes4<kEPT>(c, 0));
-        } else {
-#pragma unroll
-          for (int w = 0; w < kEPT; ++w)
-            if (e + w < p.count) q[e + w] = static_cast<int8_t>(int(c[w]));
-        }
+        store_codes<kEPT>(p.q[r], e, p.count, c);
         if (EF) {
           float d[kEPT], res[kEPT];
           mul_each(d, c, s);
@@ -320,6 +400,45 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const __grid_constan
           store_group<false, kEPT>(p.e[r], e, p.count, res);
         }
       }
+    }
+  }
+}
+
+// The compressor without error feedback, with the pipelined loads: the
+// message (codes and scales) of every rank from its gradients alone. (With
+// feedback the pipeline measured +1 % on fp32 and -1 % on bf16 at 16 ranks x
+// 192 MiB, so the batch compressor above serves that case.)
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads) compress_pipe_kernel(const __grid_constant__ CompressParams p) {
+  constexpr int kEPT = compress_pipe_ept<BF16>();
+  constexpr int kTileElems = kEPT * kThreads;
+  using Raw = RawGroup<BF16, kEPT>;
+  __shared__ float wmax[2][kWarps];
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int64_t n_tiles = (p.count + kTileElems - 1) / kTileElems;
+  const int64_t lane_off = int64_t(kEPT) * threadIdx.x;
+  const int shift = __ffs(p.block) - 1;  // block is a power of two
+  Raw ring[kAhead];
+#pragma unroll
+  for (int k = 0; k < kAhead; ++k) fetch_ahead<BF16, kEPT>(p, n_tiles, lane_off, blockIdx.x, 0, k, ring[k]);
+  int phase = 0;
+  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const int64_t e = tile * kTileElems + lane_off;
+#pragma unroll 1
+    for (int r = 0; r < p.n; ++r) {
+      const Raw w = ring[0];
+#pragma unroll
+      for (int k = 0; k + 1 < kAhead; ++k) ring[k] = ring[k + 1];
+      fetch_ahead<BF16, kEPT>(p, n_tiles, lane_off, tile, r, kAhead, ring[kAhead - 1]);
+      float x[kEPT], c[kEPT];
+      widen_raw<BF16, kEPT>(w, x);
+      const float s = block_scale<kEPT>(x, p.block, wmax[phase]);
+      phase ^= 1;
+      if (e >= p.count) continue;  // after the block maximum, which every thread joins
+      if ((e & (p.block - 1)) == 0) p.s[r][e >> shift] = s;
+      quant_group<kEPT>(x, s, c);
+      store_codes<kEPT>(p.q[r], e, p.count, c);
     }
   }
 }
@@ -409,17 +528,8 @@ __device__ __forceinline__ void fold_rank(const float (&x)[kEPT], int r, int blo
   if (EF) sub_each(res, x, d);
 }
 
-// bf16 without error feedback moves only 2 bytes in and 2 out per element
-// and rank, so a thread that loads one rank and then quantises it has little
-// in flight. Here every thread keeps the raw words of the next kAhead
-// (tile, rank) pairs of its visiting order in flight while it works on the
-// current one (tiles blockIdx.x, + gridDim.x, ...; ranks 0..n-1 within each).
-// Measured on GB300 at 16 ranks x 96 Mi bf16, block 128: 0.615 of its bytes
-// with 2 ahead, 0.611 with 1, 0.595 with 3, 0.586 with 4, against 0.54 for
-// the load-then-quantise loop. A bulk L2 prefetch of the tiles ahead, one
-// thread per CTA, reached 0.596 here and cost 7-25 % on the paths that
-// already have enough in flight (fp32, error feedback), so it is not used.
-constexpr int kAhead = 2;
+// bf16 without error feedback: 2 bytes in and 2 out per element and rank,
+// with the pipelined loads above.
 
 __global__ void __launch_bounds__(kThreads) compressed_allreduce_bf16_kernel(const __grid_constant__ CompressParams p) {
   constexpr int kEPT = 8;
@@ -429,16 +539,9 @@ __global__ void __launch_bounds__(kThreads) compressed_allreduce_bf16_kernel(con
   grid_dependents_launch();
   const int64_t n_tiles = (p.count + kTileElems - 1) / kTileElems;
   const int64_t lane_off = int64_t(kEPT) * threadIdx.x;
-  // The pair k positions ahead of (tile, r), loaded into w (+0 past the end).
-  auto fetch = [&](int64_t tile, int r, int k, uint4& w) {
-    r += k;
-    while (r >= p.n) {
-      r -= p.n;
-      tile += gridDim.x;
-    }
-    w = tile < n_tiles ? load_bf16x8_raw(p.g[r], tile * kTileElems + lane_off, p.count) : make_uint4(0u, 0u, 0u, 0u);
-  };
-  uint4 ring[kAhead];
+  using Raw = RawGroup<true, kEPT>;
+  auto fetch = [&](int64_t tile, int r, int k, Raw& w) { fetch_ahead<true, kEPT>(p, n_tiles, lane_off, tile, r, k, w); };
+  Raw ring[kAhead];
 #pragma unroll
   for (int k = 0; k < kAhead; ++k) fetch(blockIdx.x, 0, k, ring[k]);
   int phase = 0;
@@ -447,12 +550,12 @@ __global__ void __launch_bounds__(kThreads) compressed_allreduce_bf16_kernel(con
     float acc[kEPT];
 #pragma unroll 1
     for (int r = 0; r < p.n; ++r) {
-      const uint4 w = ring[0];
+      const Raw w = ring[0];
 #pragma unroll
       for (int k = 0; k + 1 < kAhead; ++k) ring[k] = ring[k + 1];
       fetch(tile, r, kAhead, ring[kAhead - 1]);
       float x[kEPT], res[kEPT];
-      widen_bf16x8(w, x);
+      widen_raw<true, kEPT>(w, x);
       fold_rank<kEPT, false>(x, r, p.block, wmax[phase], acc, res);
       phase ^= 1;
     }
@@ -539,9 +642,11 @@ int64_t n_tiles(int64_t count, int elems_per_thread) {
 
 cudaError_t launch_compress(const CompressParams& p, ar_dtype dtype, cudaStream_t stream) {
   const bool bf = dtype == AR_BF16;
-  const Kern k = bf ? (p.ef ? compress_kernel<true, true> : compress_kernel<true, false>)
-                    : (p.ef ? compress_kernel<false, true> : compress_kernel<false, false>);
-  return launch(k, n_tiles(p.count, bf ? compress_ept<true>() : compress_ept<false>()), p, stream);
+  const Kern k = bf ? (p.ef ? compress_kernel<true, true> : compress_pipe_kernel<true>)
+                    : (p.ef ? compress_kernel<false, true> : compress_pipe_kernel<false>);
+  const int ept = p.ef ? (bf ? compress_ept<true>() : compress_ept<false>())
+                       : (bf ? compress_pipe_ept<true>() : compress_pipe_ept<false>());
+  return launch(k, n_tiles(p.count, ept), p, stream);
 }
 
 cudaError_t launch_compressed_reduce(const CompressParams& p, ar_dtype out_dtype, cudaStream_t stream) {
