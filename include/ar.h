@@ -244,8 +244,8 @@ ar_status ar_execute_host(const ar_plan_t* plan, const void* const* host_in, voi
  * ar_execute_noalloc. */
 #define AR_STATIC_WORKSPACE_BYTES (64u << 20)
 
-/* ar_execute for callers that cannot allocate device memory. The paper has no
- * counterpart to this call.
+/* ar_execute for callers that cannot allocate device memory. None of the
+ * source pages describes such a call.
  *
  * Who needs it: callers whose device memory is owned by another allocator (a
  * framework's caching pool, or a fixed budget handed out by a host
