@@ -204,14 +204,27 @@ __device__ __forceinline__ void store_group(void* base, int64_t e, int64_t count
 // one barrier per call suffices (a warp that writes the next call's slot has
 // passed this call's barrier, after every warp finished reading the slot of
 // the call before).
-template <int kEPT>
+// The maximum over the block's lanes of one warp is a butterfly of shuffles,
+// or with kRedux one warp reduction: m is a non-negative float (fmaxf drops
+// NaN), and non-negative floats order as their bit patterns do, so an
+// unsigned maximum of the bits is the float maximum; each group of lanes of
+// one block reduces under its own mask. Measured at 16 ranks x 192 MiB: the
+// reduction lifts the pipelined kernels without feedback (bf16 fused pass
+// 0.61 -> 0.63) and slows the kernels with feedback (bf16 fused pass 0.97 ->
+// 0.85), so only the former use it.
+template <int kEPT, bool kRedux = false>
 __device__ __forceinline__ float block_scale(const float (&x)[kEPT], int block, float* wmax) {
   float m = 0.0f;
 #pragma unroll
   for (int w = 0; w < kEPT; ++w) m = fmaxf(m, fabsf(x[w]));
   constexpr int kWarpElems = 32 * kEPT;
   const int lanes = block < kWarpElems ? block / kEPT : 32;
-  for (int o = lanes >> 1; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  if (kRedux) {
+    const unsigned mask = lanes == 32 ? kFull : ((1u << lanes) - 1u) << ((threadIdx.x & 31) & ~(lanes - 1));
+    m = __uint_as_float(__reduce_max_sync(mask, __float_as_uint(m)));
+  } else {
+    for (int o = lanes >> 1; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  }
   if (block > kWarpElems) {
     const int warp = threadIdx.x >> 5;
     if ((threadIdx.x & 31) == 0) wmax[warp] = m;
@@ -433,7 +446,7 @@ __global__ void __launch_bounds__(kThreads) compress_pipe_kernel(const __grid_co
       fetch_ahead<BF16, kEPT>(p, n_tiles, lane_off, tile, r, kAhead, ring[kAhead - 1]);
       float x[kEPT], c[kEPT];
       widen_raw<BF16, kEPT>(w, x);
-      const float s = block_scale<kEPT>(x, p.block, wmax[phase]);
+      const float s = block_scale<kEPT, true>(x, p.block, wmax[phase]);
       phase ^= 1;
       if (e >= p.count) continue;  // after the block maximum, which every thread joins
       if ((e & (p.block - 1)) == 0) p.s[r][e >> shift] = s;
@@ -512,11 +525,11 @@ __global__ void __launch_bounds__(kThreads) compressed_reduce_kernel(const __gri
 // One rank's step of the fused pass for this thread's values x: quantise the
 // block, add the reconstruction d to the running sum (acc = d for rank 0)
 // and, with error feedback, return the residual x - d.
-template <int kEPT, bool EF>
+template <int kEPT, bool EF, bool kRedux = false>
 __device__ __forceinline__ void fold_rank(const float (&x)[kEPT], int r, int block, float* wmax, float (&acc)[kEPT],
                                           float (&res)[kEPT]) {
   float c[kEPT], d[kEPT];
-  const float s = block_scale<kEPT>(x, block, wmax);
+  const float s = block_scale<kEPT, kRedux>(x, block, wmax);
   quant_group<kEPT>(x, s, c);
   mul_each(d, c, s);
   if (r == 0) {
@@ -556,7 +569,7 @@ __global__ void __launch_bounds__(kThreads) compressed_allreduce_bf16_kernel(con
       fetch(tile, r, kAhead, ring[kAhead - 1]);
       float x[kEPT], res[kEPT];
       widen_raw<true, kEPT>(w, x);
-      fold_rank<kEPT, false>(x, r, p.block, wmax[phase], acc, res);
+      fold_rank<kEPT, false, true>(x, r, p.block, wmax[phase], acc, res);
       phase ^= 1;
     }
     if (e >= p.count) continue;
