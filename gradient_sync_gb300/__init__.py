@@ -339,6 +339,14 @@ def ar_selftest_wait_timeout(polls: int = 1000, stream=None):
     _check(_lib.load().ar_selftest_wait_timeout(int(polls), _stream(stream)), "ar_selftest_wait_timeout")
 
 
+def ar_selftest_scale_quotient() -> int:
+    """Mismatches of the division-free block scale against the IEEE division
+    over every non-negative float (see include/ar.h)."""
+    n = ctypes.c_ulonglong(0)
+    _check(_lib.load().ar_selftest_scale_quotient(ctypes.byref(n)), "ar_selftest_scale_quotient")
+    return n.value
+
+
 def ar_status_string(status: int) -> str:
     return _lib.load().ar_status_string(int(status)).decode()
 

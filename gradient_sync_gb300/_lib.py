@@ -59,6 +59,7 @@ SIGNATURES = {
     "ar_device_status": (c_int, [c_int]),
     "ar_plan_query": (c_int, [c_void_p]),
     "ar_selftest_wait_timeout": (c_int, [ctypes.c_uint, c_void_p]),
+    "ar_selftest_scale_quotient": (c_int, [ctypes.POINTER(ctypes.c_ulonglong)]),
     "ar_status_string": (ctypes.c_char_p, [c_int]),
     "ar_version": (c_int, []),
 }

@@ -1391,6 +1391,11 @@ ar_status ar_selftest_wait_timeout(unsigned int polls, void* stream) {
   return from_cuda(launch_wait_timeout(polls, static_cast<cudaStream_t>(stream)));
 }
 
+ar_status ar_selftest_scale_quotient(unsigned long long* mismatches) {
+  if (mismatches == nullptr) return AR_EINVAL;
+  return from_cuda(selftest_div127(mismatches));
+}
+
 const char* ar_status_string(ar_status status) {
   switch (status) {
     case AR_OK: return "AR_OK: success";

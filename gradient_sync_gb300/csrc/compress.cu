@@ -40,12 +40,32 @@
 // maximum) and are never stored.
 //
 // The code of an element is decided without a division in the common case:
-// with a normal scale s, y = x * RN(1/s) lies within 2^-15 of the correctly
-// rounded quotient RN(x / s) (|x / s| <= 127 + 2^-16, two roundings of
-// relative size 2^-24 each). When every y of a thread is farther than 2^-12
-// from a half-integer, rint(y) equals rint(RN(x / s)); otherwise (rarely: a
-// quotient near a tie) the thread takes the correctly rounded quotient
-// __fdiv_rn(x, s) itself, so ties are decided exactly as the definition says.
+// with a normal scale s, y = RN(x * r), with r = RN(1/s), or in the lean
+// variant below the hardware's approximate reciprocal (at most one ulp off,
+// 2^-23 relative), lies within 2^-15 of the correctly rounded quotient
+// RN(x / s): |x / s| <= 127 + 2^-16, so |y - x / s| <= 127.01 * (2^-23 +
+// 2^-24) < 2^-15.4 and |RN(x / s) - x / s| <= 2^-18. When every y of a thread
+// is farther than 2^-12 from a half-integer, rint(y) equals rint(RN(x / s));
+// otherwise (rarely: a quotient near a tie) the thread takes the correctly
+// rounded quotient __fdiv_rn(x, s) itself, so ties are decided exactly as the
+// definition says.
+//
+// The lean variant (kLean), for the kernels bound by instruction issue (the
+// two without error feedback), spends fewer instructions per block and rank
+// for the same results:
+//  - the block maximum is one warp reduction instead of shuffle rounds;
+//  - the scale s = RN(m / 127) is computed without a division: q0 = RN(m * c)
+//    with c = RN(1/127) is within an ulp of the quotient, the remainder
+//    m - q0 * 127 is exact in one FMA, and a second FMA, q0 + remainder * c,
+//    rounds to the correctly rounded quotient (Markstein's theorem for
+//    FMA-based division with a correctly rounded reciprocal); the library's
+//    self-test checks it against the IEEE division for every non-negative
+//    float;
+//  - the screening product uses the approximate reciprocal.
+// Measured at 16 ranks x 192 MiB, block 128 (fractions of each path's bytes):
+// bf16 without feedback 0.61 -> 0.68 fused and 0.62 -> 0.66 in two calls;
+// the kernels with feedback and the fp32 fused pass measured the same or up
+// to 12 % slower with it, so they keep the IEEE operations and the shuffles.
 // Codes are kept as integer-valued floats; a zero code is +0 (as an integer
 // code converted to float is).
 #include "common.cuh"
@@ -199,27 +219,43 @@ __device__ __forceinline__ void store_group(void* base, int64_t e, int64_t count
   }
 }
 
+// RN(m / 127) without a division (the lean variant; see the file comment);
+// +inf and NaN pass through as the division would give them.
+__device__ __forceinline__ float div127(float m) {
+  constexpr float kInv127 = 1.0f / 127.0f;  // RN(1/127) = 0x1.020408p-7
+  static_assert(kInv127 == 0x1.020408p-7f, "correctly rounded reciprocal of 127");
+  const float q0 = __fmul_rn(m, kInv127);
+  const float rem = __fmaf_rn(-q0, 127.0f, m);  // exact
+  const float q1 = __fmaf_rn(rem, kInv127, q0);
+  return q0 < __int_as_float(0x7f800000) ? q1 : q0;
+}
+
+// The hardware's approximate reciprocal (at most one ulp off); s is normal
+// here, so neither s nor 1/s is subnormal.
+__device__ __forceinline__ float rcp_approx(float s) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+  return r;
+}
+
 // The block's scale s = max|x| / 127 for this thread's kEPT values.
 // `wmax` is this call's shared-memory slot; callers alternate two slots, so
 // one barrier per call suffices (a warp that writes the next call's slot has
 // passed this call's barrier, after every warp finished reading the slot of
 // the call before).
 // The maximum over the block's lanes of one warp is a butterfly of shuffles,
-// or with kRedux one warp reduction: m is a non-negative float (fmaxf drops
+// or with kLean one warp reduction: m is a non-negative float (fmaxf drops
 // NaN), and non-negative floats order as their bit patterns do, so an
 // unsigned maximum of the bits is the float maximum; each group of lanes of
-// one block reduces under its own mask. Measured at 16 ranks x 192 MiB: the
-// reduction lifts the pipelined kernels without feedback (bf16 fused pass
-// 0.61 -> 0.63) and slows the kernels with feedback (bf16 fused pass 0.97 ->
-// 0.85), so only the former use it.
-template <int kEPT, bool kRedux = false>
+// one block reduces under its own mask.
+template <int kEPT, bool kLean = false>
 __device__ __forceinline__ float block_scale(const float (&x)[kEPT], int block, float* wmax) {
   float m = 0.0f;
 #pragma unroll
   for (int w = 0; w < kEPT; ++w) m = fmaxf(m, fabsf(x[w]));
   constexpr int kWarpElems = 32 * kEPT;
   const int lanes = block < kWarpElems ? block / kEPT : 32;
-  if (kRedux) {
+  if (kLean) {
     const unsigned mask = lanes == 32 ? kFull : ((1u << lanes) - 1u) << ((threadIdx.x & 31) & ~(lanes - 1));
     m = __uint_as_float(__reduce_max_sync(mask, __float_as_uint(m)));
   } else {
@@ -234,7 +270,7 @@ __device__ __forceinline__ float block_scale(const float (&x)[kEPT], int block, 
     m = wmax[w0];
     for (int i = 1; i < W; ++i) m = fmaxf(m, wmax[w0 + i]);
   }
-  return __fdiv_rn(m, 127.0f);
+  return kLean ? div127(m) : __fdiv_rn(m, 127.0f);
 }
 
 // Element-wise fp32 arithmetic, one IEEE operation per element rounded to
@@ -271,11 +307,11 @@ __device__ __forceinline__ float round_int(float y) {
 // [-127, 127]; all 0 when s is 0. See the file comment for the screening.
 // Every quotient here is below 255 in magnitude (a subnormal scale loses at
 // most half its value to rounding), well inside round_int's range.
-template <int kEPT>
+template <int kEPT, bool kLean = false>
 __device__ __forceinline__ void quant_group(const float (&x)[kEPT], float s, float (&c)[kEPT]) {
   if (s >= 0x1p-126f) {
     float y[kEPT], dev[kEPT];
-    mul_each(y, x, __frcp_rn(s));
+    mul_each(y, x, kLean ? rcp_approx(s) : __frcp_rn(s));
 #pragma unroll
     for (int w = 0; w < kEPT; ++w) c[w] = round_int(y[w]);
     sub_each(dev, y, c);  // exact: y and its nearest integer are within a factor of 2 (or c = 0)
@@ -450,7 +486,7 @@ __global__ void __launch_bounds__(kThreads) compress_pipe_kernel(const __grid_co
       phase ^= 1;
       if (e >= p.count) continue;  // after the block maximum, which every thread joins
       if ((e & (p.block - 1)) == 0) p.s[r][e >> shift] = s;
-      quant_group<kEPT>(x, s, c);
+      quant_group<kEPT, true>(x, s, c);
       store_codes<kEPT>(p.q[r], e, p.count, c);
     }
   }
@@ -525,12 +561,12 @@ __global__ void __launch_bounds__(kThreads) compressed_reduce_kernel(const __gri
 // One rank's step of the fused pass for this thread's values x: quantise the
 // block, add the reconstruction d to the running sum (acc = d for rank 0)
 // and, with error feedback, return the residual x - d.
-template <int kEPT, bool EF, bool kRedux = false>
+template <int kEPT, bool EF, bool kLean = false>
 __device__ __forceinline__ void fold_rank(const float (&x)[kEPT], int r, int block, float* wmax, float (&acc)[kEPT],
                                           float (&res)[kEPT]) {
   float c[kEPT], d[kEPT];
-  const float s = block_scale<kEPT, kRedux>(x, block, wmax);
-  quant_group<kEPT>(x, s, c);
+  const float s = block_scale<kEPT, kLean>(x, block, wmax);
+  quant_group<kEPT, kLean>(x, s, c);
   mul_each(d, c, s);
   if (r == 0) {
 #pragma unroll
@@ -630,6 +666,23 @@ __global__ void __launch_bounds__(kThreads) compressed_allreduce_kernel(const __
   }
 }
 
+// The self-test of div127: every non-negative float bit pattern (finite,
+// +inf and NaN) against the IEEE division; the mismatches are counted.
+__device__ unsigned long long g_div127_mismatches;
+
+__global__ void div127_selftest_kernel() {
+  unsigned long long bad = 0;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < 0x80000000u; u += stride) {
+    const float m = __uint_as_float(u);
+    const float want = __fdiv_rn(m, 127.0f);
+    const float got = div127(m);
+    const bool both_nan = want != want && got != got;
+    if (!both_nan && __float_as_uint(want) != __float_as_uint(got)) ++bad;
+  }
+  if (bad != 0) atomicAdd(&g_div127_mismatches, bad);
+}
+
 using Kern = void (*)(CompressParams);
 
 cudaError_t launch(Kern k, int64_t tiles, const CompressParams& p, cudaStream_t stream) {
@@ -672,6 +725,18 @@ cudaError_t launch_compressed_allreduce(const CompressParams& p, ar_dtype dtype,
   const Kern k = bf ? (p.ef ? compressed_allreduce_kernel<true, true> : compressed_allreduce_bf16_kernel)
                     : (p.ef ? compressed_allreduce_kernel<false, true> : compressed_allreduce_kernel<false, false>);
   return launch(k, n_tiles(p.count, bf ? ept<true>() : ept<false>()), p, stream);
+}
+
+cudaError_t selftest_div127(unsigned long long* mismatches) {
+  const unsigned long long zero = 0;
+  cudaError_t err = cudaMemcpyToSymbol(g_div127_mismatches, &zero, sizeof(zero));
+  if (err != cudaSuccess) return err;
+  div127_selftest_kernel<<<1216, 256>>>();
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  err = cudaDeviceSynchronize();
+  if (err != cudaSuccess) return err;
+  return cudaMemcpyFromSymbol(mismatches, g_div127_mismatches, sizeof(*mismatches));
 }
 
 }  // namespace ar

@@ -184,5 +184,8 @@ cudaError_t launch_allgather_bulk(const FusedParams& p, ar_dtype dtype, int sm_b
 cudaError_t launch_compress(const CompressParams& p, ar_dtype dtype, cudaStream_t stream);
 cudaError_t launch_compressed_reduce(const CompressParams& p, ar_dtype out_dtype, cudaStream_t stream);
 cudaError_t launch_compressed_allreduce(const CompressParams& p, ar_dtype dtype, cudaStream_t stream);
+// Self-test of the division-free block scale against the IEEE division, over
+// every non-negative float (synchronises the device).
+cudaError_t selftest_div127(unsigned long long* mismatches);
 
 }  // namespace ar

@@ -511,6 +511,17 @@ ar_status ar_plan_query(const ar_plan_t* plan);
  * that the bulk-copy kernels use, without any fault and without a hang. */
 ar_status ar_selftest_wait_timeout(unsigned int polls, void* stream);
 
+/* Self-test of the compression's block scale (Scaling ML Systems, "Blockwise
+ * quantization": the scale is max|x| / 127, here an fp32 quotient rounded to
+ * nearest). The kernels compute it without a division, by a product with the
+ * rounded reciprocal of 127 and an FMA correction. This call compares that
+ * computation with the IEEE division for every non-negative float bit pattern
+ * (2^31 of them: zero, subnormals, normals, +inf and NaNs, where both give a
+ * NaN) on the current device, and writes the number of differing results to
+ * *mismatches (0 when the method is exact). Synchronises the device.
+ * AR_EINVAL if mismatches is NULL; AR_ECUDA on a CUDA error. */
+ar_status ar_selftest_scale_quotient(unsigned long long* mismatches);
+
 /* Human-readable name of a status code (static string). */
 const char* ar_status_string(ar_status status);
 

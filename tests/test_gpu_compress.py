@@ -321,3 +321,11 @@ def test_compressed_allreduce_full_size(g):
         assert torch.equal(res_b[r].view(torch.int32), res[r].view(torch.int32)), r
     del grads, res, res_b, outs, outs_b, codes, scales
     torch.cuda.empty_cache()
+
+
+def test_division_free_scale_equals_the_ieee_quotient_for_every_float(g):
+    """The kernels compute the block scale max|x| / 127 without a division;
+    over every non-negative float bit pattern it must equal the IEEE
+    division's result (NaN for NaN)."""
+    assert g.ar_selftest_scale_quotient() == 0
+
