@@ -443,6 +443,18 @@ void compute_stats(ar_plan_t* p) {
   st.bytes_sent_per_rank = N > 0 ? *std::max_element(sent.begin(), sent.end()) : 0;
   const bool uses_ws = d.dtype == AR_BF16 && N > 1 && d.collective != AR_ALLGATHER;
   st.workspace_bytes = uses_ws ? size_t(N) * size_t(p->ws_stride) * 4 : 0;
+  // Tiny steps: the whole schedule in one CTA when its table fits (room kept
+  // for the all-gather's first copy of every rank's own chunk, L elements).
+  int64_t n_x = 0, step_elems = L;
+  for (const Step& s : p->steps) {
+    n_x += int64_t(s.xfers.size());
+    int64_t e = 0;
+    for (const Transfer& t : s.xfers) e += t.hi - t.lo;
+    step_elems = std::max(step_elems, e);
+  }
+  p->small = N > 1 && L > 0 && step_elems <= kSmallStepElems && n_x + N <= kMaxSmallXfers &&
+             int64_t(p->steps.size()) + 1 <= kMaxSmallSteps;
+  if (p->small) st.launches = 1;
 }
 
 ar_status check_ptr(const void* ptr) {
@@ -595,27 +607,65 @@ ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs
     sp.tile_start[1] = int32_t(std::max<int64_t>(1, (body + kStepTile - 1) / kStepTile));
     return from_cuda(launch_step(sp, d.dtype, OP_FINISH, sp.tile_start[1], false, d.sm_budget, v8, stream));
   }
+  // out of place all-gather: every rank's own chunk is copied to its output
+  // first (the ring delivers only the other N-1 chunks)
+  Step own{OP_COPY, {}};
   if (d.collective == AR_ALLGATHER && outs != nullptr) {
-    // out of place: every rank's own chunk is copied to its output first (the
-    // ring delivers only the other N-1 chunks)
-    Step own{OP_COPY, {}};
     const auto b = cuts(0, int64_t(d.count), N);
     for (int r = 0; r < N; ++r)
       if (outs[r] != bufs[r]) add_xfer(own, r, r, b[r], b[r + 1], RAW, RES, RES, false);
-    if (!own.xfers.empty()) {
-      sp.n_xfer = int(own.xfers.size());
-      int tiles = 0;
-      for (int x = 0; x < sp.n_xfer; ++x) {
-        const Transfer& t = own.xfers[size_t(x)];
-        sp.x[x] = t;
-        sp.tile_start[x] = tiles;
-        const int64_t body = std::max<int64_t>(rdown(t.hi, kStepVec) - rup(t.lo, kStepVec), 0);
-        tiles += int(std::max<int64_t>(1, (body + kStepTile - 1) / kStepTile));
+  }
+  if (p->small) {  // the whole schedule in one CTA (step.cu)
+    static thread_local SmallParams q;  // ~28 KB, reused between calls
+    std::memset(&q, 0, sizeof(q));
+    std::memcpy(q.raw, sp.raw, sizeof(q.raw));
+    std::memcpy(q.res, sp.res, sizeof(q.res));
+    q.ws = sp.ws;
+    q.ws_stride = sp.ws_stride;
+    q.scale = sp.scale;
+    int nx = 0, ns = 0;
+    auto add = [&](const Step& st) {
+      q.step_start[ns] = nx;
+      q.step_op[ns] = uint8_t(st.op);
+      int32_t flat = 0;
+      for (const Transfer& t : st.xfers) {
+        SmallXfer& y = q.x[nx++];
+        y.src = t.src;
+        y.dst = t.dst;
+        y.src2 = t.src2;
+        y.xs = t.xs;
+        y.ys = t.ys;
+        y.ds = t.ds;
+        y.x2s = t.x2s;
+        y.fin = t.fin;
+        y.pair = t.pair;
+        y.lo = int32_t(t.lo);
+        y.len = int32_t(t.hi - t.lo);
+        y.flat = flat;
+        flat += y.len;
       }
-      sp.tile_start[sp.n_xfer] = tiles;
-      const ar_status s = from_cuda(launch_step(sp, d.dtype, OP_COPY, tiles, true, d.sm_budget, v8, stream));
-      if (s != AR_OK) return s;
+      q.step_elems[ns] = flat;
+      ++ns;
+    };
+    if (!own.xfers.empty()) add(own);
+    for (const Step& st : p->steps) add(st);
+    q.step_start[ns] = nx;
+    q.n_steps = ns;
+    return from_cuda(launch_small_steps(q, d.dtype, stream));
+  }
+  if (!own.xfers.empty()) {
+    sp.n_xfer = int(own.xfers.size());
+    int tiles = 0;
+    for (int x = 0; x < sp.n_xfer; ++x) {
+      const Transfer& t = own.xfers[size_t(x)];
+      sp.x[x] = t;
+      sp.tile_start[x] = tiles;
+      const int64_t body = std::max<int64_t>(rdown(t.hi, kStepVec) - rup(t.lo, kStepVec), 0);
+      tiles += int(std::max<int64_t>(1, (body + kStepTile - 1) / kStepTile));
     }
+    sp.tile_start[sp.n_xfer] = tiles;
+    const ar_status s = from_cuda(launch_step(sp, d.dtype, OP_COPY, tiles, true, d.sm_budget, v8, stream));
+    if (s != AR_OK) return s;
   }
   for (const Step& st : p->steps) {
     // a step's transfers are independent (none writes what another reads), so

@@ -62,6 +62,7 @@ struct ar_plan {
   std::vector<ar::Step> steps;  // empty for AR_FUSED
   ar_stats stats;
   int64_t ws_stride;  // fp32 elements per rank in the workspace (multiple of 64)
+  bool small = false; // step plan run whole in one CTA (one launch)
   mutable ar::DeviceTag last_device;
 };
 
@@ -96,6 +97,40 @@ struct FusedParams {
   int64_t tiles_per_seg;
   float scale;
 };
+
+// The whole schedule of a small step plan in one CTA (step.cu): every step's
+// transfers in one table, element ranges below 2^31.
+struct SmallXfer {
+  int16_t src, dst, src2;
+  uint8_t xs, ys, ds, x2s, fin, pair;
+  int32_t lo, len;  // element range [lo, lo + len) of the ranks' buffers
+  int32_t flat;     // elements of the step's earlier transfers
+};
+
+constexpr int kMaxSmallXfers = 1024;
+constexpr int kMaxSmallSteps = 256;
+// A step plan runs in one CTA when its table fits and no step moves more
+// than kSmallStepElems elements (two per thread of the CTA). Measured on
+// GB300, 16 ranks, bound calls: ring at 256 / 1024 elements per rank 32.8 /
+// 38.9 us against 49 us one kernel per step; Rabenseifner at 256 (2048
+// elements in its first step) 12.3 us against about 15. At 4096 elements per
+// step and more the one-CTA path was slower (ring at 4096 per rank: 98 us
+// against about 50), so those plans keep one kernel per step.
+constexpr int64_t kSmallStepElems = 2048;
+
+struct SmallParams {
+  void* raw[AR_MAX_RANKS];
+  void* res[AR_MAX_RANKS];
+  float* ws;
+  int64_t ws_stride;
+  float scale;
+  int n_steps;
+  int32_t step_start[kMaxSmallSteps + 1];  // first transfer of each step in x[]
+  int32_t step_elems[kMaxSmallSteps];      // elements of each step, all transfers
+  uint8_t step_op[kMaxSmallSteps];         // StepOp of each step
+  SmallXfer x[kMaxSmallXfers];
+};
+static_assert(sizeof(SmallParams) <= 32764, "kernel parameter limit");
 
 constexpr int kMaxBucketPtrs = 256;  // n_ranks * tensors per launch
 constexpr int kMaxBucketSegs = 96;
@@ -156,6 +191,8 @@ constexpr int kPackTile = kThreads * 8;                   // 2048 elements
 cudaError_t launch_step(const StepParams& p, ar_dtype dtype, StepOp op, int total_tiles, bool pdl,
                         int sm_budget, bool v8, cudaStream_t stream);
 cudaError_t launch_fused(const FusedParams& p, ar_dtype dtype, int sm_budget, cudaStream_t stream);
+// All steps of a small plan in one CTA, a block barrier between steps.
+cudaError_t launch_small_steps(const SmallParams& p, ar_dtype dtype, cudaStream_t stream);
 // Register pipeline: elements per vector (v8: 32-byte vectors, bucket kernel
 // only, N > 4 and every pointer 32-byte aligned) and per tile.
 int fused_vec_elems(ar_dtype dtype, bool v8);

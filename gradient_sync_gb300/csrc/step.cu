@@ -264,6 +264,89 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
   }
 }
 
+// ---------------------------------------------------------------- small plans
+// A plan whose buffers are a few KiB spends its time on the step boundaries:
+// a kernel boundary costs about 1.6 us, the data of a step a fraction of that.
+// Here one CTA runs every step of the schedule, with a block barrier as the
+// step boundary: a step's stores are visible to every thread of the block
+// after the barrier, and no CTA waits on another. Each thread takes the
+// step's elements kSmallThreads apart, finds each element's transfer by a
+// binary search over the step's prefix counts, and applies exactly the step
+// kernel's per-element operations (x + y, + x2, times the scale, rounded to
+// the destination type), so the results are the same bits.
+template <bool BF16>
+__device__ __forceinline__ Operand small_operand(const SmallParams& p, int space, int rank) {
+  if (space == RAW) return {static_cast<char*>(p.raw[rank]), !BF16};
+  if (space == RES) return {static_cast<char*>(p.res[rank]), !BF16};
+  if (BF16) return {reinterpret_cast<char*>(p.ws + int64_t(rank) * p.ws_stride), true};
+  return {static_cast<char*>(p.res[rank]), true};
+}
+
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallBatch = 4;  // elements per thread with their loads in flight together
+
+template <bool BF16>
+__global__ void __launch_bounds__(kSmallThreads) small_steps_kernel(const __grid_constant__ SmallParams p) {
+  grid_dependency_wait();
+  grid_dependents_launch();
+  for (int s = 0; s < p.n_steps; ++s) {
+    const int x0 = p.step_start[s], x1 = p.step_start[s + 1];
+    const int total = p.step_elems[s];
+    const int op = p.step_op[s];
+    for (int f0 = threadIdx.x; f0 < total; f0 += kSmallThreads * kSmallBatch) {
+      int xi[kSmallBatch];
+      int64_t e[kSmallBatch];
+      float v[kSmallBatch];
+      uint32_t bits[kSmallBatch];
+#pragma unroll
+      for (int u = 0; u < kSmallBatch; ++u) {
+        const int f = f0 + u * kSmallThreads;
+        xi[u] = -1;
+        if (f >= total) continue;
+        int lo = x0, hi = x1;  // the last transfer whose first flat index is <= f
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (p.x[mid].flat <= f)
+            lo = mid;
+          else
+            hi = mid;
+        }
+        xi[u] = lo;
+        const SmallXfer& t = p.x[lo];
+        e[u] = int64_t(t.lo) + (f - t.flat);
+        const Operand X = small_operand<BF16>(p, t.xs, t.src);
+        if (op == OP_COPY) {  // same type on both sides: move the bits
+          bits[u] = X.f32 ? reinterpret_cast<const uint32_t*>(X.base)[e[u]]
+                          : uint32_t(reinterpret_cast<const uint16_t*>(X.base)[e[u]]);
+          continue;
+        }
+        v[u] = load1(X, e[u]);
+        if (op == OP_ADD) {
+          v[u] = fadd(v[u], load1(small_operand<BF16>(p, t.ys, t.dst), e[u]));
+          if (t.src2 >= 0) v[u] = fadd(v[u], load1(small_operand<BF16>(p, t.x2s, t.src2), e[u]));
+        }
+        if (t.fin) v[u] = fmul(v[u], p.scale);
+      }
+#pragma unroll
+      for (int u = 0; u < kSmallBatch; ++u) {
+        if (xi[u] < 0) continue;
+        const SmallXfer& t = p.x[xi[u]];
+        const Operand D = small_operand<BF16>(p, t.ds, t.dst);
+        if (op == OP_COPY) {
+          if (D.f32)
+            reinterpret_cast<uint32_t*>(D.base)[e[u]] = bits[u];
+          else
+            reinterpret_cast<uint16_t*>(D.base)[e[u]] = uint16_t(bits[u]);
+          continue;
+        }
+        store1(D, e[u], v[u]);
+        if (op == OP_ADD && t.pair) store1(small_operand<BF16>(p, t.ds, t.src), e[u], v[u]);
+      }
+    }
+    __syncthreads();  // the step boundary
+  }
+}
+
 template <bool BF16, bool V8>
 cudaError_t launch_op(const StepParams& p, StepOp op, int tiles, bool pdl, int sm_budget, cudaStream_t stream) {
   void (*k)(StepParams) = op == OP_ADD ? step_kernel<BF16, OP_ADD, V8>
@@ -283,6 +366,20 @@ cudaError_t launch_op(const StepParams& p, StepOp op, int tiles, bool pdl, int s
 }
 
 }  // namespace
+
+cudaError_t launch_small_steps(const SmallParams& p, ar_dtype dtype, cudaStream_t stream) {
+  void (*k)(SmallParams) = dtype == AR_BF16 ? small_steps_kernel<true> : small_steps_kernel<false>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(kSmallThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, p);
+}
 
 cudaError_t launch_step(const StepParams& p, ar_dtype dtype, StepOp op, int total_tiles, bool pdl,
                         int sm_budget, bool v8, cudaStream_t stream) {

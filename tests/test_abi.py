@@ -386,3 +386,17 @@ def test_plan_query_makes_no_device_call(g):
     g.ar_execute(empty, [0x100000 * (r + 1) for r in range(4)], stream=0)
     assert g.ar_plan_query(empty) == g.AR_OK
     assert g._lib.load().ar_plan_query(None) == g.AR_EINVAL
+
+
+def test_small_step_plans_are_one_launch(g):
+    # a step plan whose every step moves at most 2048 elements runs the whole
+    # schedule in one CTA: one launch, the same steps and bytes
+    for algo, N, G, small_L in (("ring", 16, 0, 2048), ("rabenseifner", 16, 0, 256), ("hier", 8, 4, 1024),
+                                ("recdoubling", 4, 0, 1024)):
+        small = g.ar_plan(N, small_L, "f32", algo, group_size=G).stats
+        big = g.ar_plan(N, small_L + 1, "f32", algo, group_size=G).stats
+        assert small["launches"] == 1 and big["launches"] == big["steps"] >= small["steps"] > 0, algo
+        assert small["hbm_bytes"] < big["hbm_bytes"]
+    assert g.ar_plan(16, 2048, "bf16", "ring").stats["launches"] == 1
+    assert g.ar_plan(64, 20, "f32", "ring").stats["launches"] == 126  # 126 x 64 transfers: too many for one table
+    assert g.ar_plan(1, 100, "f32", "ring").stats["launches"] == 0

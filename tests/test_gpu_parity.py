@@ -357,3 +357,26 @@ def test_mixed_in_and_out_of_place(g, dtype, algo, order):
         assert_bits_equal(to_host(outs[r], dtype), want, f"rank {r}")
         if r % 2:
             np.testing.assert_array_equal(to_host(devs[r], dtype), x[r])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("algo,N,G,dims", [("ring", 16, 0, None), ("rabenseifner", 8, 0, None), ("hier", 8, 4, None),
+                                           ("recdoubling", 4, 0, None), ("dbtree", 6, 0, None),
+                                           ("torus", 8, 0, (2, 4))])
+def test_one_cta_and_per_step_executors_agree(g, algo, N, G, dims, dtype):
+    """Plans whose steps move at most 2048 elements run every step in one CTA
+    with a block barrier per step; larger ones run one kernel per step. Both
+    give the oracle's bits, in place and out of place, around the boundary."""
+    for L in (5, 256, 257, 777, 1024, 1025, 2048, 2049, 8193):
+        x = workloads.all_ranks(workloads.small_spec(N, L, dtype, "normal", seed=L + N))
+        want = expected(algo, "ring", x, dtype, group_size=G, scale=0.5, torus_dims=dims)
+        plan = g.ar_plan(N, L, dtype, algo, group_size=G, scale=0.5, torus_dims=dims or (0, 0, 0))
+        assert plan.stats["launches"] in (1, plan.stats["steps"])
+        for out_of_place in (False, True):
+            bufs = [to_device(x[r], dtype) for r in range(N)]
+            outs = [torch.empty_like(b) for b in bufs] if out_of_place else None
+            g.ar_execute(plan, bufs, outs=outs, workspace=g.workspace_for(plan))
+            torch.cuda.synchronize()
+            for r in range(N):
+                got = to_host((outs if out_of_place else bufs)[r], dtype)
+                assert_bits_equal(got, want, f"{algo} L={L} rank {r} {'out' if out_of_place else 'in'}")
