@@ -1047,8 +1047,9 @@ ar_status ar_plan_predict(const ar_plan_t* plan, const ar_fabric* f, double* sec
   const ar_desc& d = plan->desc;
   const ar_stats& st = plan->stats;
   const int N = d.n_ranks, rps = f->ranks_per_server;
-  if (f->shared_memory) {  // one memory for all ranks: each launch, then all its bytes
-    *seconds = st.launches * f->alpha + double(st.hbm_bytes) / f->bw_local;
+  if (f->shared_memory) {  // one memory for all ranks: each launch, the in-CTA steps, then all its bytes
+    const double cta_steps = plan->small ? double(st.steps) * AR_DEVICE_CTA_STEP_S : 0.0;
+    *seconds = st.launches * f->alpha + cta_steps + double(st.hbm_bytes) / f->bw_local;
     return AR_OK;
   }
   if (d.algo == AR_FUSED) {

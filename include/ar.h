@@ -101,6 +101,12 @@ typedef enum {
  * resolves to AR_FUSED. */
 #define AR_DEVICE_ALPHA_S 1.5e-6 /* per dependent kernel launch, graph-replayed */
 #define AR_DEVICE_BW 6.0e12      /* bytes/s of algorithmic HBM traffic */
+#define AR_DEVICE_CTA_STEP_S 1.0e-6 /* per step of a plan run whole in one CTA
+                                       (ar_stats.launches == 1 with more than
+                                       one step): a block barrier and the
+                                       step's memory round trip, measured on
+                                       GB300 (16-rank ring at 1 KiB: 32.8 us
+                                       for 30 steps) */
 
 /* Per-element summation order of AR_FUSED. (For AR_REDUCE_SCATTER,
  * AR_ORDER_RING is the order of its ring, which folds chunk c from rank c+1:
@@ -328,8 +334,11 @@ typedef struct {
                             sends its buffer once and receives the result once
                             (primer §4.4) */
   int shared_memory;     /* 1: all ranks share one memory of bandwidth bw_local
-                            (virtual ranks on one GPU): a step costs alpha plus
-                            its algorithmic memory bytes / bw_local */
+                            (virtual ranks on one GPU): every kernel launch of
+                            the plan costs alpha, every step of a plan run
+                            whole in one CTA AR_DEVICE_CTA_STEP_S, and the
+                            plan's algorithmic memory bytes cost
+                            bytes / bw_local */
 } ar_fabric;
 
 /* Predicted seconds of one ar_execute of `plan` on `fabric`. Transfer bytes

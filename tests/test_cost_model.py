@@ -120,6 +120,24 @@ def test_device_model_is_launches_plus_bytes(g):
             st["launches"] * g.AR_DEVICE_ALPHA_S + st["hbm_bytes"] / g.AR_DEVICE_BW, rel=1e-12)
 
 
+def test_device_model_of_one_cta_plans(g):
+    # a plan run whole in one CTA: one launch, then a block-barrier step each
+    dev = g.fabric(g.AR_DEVICE_ALPHA_S, g.AR_DEVICE_BW, shared_memory=True)
+    for algo, L in (("ring", 256), ("rabenseifner", 256)):
+        p = g.ar_plan(16, L, "f32", algo)
+        st = p.stats
+        assert st["launches"] == 1 and st["steps"] > 1
+        assert g.ar_plan_predict(p, dev) == pytest.approx(
+            g.AR_DEVICE_ALPHA_S + st["steps"] * g.AR_DEVICE_CTA_STEP_S + st["hbm_bytes"] / g.AR_DEVICE_BW, rel=1e-12)
+    # measured on GB300, bound: ring 32.8 us, Rabenseifner 12.3 us (within the
+    # ~3 us of launch and host time the model leaves out)
+    ring = g.ar_plan_predict(g.ar_plan(16, 256, "f32", "ring"), dev)
+    rab = g.ar_plan_predict(g.ar_plan(16, 256, "f32", "rabenseifner"), dev)
+    assert 28e-6 < ring < 34e-6 and 8e-6 < rab < 12.5e-6
+    # still the single pass for AR_AUTO at any size
+    assert g.ar_select(16, 256, dev)[0] == "fused"
+
+
 def test_auto_resolves_to_the_single_pass(g):
     for N, order in ((16, "ring"), (8, "tree"), (5, "rank")):
         p = g.ar_plan(N, 12345, "f32", "auto", order=order)
