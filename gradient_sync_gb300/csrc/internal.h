@@ -111,8 +111,8 @@ constexpr int kMaxSmallXfers = 1024;
 constexpr int kMaxSmallSteps = 256;
 // A step plan runs in one CTA when its table fits and no step moves more
 // than kSmallStepElems elements (two per thread of the CTA). Measured on
-// GB300, 16 ranks, bound calls: ring at 256 / 1024 elements per rank 32.8 /
-// 38.9 us against 49 us one kernel per step; Rabenseifner at 256 (2048
+// GB300, 16 ranks, bound calls: ring at 256 / 1024 elements per rank 30.7 /
+// 36.9 us against 49 us one kernel per step; Rabenseifner at 256 (2048
 // elements in its first step) 12.3 us against about 15. At 4096 elements per
 // step and more the one-CTA path was slower (ring at 4096 per rank: 98 us
 // against about 50), so those plans keep one kernel per step.

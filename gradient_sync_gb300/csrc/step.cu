@@ -287,6 +287,17 @@ constexpr int kSmallBatch = 4;  // elements per thread with their loads in fligh
 
 template <bool BF16>
 __global__ void __launch_bounds__(kSmallThreads) small_steps_kernel(const __grid_constant__ SmallParams p) {
+  // The transfer table in shared memory: the per-element search reads it
+  // there rather than from parameter memory.
+  __shared__ SmallXfer tab[kMaxSmallXfers];
+  static_assert(sizeof(SmallXfer) % 4 == 0, "copied as words");
+  {
+    const int words = p.step_start[p.n_steps] * int(sizeof(SmallXfer) / 4);
+    const uint32_t* from = reinterpret_cast<const uint32_t*>(p.x);
+    uint32_t* to = reinterpret_cast<uint32_t*>(tab);
+    for (int i = threadIdx.x; i < words; i += kSmallThreads) to[i] = from[i];
+  }
+  __syncthreads();
   grid_dependency_wait();
   grid_dependents_launch();
   for (int s = 0; s < p.n_steps; ++s) {
@@ -306,13 +317,13 @@ __global__ void __launch_bounds__(kSmallThreads) small_steps_kernel(const __grid
         int lo = x0, hi = x1;  // the last transfer whose first flat index is <= f
         while (hi - lo > 1) {
           const int mid = (lo + hi) >> 1;
-          if (p.x[mid].flat <= f)
+          if (tab[mid].flat <= f)
             lo = mid;
           else
             hi = mid;
         }
         xi[u] = lo;
-        const SmallXfer& t = p.x[lo];
+        const SmallXfer& t = tab[lo];
         e[u] = int64_t(t.lo) + (f - t.flat);
         const Operand X = small_operand<BF16>(p, t.xs, t.src);
         if (op == OP_COPY) {  // same type on both sides: move the bits
@@ -330,7 +341,7 @@ __global__ void __launch_bounds__(kSmallThreads) small_steps_kernel(const __grid
 #pragma unroll
       for (int u = 0; u < kSmallBatch; ++u) {
         if (xi[u] < 0) continue;
-        const SmallXfer& t = p.x[xi[u]];
+        const SmallXfer& t = tab[xi[u]];
         const Operand D = small_operand<BF16>(p, t.ds, t.dst);
         if (op == OP_COPY) {
           if (D.f32)

@@ -105,7 +105,7 @@ typedef enum {
                                        (ar_stats.launches == 1 with more than
                                        one step): a block barrier and the
                                        step's memory round trip, measured on
-                                       GB300 (16-rank ring at 1 KiB: 32.8 us
+                                       GB300 (16-rank ring at 1 KiB: 30.7 us
                                        for 30 steps) */
 
 /* Per-element summation order of AR_FUSED. (For AR_REDUCE_SCATTER,

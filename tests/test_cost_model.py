@@ -129,7 +129,7 @@ def test_device_model_of_one_cta_plans(g):
         assert st["launches"] == 1 and st["steps"] > 1
         assert g.ar_plan_predict(p, dev) == pytest.approx(
             g.AR_DEVICE_ALPHA_S + st["steps"] * g.AR_DEVICE_CTA_STEP_S + st["hbm_bytes"] / g.AR_DEVICE_BW, rel=1e-12)
-    # measured on GB300, bound: ring 32.8 us, Rabenseifner 12.3 us (within the
+    # measured on GB300, bound: ring 30.7 us, Rabenseifner 12.3 us (within the
     # ~3 us of launch and host time the model leaves out)
     ring = g.ar_plan_predict(g.ar_plan(16, 256, "f32", "ring"), dev)
     rab = g.ar_plan_predict(g.ar_plan(16, 256, "f32", "rabenseifner"), dev)
