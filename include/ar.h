@@ -189,7 +189,11 @@ typedef struct {
   int steps;                   /* dependent steps: 2(N-1) ring, 2 log2 N
                                   Rabenseifner, 2(G-1)+2(M-1) hierarchical,
                                   1 fused */
-  int launches;                /* kernels one ar_execute launches */
+  int launches;                /* kernels one ar_execute launches: 1 for a
+                                  step plan whose every step moves at most
+                                  2048 elements (its whole schedule runs in
+                                  one CTA, a block barrier between steps,
+                                  with the same results) */
   size_t bytes_sent_per_rank;  /* largest per-rank send volume of the
                                   schedule, in bytes of the payload type */
   size_t hbm_bytes;            /* algorithmic HBM bytes of one ar_execute:
