@@ -19,6 +19,9 @@ Reported (one JSON line from rank 0):
              each against its own byte count, 5(N-1) S; and the blockwise
              INT8 compressed all-reduce with error feedback (fused pass, and
              compressor + reducer), each against its own byte count
+  latency    small messages: the 16-rank ring and Rabenseifner at 1 KiB per
+             rank, bound once and replayed (ar_execute_bound); both run
+             every step in one CTA
   e2e        the same all-reduce from pinned host buffers through
              ar_execute_host, copies included
   cpu_baseline  the CPU oracle (step-by-step ring simulation) on a bounded
@@ -378,6 +381,14 @@ def run_ours(args):
     del res, codes, scales
     torch.cuda.empty_cache()
 
+    # small messages: per-call time of a bound plan, back to back from Python
+    from gradient_sync_gb300.cases import time_case
+
+    latency = {"workload": "16 ranks x 1 KiB fp32, ar_bind once, ar_execute_bound per call, back to back"}
+    for algo in ("ring", "rabenseifner"):
+        r = time_case(16, 256, algo=algo, iters=30, warmup=5, bound=True)
+        latency[algo] = {"us_per_call": r["us"], "steps": r["steps"], "launches": r["launches"]}
+
     # end to end: pinned host buffers in and out through ar_execute_host
     host_in = [torch.from_numpy(h).pin_memory() for h in host]
     host_out = [torch.empty(L, dtype=torch.float32).pin_memory() for _ in range(N)]
@@ -408,6 +419,7 @@ def run_ours(args):
                      "kernel": "fused_flat_kernel<fp32, seq>", "peak_kind": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": st["hbm_bytes"]},
         "executors": executors,
+        "latency": latency,
         "e2e": {"value": round(S * world / (ms_e2e * 1e-3) / 1e9, 2), "unit": UNIT,
                 "h2d_bytes_per_step": N * S, "d2h_bytes_per_step": N * S, "ms_per_step": round(ms_e2e, 3),
                 "api": "ar_execute_host: pinned host buffers read and written by the kernel over NVLink-C2C"},
