@@ -386,7 +386,7 @@ def run_ours(args):
 
     latency = {"workload": "16 ranks x 1 KiB fp32, ar_bind once, ar_execute_bound per call, back to back"}
     for algo in ("ring", "rabenseifner"):
-        r = time_case(16, 256, algo=algo, iters=30, warmup=5, bound=True)
+        r = time_case(16, 256, algo=algo, iters=30, warmup=5, reps=100, bound=True)
         latency[algo] = {"us_per_call": r["us"], "steps": r["steps"], "launches": r["launches"]}
 
     # end to end: pinned host buffers in and out through ar_execute_host
