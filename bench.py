@@ -24,6 +24,8 @@ Reported (one JSON line from rank 0):
              each with the CPU oracle running the same algorithm beside it:
                ring_n4_int       4 ranks x 1,048,576 integer-valued fp32
                hier_2x8_bf16     16 ranks as 2 groups of 8, 96 Mi bf16 each
+                                 (and the INT8 compressed all-reduce of the
+                                 same gradients without error feedback)
                buckets_n8_transformer  8 ranks, 16-layer transformer bf16
                                  gradients in 25 MiB buckets, x1/8, bf16 out
                sweep             2, 16 and 64 ranks x 1 GiB fp32, and
@@ -808,6 +810,19 @@ def run_workloads(dev, stream, peak, k_big: int, warmup: int):
                                           outs, N, S, k_big),
             "fused_rank_order": plan_path(g.ar_plan(N, L, "bf16", "fused", order="rank"), bufs, outs, N, S,
                                           k_big)}}
+    # the blockwise INT8 compressed all-reduce of the same bf16 gradients,
+    # without error feedback (block 128, sum x 1/16): fused pass and two calls
+    block = 128
+    n_sc, _ = g.ar_compress_sizes(L, block)
+    codes = [torch.empty(L, dtype=torch.int8, device=dev) for _ in range(N)]
+    scales = [torch.empty(n_sc, dtype=torch.float32, device=dev) for _ in range(N)]
+    for name, path in (("compressed_int8_fused", "fused"), ("compressed_int8_two_calls", "two")):
+        fn = compressed_call(bufs, outs, block, "bf16", None, N, path, handle, codes, scales)
+        ms = event_ms(fn, stream, k_big, warmup)
+        out["hier_2x8_bf16"]["paths"][name] = figures(
+            ms, N, S, compressed_hbm_bytes(N, L, "bf16", block, path, False), peak, block=block,
+            error_feedback=False, launches=1 if path == "fused" else 2)
+    del codes, scales
     task, sample = _hier_task()
     tasks.append(("hier_2x8_bf16", task, sample))
     del bufs, outs

@@ -244,10 +244,12 @@ __device__ __forceinline__ float rcp_approx(float s) {
 // passed this call's barrier, after every warp finished reading the slot of
 // the call before).
 // The maximum over the block's lanes of one warp is a butterfly of shuffles,
-// or with kLean one warp reduction: m is a non-negative float (fmaxf drops
-// NaN), and non-negative floats order as their bit patterns do, so an
-// unsigned maximum of the bits is the float maximum; each group of lanes of
-// one block reduces under its own mask.
+// or with kLean, for blocks of 16 or 32 lanes, full-warp reductions: m is a
+// non-negative float (fmaxf drops NaN), and non-negative floats order as
+// their bit patterns do, so an unsigned maximum of the bits is the float
+// maximum. A 16-lane block takes two reductions over the whole warp, the other
+// half-warp contributing 0: a reduction whose mask differs between the lanes
+// of one warp measured about one pass per distinct mask.
 template <int kEPT, bool kLean = false>
 __device__ __forceinline__ float block_scale(const float (&x)[kEPT], int block, float* wmax) {
   float m = 0.0f;
@@ -255,9 +257,13 @@ __device__ __forceinline__ float block_scale(const float (&x)[kEPT], int block, 
   for (int w = 0; w < kEPT; ++w) m = fmaxf(m, fabsf(x[w]));
   constexpr int kWarpElems = 32 * kEPT;
   const int lanes = block < kWarpElems ? block / kEPT : 32;
-  if (kLean) {
-    const unsigned mask = lanes == 32 ? kFull : ((1u << lanes) - 1u) << ((threadIdx.x & 31) & ~(lanes - 1));
-    m = __uint_as_float(__reduce_max_sync(mask, __float_as_uint(m)));
+  if (kLean && lanes == 32) {
+    m = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(m)));
+  } else if (kLean && lanes == 16) {  // one full-warp reduction per half-warp (see below)
+    const bool low = (threadIdx.x & 16) == 0;
+    const unsigned a = __reduce_max_sync(kFull, low ? __float_as_uint(m) : 0u);
+    const unsigned b = __reduce_max_sync(kFull, low ? 0u : __float_as_uint(m));
+    m = __uint_as_float(low ? a : b);
   } else {
     for (int o = lanes >> 1; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
   }
@@ -615,6 +621,239 @@ __global__ void __launch_bounds__(kThreads) compressed_allreduce_bf16_kernel(con
   }
 }
 
+// ---------------------------------------------------------------- bf16 without feedback, packed
+// The kernel above spends about 30 instructions per element and rank; with 2
+// bytes in and 2 out that bounds it by instruction issue (0.68 of its bytes at
+// 16 ranks x 96 Mi). This variant decides the same codes with fewer:
+//  - the block size is a template parameter, so the lanes of one block and
+//    their reduction mask are constants;
+//  - the code is RN(x * rc + 1.5 * 2^23) - 1.5 * 2^23 (rc the approximate
+//    reciprocal of s): the sum lands in the binade [2^23, 2^24), whose
+//    spacing is 1, so one FMA rounds the exact product x * rc to the nearest
+//    integer (ties to even, 1.5 * 2^23 being even) and the subtraction is
+//    exact. The screening deviation is one more FMA, RN(x * rc - c), the
+//    exact product's distance from its code. With |rc - 1/s| <= 2^-23 / s,
+//    |x * rc - x / s| <= 127.5 * 2^-23 < 2^-16, and RN(x / s) is within 2^-18
+//    of x / s; so when every |RN(x * rc - c)| is below 1/2 - 2^-14, c is the
+//    one integer within 1/2 of RN(x / s), which is the code the definition
+//    takes. Otherwise the element takes the correctly rounded quotient.
+//  - element pairs go through Blackwell's packed fp32x2 FMA, add and multiply
+//    (one instruction for two lanes of arithmetic, each lane an IEEE fp32
+//    operation rounded to nearest even). The reconstruction d = RN(c * s) is
+//    a packed FMA with +0: c * s is never -0 here (c is +0 or a nonzero
+//    integer, s a normal), so it equals the rounded product bit for bit, and
+//    an FMA is never merged with the add that follows it;
+//  - the block maximum and the screening maximum take three operands per
+//    instruction;
+//  - the rank loop is unrolled by two over two load buffers: each buffer is
+//    refilled, two (tile, rank) pairs ahead, as soon as its words are
+//    widened, so no registers are copied to keep the pipeline going.
+// Ranks come in pairs, so the rank count is even; the tile of the ragged end
+// is folded by the generic per-rank path above (the same bits).
+
+// Two fp32 values as the 64-bit operand of a packed instruction (lo first).
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// max(|a|, |b|, |c|) in one instruction.
+__device__ __forceinline__ float max3abs(float a, float b, float c) {
+  float d;
+  asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Pairs of one thread's 8 elements of one rank.
+struct Pairs8 {
+  uint64_t v[4];
+};
+
+// Fold rank `r`'s words w (8 bf16, widened here) into the running sum.
+// kFirst: acc = d (rank 0). wm: this call's shared-memory slot for blocks
+// that span warps (callers alternate two slots).
+template <int kBlock, bool kFirst>
+__device__ __forceinline__ void lean_bf16_rank(const float (&x)[8], float* wm, Pairs8& acc) {
+  constexpr int kLanes = kBlock >= 32 * 8 ? 32 : kBlock / 8;  // lanes of one block within a warp
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  constexpr float kTie = 0.5f - 0x1p-14f;
+  float m = max3abs(x[0], x[1], x[2]);
+  m = max3abs(m, x[3], x[4]);
+  m = max3abs(m, x[5], x[6]);
+  m = fmaxf(m, fabsf(x[7]));
+  // The maximum over the block's lanes. m is non-negative, and non-negative
+  // floats order as their bits do, so a warp reduction of the bits (unsigned
+  // maximum) is the float maximum. A reduction whose mask differs between the
+  // lanes of one warp ran about once per distinct mask (block 16 slower than
+  // shuffles, block 128 barely faster), so only full-warp reductions are
+  // used: one for blocks of 32 or more lanes, two (one per half-warp, the
+  // other half contributing 0) for 16 lanes, and shuffle rounds below that.
+  if constexpr (kLanes == 32) {
+    m = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(m)));
+  } else if constexpr (kLanes == 16) {
+    const bool low = (threadIdx.x & 16) == 0;
+    const unsigned a = __reduce_max_sync(kFull, low ? __float_as_uint(m) : 0u);
+    const unsigned b = __reduce_max_sync(kFull, low ? 0u : __float_as_uint(m));
+    m = __uint_as_float(low ? a : b);
+  } else {
+#pragma unroll
+    for (int o = kLanes / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  }
+  if constexpr (kBlock > 32 * 8) {
+    constexpr int W = kBlock / (32 * 8);
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) wm[warp] = m;
+    __syncthreads();
+    const int w0 = warp & ~(W - 1);
+    m = wm[w0];
+#pragma unroll
+    for (int i = 1; i < W; ++i) m = fmaxf(m, wm[w0 + i]);
+  }
+  const float s = div127(m);
+  float c[8];
+  if (s >= 0x1p-126f) {
+    const float rc = rcp_approx(s);
+    const uint64_t RC = pk2(rc, rc), MM = pk2(kMagic, kMagic);
+    float worst = 0.0f, dv[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint64_t X = pk2(x[2 * i], x[2 * i + 1]);
+      const uint64_t Y = fma2(X, RC, MM);  // M + the nearest integer to x * rc
+      const uint64_t C = sub2(Y, MM);      // exact
+      const uint64_t D = fma2(X, RC, sub2(MM, Y));  // RN(x * rc - c)
+      upk2(C, c[2 * i], c[2 * i + 1]);
+      upk2(D, dv[2 * i], dv[2 * i + 1]);
+      worst = max3abs(worst, dv[2 * i], dv[2 * i + 1]);
+    }
+    if (worst >= kTie) {  // a quotient near a tie: the correctly rounded quotient decides
+#pragma unroll
+      for (int w = 0; w < 8; ++w)
+        if (fabsf(dv[w]) >= kTie) c[w] = round_int(__fdiv_rn(x[w], s));
+    }
+    // |x / s| < 127.5 for a normal s, so no clamp is needed here
+  } else if (s > 0.0f) {  // a subnormal scale: exact quotients, clamped
+#pragma unroll
+    for (int w = 0; w < 8; ++w) c[w] = fminf(fmaxf(round_int(__fdiv_rn(x[w], s)), -127.0f), 127.0f);
+  } else {
+#pragma unroll
+    for (int w = 0; w < 8; ++w) c[w] = 0.0f;
+  }
+  const uint64_t S2 = pk2(s, s), Z2 = pk2(0.0f, 0.0f);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint64_t D = fma2(pk2(c[2 * i], c[2 * i + 1]), S2, Z2);  // RN(c * s), see above
+    acc.v[i] = kFirst ? D : add2(acc.v[i], D);
+  }
+}
+
+__device__ __forceinline__ void widen8(const uint4& w, float (&x)[8]) {
+  x[0] = bf16lo(w.x); x[1] = bf16hi(w.x); x[2] = bf16lo(w.y); x[3] = bf16hi(w.y);
+  x[4] = bf16lo(w.z); x[5] = bf16hi(w.z); x[6] = bf16lo(w.w); x[7] = bf16hi(w.w);
+}
+
+template <int kLogBlock>
+__global__ void __launch_bounds__(kThreads) compressed_allreduce_bf16_packed_kernel(
+    const __grid_constant__ CompressParams p) {
+  constexpr int kEPT = 8;
+  constexpr int kTileElems = kEPT * kThreads;
+  constexpr int kBlock = 1 << kLogBlock;
+  __shared__ float wmax[2][kWarps];
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int n = p.n;  // even
+  const int64_t n_full = p.count / kTileElems;
+  const int64_t lane_off = int64_t(kEPT) * threadIdx.x;
+  const int64_t stride = int64_t(gridDim.x) * kTileElems;
+  // the fetch cursor: the (tile, rank) pair the next load is for, two pairs
+  // ahead of the one being folded
+  int64_t f_off = int64_t(blockIdx.x) * kTileElems + lane_off;
+  int f_r = 0;
+  const int64_t f_end = n_full * kTileElems;
+  auto fetch = [&](uint4& w) {
+    if (f_off < f_end) w = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.g[f_r]) + f_off));
+    if (++f_r == n) {
+      f_r = 0;
+      f_off += stride;
+    }
+  };
+  uint4 X0 = make_uint4(0u, 0u, 0u, 0u), X1 = X0;
+  fetch(X0);
+  fetch(X1);
+  int phase = 0;
+  for (int64_t tile = blockIdx.x; tile < n_full; tile += gridDim.x) {
+    Pairs8 acc;
+    float x[8];
+    widen8(X0, x);
+    fetch(X0);
+    lean_bf16_rank<kBlock, true>(x, wmax[phase], acc);
+    phase ^= 1;
+    widen8(X1, x);
+    fetch(X1);
+    lean_bf16_rank<kBlock, false>(x, wmax[phase], acc);
+    phase ^= 1;
+#pragma unroll 1
+    for (int r = 2; r < n; r += 2) {
+      widen8(X0, x);
+      fetch(X0);
+      lean_bf16_rank<kBlock, false>(x, wmax[phase], acc);
+      phase ^= 1;
+      widen8(X1, x);
+      fetch(X1);
+      lean_bf16_rank<kBlock, false>(x, wmax[phase], acc);
+      phase ^= 1;
+    }
+    const uint64_t SC = pk2(p.scale, p.scale);
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) upk2(mul2(acc.v[i], SC), a[2 * i], a[2 * i + 1]);
+    const uint4 out = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                                 pack_bf16x2(a[6], a[7]));
+    const int64_t e = tile * kTileElems + lane_off;
+#pragma unroll 1
+    for (int r = 0; r < n; ++r) __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out[r]) + e), out);
+  }
+  // the ragged end: one partial tile, folded by the last CTA with bounds
+  if (blockIdx.x == gridDim.x - 1 && n_full * kTileElems < p.count) {
+    const int64_t e = n_full * kTileElems + lane_off;
+    float acc[kEPT];
+#pragma unroll 1
+    for (int r = 0; r < n; ++r) {
+      float x[kEPT], res[kEPT];
+      load_group<true, kEPT>(p.g[r], e, p.count, x);
+      fold_rank<kEPT, false, true>(x, r, kBlock, wmax[phase], acc, res);
+      phase ^= 1;
+    }
+    if (e < p.count) {
+      mul_each(acc, acc, p.scale);
+#pragma unroll 1
+      for (int r = 0; r < n; ++r) store_group<true, kEPT>(p.out[r], e, p.count, acc);
+    }
+  }
+}
+
 // Each tile, ranks in order: quantise rank r's block, add its reconstruction
 // to the running sum and store its residual; then write the scaled sum to
 // every rank. No message leaves the registers.
@@ -720,8 +959,26 @@ cudaError_t launch_compressed_reduce(const CompressParams& p, ar_dtype out_dtype
   return launch(k, n_tiles(p.count, out_dtype == AR_BF16 ? reduce_ept<true>() : reduce_ept<false>()), p, stream);
 }
 
+// The packed bf16 kernel for each block size, 16 (2^4) to 1024 (2^10).
+Kern packed_bf16_kernel(int block) {
+  switch (block) {
+    case 16: return compressed_allreduce_bf16_packed_kernel<4>;
+    case 32: return compressed_allreduce_bf16_packed_kernel<5>;
+    case 64: return compressed_allreduce_bf16_packed_kernel<6>;
+    case 128: return compressed_allreduce_bf16_packed_kernel<7>;
+    case 256: return compressed_allreduce_bf16_packed_kernel<8>;
+    case 512: return compressed_allreduce_bf16_packed_kernel<9>;
+    case 1024: return compressed_allreduce_bf16_packed_kernel<10>;
+    default: return nullptr;
+  }
+}
+
 cudaError_t launch_compressed_allreduce(const CompressParams& p, ar_dtype dtype, cudaStream_t stream) {
   const bool bf = dtype == AR_BF16;
+  if (bf && !p.ef && p.n % 2 == 0) {
+    const Kern k = packed_bf16_kernel(p.block);
+    if (k != nullptr) return launch(k, n_tiles(p.count, ept<true>()), p, stream);
+  }
   const Kern k = bf ? (p.ef ? compressed_allreduce_kernel<true, true> : compressed_allreduce_bf16_kernel)
                     : (p.ef ? compressed_allreduce_kernel<false, true> : compressed_allreduce_kernel<false, false>);
   return launch(k, n_tiles(p.count, bf ? ept<true>() : ept<false>()), p, stream);

@@ -206,6 +206,86 @@ def test_compressed_allreduce_matches_oracle(g, block, dtype, ef):
                 assert_bits_equal(to_host(res[r], "f32"), want_e[r], f"residual N={N} L={L} rank {r}")
 
 
+def _bf16_near_tie_blocks(block, nb, seed):
+    """[nb * block] bf16 bit patterns: block k holds its maximum +-m_k first,
+    then the bf16 values x whose quotients x / s_k (s_k = RN(m_k / 127)) lie
+    closest to a half-integer (within 2^-13, exact ties included), both
+    signs. Every m_k is a bf16 value, so s_k is the scale the kernels and the
+    oracle compute for the block."""
+    rng = np.random.default_rng(seed)
+    out = np.zeros((nb, block), np.uint16)
+    for k in range(nb):
+        exp = int(rng.integers(110, 140))
+        if k % 4 == 0:  # m = 127 * 2^j: s is a power of two and ties are exact
+            mbits = int(numerics.f32_to_bf16_rne(np.array([127.0 * 2.0 ** (exp - 127)], F32))[0])
+        else:
+            mbits = (exp << 7) | int(rng.integers(0, 128))
+        m = numerics.bf16_to_f32(np.array([mbits], np.uint16))[0]
+        s = np.float64(F32(m) / F32(127))
+        cand = np.arange(1, mbits, dtype=np.uint16)  # every positive bf16 value below m
+        q = numerics.bf16_to_f32(cand).astype(np.float64) / s
+        dist = np.abs(q - (np.floor(q) + 0.5))
+        near = cand[dist < 2.0 ** -13]
+        if near.size == 0:
+            near = cand[np.argsort(dist)[:8]]
+        vals = np.resize(near, block - 1)
+        signs = rng.integers(0, 2, block - 1).astype(np.uint16) << 15
+        out[k, 0] = mbits | (np.uint16(rng.integers(0, 2)) << 15)
+        out[k, 1:] = vals | signs
+        rng.shuffle(out[k, 1:])
+    return out.reshape(-1)
+
+
+@pytest.mark.parametrize("block", [16, 128, 1024])
+@pytest.mark.parametrize("N", [2, 3, 4])
+def test_compressed_allreduce_bf16_near_ties(g, N, block):
+    """bf16 without feedback on quotients next to half-integers and on exact
+    ties: the code of every element must be the one the correctly rounded
+    quotient gives, so the result is the oracle's bit for bit (even N runs the
+    packed kernel, odd N the generic one)."""
+    nb = max(8, 4096 // block)
+    x = np.stack([_bf16_near_tie_blocks(block, nb, seed=100 * N + block + r) for r in range(N)])
+    L = x.shape[1] - 3  # a ragged end as well
+    x = np.ascontiguousarray(x[:, :L])
+    grads = _dev(x, "bf16")
+    outs = [torch.empty_like(t) for t in grads]
+    g.ar_compressed_allreduce(grads, block, dtype="bf16", scale=1.0 / N, outs=outs, count=L)
+    torch.cuda.synchronize()
+    want, _, _, _ = C.compressed_allreduce(widened(x, "bf16"), None, block, scale=1.0 / N, out_dtype="bf16")
+    for r in range(N):
+        assert_bits_equal(to_host(outs[r], "bf16"), want, f"N={N} rank {r}")
+
+
+def test_compressed_allreduce_bf16_full_size(g):
+    """16 ranks x 96 Mi bf16 without feedback, block 128, x1/16, out of place:
+    the packed kernel in the benchmark's launch configuration. The oracle
+    checks block-aligned windows (blocks are independent); every rank's result
+    is bitwise identical on the whole buffer."""
+    spec = workloads.HIER_2X8_BF16
+    N, L, block = spec.n_ranks, spec.count, 128
+    rng = np.random.default_rng(1)
+    starts = np.unique(np.concatenate([[0, L - 4 * block], rng.integers(0, L // block - 8, 48) * block]))
+    idx = np.concatenate([np.arange(s, s + 4 * block) for s in starts]).astype(np.int64)
+    grads, xs = [], []
+    for r in range(N):
+        h = workloads.rank_buffer(spec, r)
+        grads.append(to_device(h, "bf16"))
+        xs.append(h[idx])
+        del h
+    xs = np.stack(xs)
+    outs = [torch.empty_like(t) for t in grads]
+    g.ar_compressed_allreduce(grads, block, dtype="bf16", scale=1 / N, outs=outs)
+    torch.cuda.synchronize()
+    want, _, _, _ = C.compressed_allreduce(widened(xs, "bf16"), None, block, scale=1 / N, out_dtype="bf16")
+    didx = torch.from_numpy(idx).cuda()
+    for r in range(N):
+        assert_bits_equal(outs[r][didx].view(torch.int16).cpu().numpy().view(np.uint16), want, f"rank {r}")
+        if r:
+            assert torch.equal(outs[r].view(torch.int16), outs[0].view(torch.int16))
+    del grads, outs
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_two_calls_equal_the_fused_pass(g, dtype):
     """ar_compress + ar_compressed_reduce against the oracle, and the fused pass
