@@ -90,13 +90,40 @@ __device__ __forceinline__ void seg_range(const FusedParams& p, int seg, int64_t
   }
 }
 
-template <bool BF16, bool TREE, int NB, int VPT>
+// The rank a segment's fold starts from when its order is a rotation of the
+// rank list (every order but the hierarchical one).
+__device__ __forceinline__ int seg_rotation(const FusedParams& p, int seg) {
+  if (p.collective == AR_ALLGATHER) return seg;  // one position: the chunk's owner
+  if (p.order != AR_ORDER_RING) return 0;        // rank order, Rabenseifner's tree
+  if (p.collective == AR_REDUCE_SCATTER) return seg + 1 < p.n ? seg + 1 : 0;
+  return seg;  // ring all-reduce: chunk c from rank c
+}
+
+// How a CTA gets the fold sequence of a segment:
+//  kSeqWritten: written to shared memory when the CTA moves to the segment,
+//    between two barriers (the hierarchical order, whose sequence is not a
+//    rotation of the rank list);
+//  kSeqRotated: the ranks' input pointers are written once, twice over in
+//    rank order, so a segment's sequence starts at its rotation (seg_rotation)
+//    with no rewrite; the per-position flags are written once too;
+//  kSeqRotatedPos: the same, with the flags taken from the position
+//    (fold_single).
+// Moving to another segment then costs one barrier, which keeps the warps of
+// a CTA on the same tile (the stores of a tile land together); without it,
+// and with the rewrite's two barriers, the kernel measured slower. At 64
+// ranks x 16 MiB a ring chunk is 64 tiles, so nearly every tile of a CTA
+// starts a new segment.
+enum SeqMode { kSeqWritten = 0, kSeqRotated = 1, kSeqRotatedPos = 2 };
+
+template <bool BF16, bool TREE, int MODE, int NB, int VPT>
 __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_flat_kernel(const __grid_constant__ FusedParams p) {
   using LV = Lane<BF16, true>;
   using LS = Lane<BF16, false>;
   constexpr int W = LV::W;
   constexpr int64_t kTile = int64_t(kThreads) * W * VPT;
-  __shared__ const char* s_seq[AR_MAX_RANKS];
+  constexpr bool kRot = MODE != kSeqWritten;
+  // kSeqWritten: the segment's sequence; otherwise the ranks in order, twice
+  __shared__ const char* s_seq[2 * AR_MAX_RANKS];
   __shared__ uint8_t s_flag[AR_MAX_RANKS];
   __shared__ char* s_out[AR_MAX_RANKS];
   grid_dependency_wait();  // the previous kernel on the stream has finished and its writes are visible
@@ -104,8 +131,14 @@ __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_flat_kernel(con
   const int n = p.n;
   const int nf = p.collective == AR_ALLGATHER ? 1 : n;  // ranks folded per element
   const bool owner_only = p.collective == AR_REDUCE_SCATTER;
-  if (threadIdx.x < n) s_out[threadIdx.x] = static_cast<char*>(p.out[threadIdx.x]);
-  int cur = -1;
+  if (threadIdx.x < n) {
+    s_out[threadIdx.x] = static_cast<char*>(p.out[threadIdx.x]);
+    if (kRot) {
+      s_seq[threadIdx.x] = s_seq[threadIdx.x + n] = static_cast<const char*>(p.in[threadIdx.x]);
+      s_flag[threadIdx.x] = (threadIdx.x == 0 ? kStart : 0) | (threadIdx.x == nf - 1 ? (kEnd | kFirst) : 0);
+    }
+  }
+  int cur = -1, rot = 0;
   int64_t lo = 0, hi = 0;
   const int64_t total = int64_t(p.n_seg) * p.tiles_per_seg;
   for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
@@ -113,17 +146,21 @@ __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_flat_kernel(con
     const int64_t tt = t - int64_t(seg) * p.tiles_per_seg;
     if (seg != cur) {  // uniform across the CTA
       __syncthreads();
-      cur = seg;
-      seg_range(p, seg, lo, hi);
-      if (threadIdx.x < n) {
-        int rank;
-        uint8_t flag;
-        seq_position(p, seg, threadIdx.x, rank, flag);
-        s_seq[threadIdx.x] = static_cast<const char*>(p.in[rank]);
-        s_flag[threadIdx.x] = flag;
+      if (!kRot) {
+        if (threadIdx.x < n) {
+          int rank;
+          uint8_t flag;
+          seq_position(p, seg, threadIdx.x, rank, flag);
+          s_seq[threadIdx.x] = static_cast<const char*>(p.in[rank]);
+          s_flag[threadIdx.x] = flag;
+        }
+        __syncthreads();
       }
-      __syncthreads();
+      cur = seg;
+      rot = kRot ? seg_rotation(p, seg) : 0;
+      seg_range(p, seg, lo, hi);
     }
+    const char* const* seq = s_seq + rot;
     const int64_t clo = lo > p.e_lo ? lo : p.e_lo;
     const int64_t chi = hi < p.e_hi ? hi : p.e_hi;
     if (clo >= chi) continue;
@@ -142,9 +179,11 @@ __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_flat_kernel(con
     if (any) {
       float acc[VPT][W];
       if (TREE) {
-        fold_tree<LV, NB>(acc[0], s_seq, nf, e[0]);
+        fold_tree<LV, NB>(acc[0], seq, nf, e[0]);
+      } else if (MODE == kSeqRotatedPos) {
+        fold_single<LV, NB, VPT>(acc, seq, nf, e, ok);
       } else {
-        fold_sequence<LV, NB, VPT>(acc, s_seq, s_flag, nf, e, ok);
+        fold_sequence<LV, NB, VPT>(acc, seq, s_flag, nf, e, ok);
       }
       typename LV::raw_t r[VPT];
 #pragma unroll
@@ -180,9 +219,9 @@ __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_flat_kernel(con
         const int64_t es1[1] = {es};
         const bool ok1[1] = {true};
         if (TREE)
-          fold_tree<LS, 8>(acc[0], s_seq, nf, es);
+          fold_tree<LS, 8>(acc[0], seq, nf, es);
         else
-          fold_sequence<LS, 8, 1>(acc, s_seq, s_flag, nf, es1, ok1);
+          fold_sequence<LS, 8, 1>(acc, seq, s_flag, nf, es1, ok1);
         acc[0][0] = fmul(acc[0][0], p.scale);
         const typename LS::raw_t r = LS::narrow(acc[0]);
         if (owner_only)
@@ -327,19 +366,39 @@ int64_t fused_tile_elems(ar_dtype dtype, int n, int order, int collective, bool 
   return int64_t(kThreads) * fused_vec_elems(dtype, v8) * (v8 ? 1 : fused_vpt(n, order, collective));
 }
 
+// Every order but the hierarchical one (rotations of the rank list). The
+// flags are taken from the position for more than 16 ranks and for the
+// reduce-scatter, and read from shared memory otherwise (fold_single).
+template <bool BF16>
+cudaError_t launch_fused_rot(const FusedParams& p, int64_t tiles, int sm_budget, cudaStream_t stream) {
+  if (p.order == AR_ORDER_TREE && p.collective != AR_ALLGATHER)
+    return launch_persistent(fused_flat_kernel<BF16, true, kSeqRotated, 8, 1>, p, tiles, sm_budget, stream);
+  if (p.collective == AR_REDUCE_SCATTER && p.n > 4)
+    return launch_persistent(fused_flat_kernel<BF16, false, kSeqRotatedPos, kRsNB, kRsVPT>, p, tiles, sm_budget,
+                             stream);
+  if (p.collective == AR_ALLGATHER)
+    return launch_persistent(fused_flat_kernel<BF16, false, kSeqRotated, 1, kAgVPT>, p, tiles, sm_budget, stream);
+  switch (fused_vpt(p.n, p.order, p.collective)) {
+    case 4: return launch_persistent(fused_flat_kernel<BF16, false, kSeqRotated, 2, 4>, p, tiles, sm_budget, stream);
+    case 2: return launch_persistent(fused_flat_kernel<BF16, false, kSeqRotated, 4, 2>, p, tiles, sm_budget, stream);
+    default:
+      return p.n > 16 ? launch_persistent(fused_flat_kernel<BF16, false, kSeqRotatedPos, 8, 1>, p, tiles, sm_budget, stream)
+                      : launch_persistent(fused_flat_kernel<BF16, false, kSeqRotated, 8, 1>, p, tiles, sm_budget, stream);
+  }
+}
+
+// The hierarchical order writes each segment's sequence; the other orders
+// are rotations of the rank list.
 template <bool BF16>
 cudaError_t launch_fused_t(const FusedParams& p, int64_t tiles, int sm_budget, cudaStream_t stream) {
-  if (p.order == AR_ORDER_TREE && p.collective != AR_ALLGATHER)
-    return launch_persistent(fused_flat_kernel<BF16, true, 8, 1>, p, tiles, sm_budget, stream);
-  if (p.collective == AR_REDUCE_SCATTER && p.n > 4)
-    return launch_persistent(fused_flat_kernel<BF16, false, kRsNB, kRsVPT>, p, tiles, sm_budget, stream);
-  if (p.collective == AR_ALLGATHER)
-    return launch_persistent(fused_flat_kernel<BF16, false, 1, kAgVPT>, p, tiles, sm_budget, stream);
-  switch (fused_vpt(p.n, p.order, p.collective)) {
-    case 4: return launch_persistent(fused_flat_kernel<BF16, false, 2, 4>, p, tiles, sm_budget, stream);
-    case 2: return launch_persistent(fused_flat_kernel<BF16, false, 4, 2>, p, tiles, sm_budget, stream);
-    default: return launch_persistent(fused_flat_kernel<BF16, false, 8, 1>, p, tiles, sm_budget, stream);
+  if (p.order == AR_ORDER_HIER && p.collective == AR_ALLREDUCE) {  // the planner allows it for all-reduce only
+    switch (fused_vpt(p.n, p.order, p.collective)) {
+      case 4: return launch_persistent(fused_flat_kernel<BF16, false, kSeqWritten, 2, 4>, p, tiles, sm_budget, stream);
+      case 2: return launch_persistent(fused_flat_kernel<BF16, false, kSeqWritten, 4, 2>, p, tiles, sm_budget, stream);
+      default: return launch_persistent(fused_flat_kernel<BF16, false, kSeqWritten, 8, 1>, p, tiles, sm_budget, stream);
+    }
   }
+  return launch_fused_rot<BF16>(p, tiles, sm_budget, stream);
 }
 
 cudaError_t launch_fused(const FusedParams& p, ar_dtype dtype, int sm_budget, cudaStream_t stream) {
