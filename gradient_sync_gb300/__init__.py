@@ -27,7 +27,7 @@ AR_RECDOUBLING, AR_DBTREE, AR_TORUS = 5, 6, 7
 ALGOS = {"ring": AR_RING, "rabenseifner": AR_RABENSEIFNER, "hier": AR_HIER, "fused": AR_FUSED, "auto": AR_AUTO,
          "recdoubling": AR_RECDOUBLING, "dbtree": AR_DBTREE, "torus": AR_TORUS}
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
-AR_DEVICE_ALPHA_S, AR_DEVICE_BW, AR_DEVICE_CTA_STEP_S = 1.5e-6, 6.0e12, 1.0e-6
+AR_DEVICE_ALPHA_S, AR_DEVICE_BW, AR_DEVICE_CTA_STEP_S, AR_DEVICE_CTA_STEP_MEM_S = 1.5e-6, 6.0e12, 0.28e-6, 0.75e-6
 ORDERS = {"ring": AR_ORDER_RING, "rank": AR_ORDER_RANK, "tree": AR_ORDER_TREE, "hier": AR_ORDER_HIER}
 DTYPES = {"f32": AR_F32, "bf16": AR_BF16}
 COLLECTIVES = {"allreduce": AR_ALLREDUCE, "reduce_scatter": AR_REDUCE_SCATTER, "allgather": AR_ALLGATHER}

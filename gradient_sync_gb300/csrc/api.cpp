@@ -4,6 +4,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <memory>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -454,6 +455,14 @@ void compute_stats(ar_plan_t* p) {
   }
   p->small = N > 1 && L > 0 && step_elems <= kSmallStepElems && n_x + N <= kMaxSmallXfers &&
              int64_t(p->steps.size()) + 1 <= kMaxSmallSteps;
+  {  // on chip: the data fit, rows are whole 4-byte words, and the pieces fit the table
+    int64_t pieces = 0;
+    for (const Step& s : p->steps)
+      for (const Transfer& t : s.xfers) pieces += (t.hi - t.lo + kSmallPiece - 1) / kSmallPiece;
+    pieces += N + L / kSmallPiece;  // the all-gather's own-chunk copies, at most
+    p->small_smem = p->small && small_smem_data_bytes(N, L) <= kSmallSmemDataBytes &&
+                    (L * int64_t(esize(d.dtype))) % 4 == 0 && pieces <= kMaxSmallXfers;
+  }
   if (p->small) st.launches = 1;
 }
 
@@ -575,8 +584,10 @@ ar_status execute_fused(const ar_plan_t* p, void* const* bufs, void* const* outs
   return from_cuda(launch_fused(fp, d.dtype, d.sm_budget, stream));
 }
 
+// `keep` (a plan that runs in one CTA only): fill *keep with the launch's
+// parameters and *keep_smem with its kernel instead of launching (ar_bind).
 ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs, void* workspace,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, SmallParams* keep = nullptr, bool* keep_smem = nullptr) {
   const ar_desc& d = p->desc;
   const int N = d.n_ranks;
   static thread_local StepParams sp;  // ~3 KB, reused between calls
@@ -647,10 +658,89 @@ ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs
       q.step_elems[ns] = flat;
       ++ns;
     };
-    if (!own.xfers.empty()) add(own);
-    for (const Step& st : p->steps) add(st);
+    // on chip: rows copied as words, so every buffer must be 4-byte aligned
+    bool smem = p->small_smem, vec16 = (int64_t(d.count) * int64_t(esize(d.dtype))) % 16 == 0;
+    for (int r = 0; r < N; ++r) {
+      const uintptr_t a = reinterpret_cast<uintptr_t>(q.raw[r]), b = reinterpret_cast<uintptr_t>(q.res[r]);
+      smem = smem && a % 4 == 0 && b % 4 == 0;
+      vec16 = vec16 && a % 16 == 0 && b % 16 == 0;
+    }
+    if (smem) {  // the same steps, their transfers cut into pieces of one warp
+      // The kernel's shared-memory layout (step.cu, small_steps_smem_kernel):
+      // pieces, then (bf16) the fp32 partials, the inputs, the outputs.
+      const int64_t L = int64_t(d.count), es = int64_t(esize(d.dtype));
+      const bool bf = d.dtype == AR_BF16;
+      int64_t n_pieces = 0;
+      auto count_pieces = [&](const Step& st) {
+        for (const Transfer& t : st.xfers) n_pieces += (t.hi - t.lo + kSmallPiece - 1) / kSmallPiece;
+      };
+      if (!own.xfers.empty()) count_pieces(own);
+      for (const Step& st : p->steps) count_pieces(st);
+      const int64_t tab = (n_pieces * int64_t(sizeof(SmemPiece)) + 15) / 16 * 16;
+      const int64_t part0 = tab, raw0 = tab + (bf ? 4 * N * L : 0), res0 = raw0 + N * L * es;
+      // (byte offset of element 0 of the operand, fp32?)
+      auto where = [&](int space, int rank) -> std::pair<int64_t, bool> {
+        const bool in_place = q.res[rank] == q.raw[rank];
+        const int64_t in = raw0 + rank * L * es, out = in_place ? in : res0 + rank * L * es;
+        if (space == RAW) return {in, !bf};
+        if (space == RES) return {out, !bf};
+        if (bf) return {part0 + rank * L * 4, true};
+        return {out, true};
+      };
+      int widest = 1;
+      auto add_pieces = [&](const Step& st) {
+        q.step_start[ns] = nx;
+        q.step_op[ns] = uint8_t(st.op);
+        const int first = nx;
+        for (const Transfer& t : st.xfers)
+          for (int64_t lo = t.lo; lo < t.hi; lo += kSmallPiece) {
+            SmemPiece& y = q.px[nx++];
+            std::memset(&y, 0, sizeof(y));
+            const auto X = where(t.xs, t.src), Y = where(t.ys, t.dst), D = where(t.ds, t.dst);
+            y.x = uint32_t(X.first + lo * (X.second ? 4 : 2));
+            y.y = uint32_t(Y.first + lo * (Y.second ? 4 : 2));
+            y.d = uint32_t(D.first + lo * (D.second ? 4 : 2));
+            y.flags = uint8_t((X.second ? kPieceX32 : 0) | (Y.second ? kPieceY32 : 0) | (D.second ? kPieceD32 : 0) |
+                              (t.fin ? kPieceFin : 0));
+            if (t.src2 >= 0) {
+              const auto X2 = where(t.x2s, t.src2);
+              y.x2 = uint32_t(X2.first + lo * (X2.second ? 4 : 2));
+              y.flags |= uint8_t(kPieceTwo | (X2.second ? kPieceX2_32 : 0));
+            }
+            if (t.pair) {  // the partner's copy of the same space
+              const auto D2 = where(t.ds, t.src);
+              y.d2 = uint32_t(D2.first + lo * (D2.second ? 4 : 2));
+              y.flags |= kPiecePair;
+            }
+            y.len = uint16_t(std::min<int64_t>(kSmallPiece, t.hi - lo));
+          }
+        widest = std::max(widest, nx - first);
+        q.step_elems[ns] = 0;
+        ++ns;
+      };
+      if (!own.xfers.empty()) add_pieces(own);
+      for (const Step& st : p->steps) add_pieces(st);
+      int threads = 128;  // at least 4 warps for the copies in and out
+      while (threads < 32 * widest && threads < 1024) threads *= 2;
+      q.threads = threads;
+    } else {
+      if (!own.xfers.empty()) add(own);
+      for (const Step& st : p->steps) add(st);
+    }
     q.step_start[ns] = nx;
     q.n_steps = ns;
+    q.n_ranks = N;
+    q.count = int32_t(d.count);
+    q.in_place = 0;
+    q.vec16 = vec16 ? 1 : 0;
+    for (int r = 0; r < N; ++r)
+      if (q.res[r] == q.raw[r]) q.in_place |= uint64_t(1) << r;
+    if (keep != nullptr) {
+      std::memcpy(keep, &q, sizeof(q));
+      *keep_smem = smem;
+      return AR_OK;
+    }
+    if (smem) return from_cuda(launch_small_steps_smem(q, d.dtype, stream));
     return from_cuda(launch_small_steps(q, d.dtype, stream));
   }
   if (!own.xfers.empty()) {
@@ -852,6 +942,8 @@ ar_status ar_execute(const ar_plan_t* plan, void* const* bufs, void* const* outs
 // Single-pass plans are one kernel, which a direct launch starts sooner than
 // a one-node graph (measured on GB300: 3.8 against 6.2 us per call back to
 // back), so they keep the validated plan and buffers and launch directly.
+// So do step plans that run whole in one CTA: their launch parameters are
+// built once, here, and launched as they are on every call.
 struct ar_bound {
   int device = -1;
   cudaGraph_t graph = nullptr;
@@ -859,6 +951,9 @@ struct ar_bound {
   struct ar_plan plan;          // fused: a copy of the plan (its descriptor and stats)
   std::vector<void*> bufs, outs;
   bool direct = false;
+  std::unique_ptr<ar::SmallParams> small;  // one-CTA step plan: its launch parameters
+  bool small_smem = false;
+  ar_dtype dtype = AR_F32;
 };
 
 namespace {
@@ -899,6 +994,21 @@ ar_status ar_bind(const ar_plan_t* plan, void* const* bufs, void* const* outs, v
     *out = b;
     return AR_OK;
   }
+  if (plan->small) {  // one CTA: the parameters once, a direct launch per call
+    b->small.reset(new (std::nothrow) ar::SmallParams);
+    if (!b->small) {
+      release(b);
+      return AR_ENOMEM;
+    }
+    b->dtype = plan->desc.dtype;
+    const ar_status s = execute_steps(plan, bufs, outs, workspace, nullptr, b->small.get(), &b->small_smem);
+    if (s != AR_OK) {
+      release(b);
+      return s;
+    }
+    *out = b;
+    return AR_OK;
+  }
   // Record on a private stream. Relaxed mode: the launchers' first-use
   // occupancy queries are allowed while capturing.
   cudaStream_t cap = nullptr;
@@ -926,7 +1036,7 @@ ar_status ar_bind(const ar_plan_t* plan, void* const* bufs, void* const* outs, v
 
 ar_status ar_execute_bound(const ar_bound_t* bound, void* stream) {
   if (bound == nullptr) return AR_EINVAL;
-  if (bound->exec == nullptr && !bound->direct) return AR_OK;  // count == 0
+  if (bound->exec == nullptr && !bound->direct && !bound->small) return AR_OK;  // count == 0
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return AR_ECUDA;
   if (dev != bound->device) return AR_EINVAL;
@@ -936,6 +1046,10 @@ ar_status ar_execute_bound(const ar_bound_t* bound, void* stream) {
   if (bound->direct)
     return execute_fused(&bound->plan, bound->bufs.data(), bound->outs.empty() ? nullptr : bound->outs.data(), 0,
                          int64_t(bound->plan.desc.count), static_cast<cudaStream_t>(stream));
+  if (bound->small)
+    return from_cuda(bound->small_smem
+                         ? launch_small_steps_smem(*bound->small, bound->dtype, static_cast<cudaStream_t>(stream))
+                         : launch_small_steps(*bound->small, bound->dtype, static_cast<cudaStream_t>(stream)));
   return from_cuda(cudaGraphLaunch(bound->exec, static_cast<cudaStream_t>(stream)));
 }
 
@@ -1048,7 +1162,8 @@ ar_status ar_plan_predict(const ar_plan_t* plan, const ar_fabric* f, double* sec
   const ar_stats& st = plan->stats;
   const int N = d.n_ranks, rps = f->ranks_per_server;
   if (f->shared_memory) {  // one memory for all ranks: each launch, the in-CTA steps, then all its bytes
-    const double cta_steps = plan->small ? double(st.steps) * AR_DEVICE_CTA_STEP_S : 0.0;
+    const double per_step = plan->small_smem ? AR_DEVICE_CTA_STEP_S : AR_DEVICE_CTA_STEP_MEM_S;
+    const double cta_steps = plan->small ? double(st.steps) * per_step : 0.0;
     *seconds = st.launches * f->alpha + cta_steps + double(st.hbm_bytes) / f->bw_local;
     return AR_OK;
   }

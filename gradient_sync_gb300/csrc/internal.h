@@ -63,6 +63,7 @@ struct ar_plan {
   ar_stats stats;
   int64_t ws_stride;  // fp32 elements per rank in the workspace (multiple of 64)
   bool small = false; // step plan run whole in one CTA (one launch)
+  bool small_smem = false;  // ... with its buffers in shared memory
   mutable ar::DeviceTag last_device;
 };
 
@@ -107,6 +108,22 @@ struct SmallXfer {
   int32_t flat;     // elements of the step's earlier transfers
 };
 
+// One piece of a step run on chip (small_steps_smem_kernel): the byte
+// offsets, in the kernel's shared memory, of element `lo` of each operand,
+// the element count and the operation's options. The host resolves the
+// ranks, spaces and types once, so a warp reads one entry per piece.
+struct SmemPiece {
+  uint32_t x, y, x2, d, d2;  // sources, destination, exchange partner
+  uint16_t len;              // elements, at most kSmallPiece
+  uint8_t flags;             // kPiece* below
+  uint8_t pad;
+};
+enum : uint8_t {
+  kPieceX32 = 1, kPieceY32 = 2, kPieceX2_32 = 4, kPieceD32 = 8,  // operand is fp32 (else bf16)
+  kPieceTwo = 16, kPiecePair = 32, kPieceFin = 64                 // second source, exchange, scale
+};
+static_assert(sizeof(SmemPiece) == sizeof(SmallXfer), "the two tables share storage");
+
 constexpr int kMaxSmallXfers = 1024;
 constexpr int kMaxSmallSteps = 256;
 // A step plan runs in one CTA when its table fits and no step moves more
@@ -117,6 +134,15 @@ constexpr int kMaxSmallSteps = 256;
 // step and more the one-CTA path was slower (ring at 4096 per rank: 98 us
 // against about 50), so those plans keep one kernel per step.
 constexpr int64_t kSmallStepElems = 2048;
+// Such a plan runs on chip when its buffers fit in shared memory beside the
+// transfer table: 8 bytes per element and rank (input and output copies,
+// plus fp32 partials for bf16), up to this many bytes.
+// On chip the table holds pieces of at most kSmallPiece elements (one warp
+// each) instead of whole transfers, and the ranks' rows are copied as 4-byte
+// words, so count * element size must be a multiple of 4.
+constexpr int64_t kSmallSmemDataBytes = 160 * 1024;
+constexpr int kSmallPiece = 128;
+inline int64_t small_smem_data_bytes(int n_ranks, int64_t count) { return 8 * int64_t(n_ranks) * count; }
 
 struct SmallParams {
   void* raw[AR_MAX_RANKS];
@@ -125,10 +151,19 @@ struct SmallParams {
   int64_t ws_stride;
   float scale;
   int n_steps;
+  // On chip (small_steps_smem_kernel): the ranks' elements, and which ranks
+  // run in place (bit r: res[r] is raw[r]).
+  int32_t n_ranks, count;
+  uint64_t in_place;
+  int32_t vec16;  // every buffer 16-byte aligned and count * element size a multiple of 16
   int32_t step_start[kMaxSmallSteps + 1];  // first transfer of each step in x[]
   int32_t step_elems[kMaxSmallSteps];      // elements of each step, all transfers
   uint8_t step_op[kMaxSmallSteps];         // StepOp of each step
-  SmallXfer x[kMaxSmallXfers];
+  union {
+    SmallXfer x[kMaxSmallXfers];   // small_steps_kernel
+    SmemPiece px[kMaxSmallXfers];  // small_steps_smem_kernel
+  };
+  int32_t threads;  // small_steps_smem_kernel: the CTA's threads (32 per piece of the widest step)
 };
 static_assert(sizeof(SmallParams) <= 32764, "kernel parameter limit");
 
@@ -193,6 +228,9 @@ cudaError_t launch_step(const StepParams& p, ar_dtype dtype, StepOp op, int tota
 cudaError_t launch_fused(const FusedParams& p, ar_dtype dtype, int sm_budget, cudaStream_t stream);
 // All steps of a small plan in one CTA, a block barrier between steps.
 cudaError_t launch_small_steps(const SmallParams& p, ar_dtype dtype, cudaStream_t stream);
+// The same schedule with the buffers copied to shared memory first and every
+// step run there (p.n_ranks, p.count, p.in_place set; the data fit).
+cudaError_t launch_small_steps_smem(const SmallParams& p, ar_dtype dtype, cudaStream_t stream);
 // Register pipeline: elements per vector (v8: 32-byte vectors, bucket kernel
 // only, N > 4 and every pointer 32-byte aligned) and per tile.
 int fused_vec_elems(ar_dtype dtype, bool v8);

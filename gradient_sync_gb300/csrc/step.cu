@@ -17,6 +17,8 @@
 // in place. An exchange (`pair`: both partners receive the same sum, as in
 // recursive doubling) reads both copies of an element and writes both from
 // the same thread, so it is safe in place too.
+#include <atomic>
+
 #include "common.cuh"
 
 namespace ar {
@@ -358,6 +360,180 @@ __global__ void __launch_bounds__(kSmallThreads) small_steps_kernel(const __grid
   }
 }
 
+// The same schedule on chip. A step's time above is mostly a round trip to
+// the L2 (a thread reads what another thread stored a step earlier), the
+// per-element search for its transfer, and the barrier. Here the CTA first
+// copies every rank's input (and the output of ranks that run out of place)
+// into shared memory, runs every step there with the same per-element
+// operations and the same roundings (a bf16 space holds bf16 values, the
+// partials fp32), and finally writes every rank's output back. The spaces
+// alias as they do in memory: a rank that runs in place has one copy for its
+// input and output, and fp32 partials are the output itself. The host cuts
+// the transfers into pieces of at most kSmallPiece elements and resolves
+// each piece's operands to shared-memory offsets; a warp takes whole pieces
+// (lane l: elements l, l + 32, ...), so no element searches for its transfer
+// and a piece is one table read. The CTA has one warp per piece of the
+// widest step (a block barrier costs less with fewer warps).
+//
+// Layout of the dynamic shared memory (the host computes the same offsets):
+//   [0, T)             the pieces, T = their bytes rounded up to 16
+//   [T, T + 4NL)       bf16 only: the fp32 partials of the N ranks
+//   then               the N ranks' inputs (NL elements of the buffers' type)
+//   then               the N ranks' outputs, for the ranks out of place
+
+__device__ __forceinline__ float smem_ld(const char* base, uint32_t off, int k, bool f32) {
+  if (f32) return *reinterpret_cast<const float*>(base + off + 4 * k);
+  return bf16_to_f32(*reinterpret_cast<const uint16_t*>(base + off + 2 * k));
+}
+__device__ __forceinline__ void smem_st(char* base, uint32_t off, int k, bool f32, float v) {
+  if (f32)
+    *reinterpret_cast<float*>(base + off + 4 * k) = v;
+  else
+    *reinterpret_cast<uint16_t*>(base + off + 2 * k) = f32_to_bf16(v);
+}
+
+// Copy `words` 4-byte words or (vec) 16-byte vectors of every rank between
+// memory and shared memory, all of a thread's loads issued before its stores.
+// Rank r's words are [r * words, (r + 1) * words) of the shared copy; ranks
+// whose bit is set in `skip` are left out.
+template <class W, bool TO_SMEM>
+__device__ __forceinline__ void copy_ranks(char* const* mem, const uint64_t skip, char* smem_base, int n, int words) {
+  constexpr int kU = 8;
+  const int total = n * words, step = int(blockDim.x);
+  for (int i0 = threadIdx.x; i0 < total; i0 += step * kU) {
+    W v[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = i0 + u * step;
+      if (i >= total) continue;
+      const int r = i / words;
+      if ((skip >> r) & 1) continue;
+      W* m = reinterpret_cast<W*>(mem[r]) + (i - r * words);
+      W* sm = reinterpret_cast<W*>(smem_base) + i;
+      v[u] = TO_SMEM ? *m : *sm;
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = i0 + u * step;
+      if (i >= total) continue;
+      const int r = i / words;
+      if ((skip >> r) & 1) continue;
+      W* m = reinterpret_cast<W*>(mem[r]) + (i - r * words);
+      W* sm = reinterpret_cast<W*>(smem_base) + i;
+      if (TO_SMEM)
+        *sm = v[u];
+      else
+        *m = v[u];
+    }
+  }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kSmallThreads) small_steps_smem_kernel(const __grid_constant__ SmallParams p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  char* const base = reinterpret_cast<char*>(smem);
+  constexpr int esz = BF16 ? 2 : 4;
+  const int n = p.n_ranks, L = p.count, nt = int(blockDim.x);
+  const int n_x = p.step_start[p.n_steps];
+  const SmemPiece* tab = reinterpret_cast<const SmemPiece*>(smem);
+  const int tab_bytes = (n_x * int(sizeof(SmemPiece)) + 15) / 16 * 16;
+  char* const raw_s = base + tab_bytes + (BF16 ? n * L * 4 : 0);
+  char* const res_s = raw_s + n * L * esz;
+  // The table and the steps' starts and ops in shared memory: a parameter
+  // read at an index that changes every step can miss the constant cache.
+  __shared__ int32_t s_start[kMaxSmallSteps + 1];
+  __shared__ uint8_t s_op[kMaxSmallSteps];
+  {
+    const int words = n_x * int(sizeof(SmemPiece) / 4);
+    const uint32_t* from = reinterpret_cast<const uint32_t*>(p.px);
+    uint32_t* to = reinterpret_cast<uint32_t*>(smem);
+    for (int i = threadIdx.x; i < words; i += nt) to[i] = from[i];
+    for (int i = threadIdx.x; i <= p.n_steps; i += nt) s_start[i] = p.step_start[i];
+    for (int i = threadIdx.x; i < p.n_steps; i += nt) s_op[i] = p.step_op[i];
+  }
+  grid_dependency_wait();
+  grid_dependents_launch();
+  // every rank's input, and the current output of the ranks out of place
+  // (elements a plan does not write keep their value on the way back)
+  const int bytes = L * esz;  // a multiple of 4 (the host checks), of 16 with vec16
+  char* const* raw = reinterpret_cast<char* const*>(p.raw);
+  char* const* res = reinterpret_cast<char* const*>(p.res);
+  if (p.vec16) {
+    copy_ranks<uint4, true>(raw, 0, raw_s, n, bytes / 16);
+    copy_ranks<uint4, true>(res, p.in_place, res_s, n, bytes / 16);
+  } else {
+    copy_ranks<uint32_t, true>(raw, 0, raw_s, n, bytes / 4);
+    copy_ranks<uint32_t, true>(res, p.in_place, res_s, n, bytes / 4);
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, warps = nt >> 5;
+  constexpr int kPer = kSmallPiece / 32;  // elements per lane of a piece
+  const int n_steps = p.n_steps;
+  const float scale = p.scale;
+  for (int s = 0; s < n_steps; ++s) {
+    const int x1 = s_start[s + 1];
+    const int op = s_op[s];
+    for (int x = s_start[s] + warp; x < x1; x += warps) {
+      const SmemPiece t = tab[x];  // the same piece for the whole warp
+      const bool x32 = !BF16 || (t.flags & kPieceX32), d32 = !BF16 || (t.flags & kPieceD32);
+      if (op == OP_COPY) {  // same type on both sides: move the bits
+        uint32_t bits[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int k = lane + 32 * u;
+          if (k < t.len)
+            bits[u] = x32 ? *reinterpret_cast<const uint32_t*>(base + t.x + 4 * k)
+                          : uint32_t(*reinterpret_cast<const uint16_t*>(base + t.x + 2 * k));
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int k = lane + 32 * u;
+          if (k >= t.len) continue;
+          if (d32)
+            *reinterpret_cast<uint32_t*>(base + t.d + 4 * k) = bits[u];
+          else
+            *reinterpret_cast<uint16_t*>(base + t.d + 2 * k) = uint16_t(bits[u]);
+        }
+        continue;
+      }
+      const bool add = op == OP_ADD;
+      const bool two = add && (t.flags & kPieceTwo), pair = add && (t.flags & kPiecePair);
+      const bool fin = t.flags & kPieceFin;
+      const bool y32 = !BF16 || (t.flags & kPieceY32), x2_32 = !BF16 || (t.flags & kPieceX2_32);
+      float v[kPer];
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int k = lane + 32 * u;
+        if (k >= t.len) continue;
+        v[u] = smem_ld(base, t.x, k, x32);
+        if (add) {
+          v[u] = fadd(v[u], smem_ld(base, t.y, k, y32));
+          if (two) v[u] = fadd(v[u], smem_ld(base, t.x2, k, x2_32));
+        }
+        if (fin) v[u] = fmul(v[u], scale);
+      }
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int k = lane + 32 * u;
+        if (k >= t.len) continue;
+        smem_st(base, t.d, k, d32, v[u]);
+        if (pair) smem_st(base, t.d2, k, d32, v[u]);
+      }
+    }
+    __syncthreads();  // the step boundary
+  }
+  // every rank's output back to memory: from its own copy for the ranks out
+  // of place, from the shared input copy for the ranks in place
+  const uint64_t all = n == 64 ? ~uint64_t(0) : (uint64_t(1) << n) - 1;
+  if (p.vec16) {
+    copy_ranks<uint4, false>(res, p.in_place, res_s, n, bytes / 16);
+    copy_ranks<uint4, false>(raw, all & ~p.in_place, raw_s, n, bytes / 16);
+  } else {
+    copy_ranks<uint32_t, false>(res, p.in_place, res_s, n, bytes / 4);
+    copy_ranks<uint32_t, false>(raw, all & ~p.in_place, raw_s, n, bytes / 4);
+  }
+}
+
 template <bool BF16, bool V8>
 cudaError_t launch_op(const StepParams& p, StepOp op, int tiles, bool pdl, int sm_budget, cudaStream_t stream) {
   void (*k)(StepParams) = op == OP_ADD ? step_kernel<BF16, OP_ADD, V8>
@@ -383,6 +559,36 @@ cudaError_t launch_small_steps(const SmallParams& p, ar_dtype dtype, cudaStream_
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1);
   cfg.blockDim = dim3(kSmallThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, p);
+}
+
+cudaError_t launch_small_steps_smem(const SmallParams& p, ar_dtype dtype, cudaStream_t stream) {
+  void (*k)(SmallParams) = dtype == AR_BF16 ? small_steps_smem_kernel<true> : small_steps_smem_kernel<false>;
+  const int64_t tab = (int64_t(p.step_start[p.n_steps]) * int64_t(sizeof(SmemPiece)) + 15) / 16 * 16;
+  const int64_t bytes = tab + small_smem_data_bytes(p.n_ranks, p.count);
+  // Allow the largest table and data once per device and kernel.
+  static std::atomic<uint64_t> allowed[2];
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const uint64_t bit = uint64_t(1) << (dev & 63);
+  std::atomic<uint64_t>& mask = allowed[dtype == AR_BF16 ? 1 : 0];
+  if ((mask.load(std::memory_order_acquire) & bit) == 0) {
+    const int most = int(int64_t(kMaxSmallXfers) * int64_t(sizeof(SmemPiece)) + kSmallSmemDataBytes);
+    err = cudaFuncSetAttribute(reinterpret_cast<const void*>(k), cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (err != cudaSuccess) return err;
+    mask.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(p.threads);
+  cfg.dynamicSmemBytes = size_t(bytes);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -101,12 +101,21 @@ typedef enum {
  * resolves to AR_FUSED. */
 #define AR_DEVICE_ALPHA_S 1.5e-6 /* per dependent kernel launch, graph-replayed */
 #define AR_DEVICE_BW 6.0e12      /* bytes/s of algorithmic HBM traffic */
-#define AR_DEVICE_CTA_STEP_S 1.0e-6 /* per step of a plan run whole in one CTA
-                                       (ar_stats.launches == 1 with more than
-                                       one step): a block barrier and the
-                                       step's memory round trip, measured on
-                                       GB300 (16-rank ring at 1 KiB: 30.7 us
-                                       for 30 steps) */
+#define AR_DEVICE_CTA_STEP_S 0.28e-6 /* per step of a plan run whole in one
+                                        CTA (ar_stats.launches == 1 with more
+                                        than one step) with its buffers copied
+                                        to shared memory (8 bytes per element
+                                        and rank fit in 160 KiB): a block
+                                        barrier and the step's shared-memory
+                                        accesses, measured on GB300 (device
+                                        time: 16-rank ring at 1 KiB 13.2 us
+                                        for 30 steps, Rabenseifner 7.2 us for
+                                        8; the rest is the launch and the
+                                        copies in and out) */
+#define AR_DEVICE_CTA_STEP_MEM_S 0.75e-6 /* the same for a one-CTA plan whose
+                                            buffers stay in memory: a block
+                                            barrier and the step's round trip
+                                            to the L2 */
 
 /* Per-element summation order of AR_FUSED. (For AR_REDUCE_SCATTER,
  * AR_ORDER_RING is the order of its ring, which folds chunk c from rank c+1:
@@ -193,7 +202,15 @@ typedef struct {
                                   step plan whose every step moves at most
                                   2048 elements (its whole schedule runs in
                                   one CTA, a block barrier between steps,
-                                  with the same results) */
+                                  with the same results; when 8 bytes per
+                                  element and rank fit in 160 KiB and every
+                                  buffer is 4-byte aligned with count times
+                                  the element size a multiple of 4, the
+                                  buffers are copied to shared memory, every
+                                  step runs there and the results are
+                                  written back). ar_bind keeps such a plan's
+                                  launch parameters and ar_execute_bound
+                                  launches it directly. */
   size_t bytes_sent_per_rank;  /* largest per-rank send volume of the
                                   schedule, in bytes of the payload type */
   size_t hbm_bytes;            /* algorithmic HBM bytes of one ar_execute:
@@ -297,8 +314,10 @@ ar_status ar_execute_noalloc(const ar_plan_t* plan, void* const* bufs, void* con
  * records every launch of one ar_execute(plan, bufs, outs, workspace) into a
  * CUDA graph, which ar_execute_bound replays with one host call: 2(N-1) ring
  * steps cost one graph launch on the host instead of 2(N-1) kernel launches.
- * A single-pass (AR_FUSED) plan is one kernel, launched directly without the
- * argument checks. The results are those of ar_execute, bit for bit. */
+ * A single-pass (AR_FUSED) plan, and a step plan that runs whole in one CTA
+ * (ar_stats.launches == 1), are one kernel, launched directly without the
+ * argument checks (the one-CTA plan's launch parameters are built here,
+ * once). The results are those of ar_execute, bit for bit. */
 typedef struct ar_bound ar_bound_t;
 
 /* Bind `plan` to its buffers (arguments and errors as ar_execute; nothing is
@@ -307,7 +326,9 @@ typedef struct ar_bound ar_bound_t;
  * to the device current at this call. count == 0 makes no CUDA call. Errors:
  * AR_EINVAL (as ar_execute, or NULL out), AR_ENOMEM, AR_ECUDA (a CUDA call
  * failed while recording; nothing is left behind). Recording a step plan
- * creates CUDA graph objects (driver-managed); no buffer is allocated. */
+ * creates CUDA graph objects (driver-managed); no device buffer is
+ * allocated (a one-CTA plan keeps its launch parameters, about 29 KB, in
+ * host memory). */
 ar_status ar_bind(const ar_plan_t* plan, void* const* bufs, void* const* outs, void* workspace,
                   ar_bound_t** out);
 
@@ -340,7 +361,8 @@ typedef struct {
   int shared_memory;     /* 1: all ranks share one memory of bandwidth bw_local
                             (virtual ranks on one GPU): every kernel launch of
                             the plan costs alpha, every step of a plan run
-                            whole in one CTA AR_DEVICE_CTA_STEP_S, and the
+                            whole in one CTA AR_DEVICE_CTA_STEP_S (buffers on
+                            chip) or AR_DEVICE_CTA_STEP_MEM_S, and the
                             plan's algorithmic memory bytes cost
                             bytes / bw_local */
 } ar_fabric;

@@ -129,11 +129,19 @@ def test_device_model_of_one_cta_plans(g):
         assert st["launches"] == 1 and st["steps"] > 1
         assert g.ar_plan_predict(p, dev) == pytest.approx(
             g.AR_DEVICE_ALPHA_S + st["steps"] * g.AR_DEVICE_CTA_STEP_S + st["hbm_bytes"] / g.AR_DEVICE_BW, rel=1e-12)
-    # measured on GB300, bound: ring 30.7 us, Rabenseifner 12.3 us (within the
-    # ~3 us of launch and host time the model leaves out)
+    # measured on GB300 (device time, buffers on chip): ring 13.2 us,
+    # Rabenseifner 7.2 us, of which about 4 us are the launch and the copies
+    # in and out that the model leaves out
     ring = g.ar_plan_predict(g.ar_plan(16, 256, "f32", "ring"), dev)
     rab = g.ar_plan_predict(g.ar_plan(16, 256, "f32", "rabenseifner"), dev)
-    assert 28e-6 < ring < 34e-6 and 8e-6 < rab < 12.5e-6
+    assert 8e-6 < ring < 11e-6 and 3e-6 < rab < 4.5e-6
+    # 16 x 2048 fp32 does not fit on chip (8 bytes per element and rank over
+    # 160 KiB): its one-CTA steps are priced at the in-memory rate
+    p = g.ar_plan(16, 2048, "f32", "ring")
+    st = p.stats
+    assert st["launches"] == 1
+    assert g.ar_plan_predict(p, dev) == pytest.approx(
+        g.AR_DEVICE_ALPHA_S + st["steps"] * g.AR_DEVICE_CTA_STEP_MEM_S + st["hbm_bytes"] / g.AR_DEVICE_BW, rel=1e-12)
     # still the single pass for AR_AUTO at any size
     assert g.ar_select(16, 256, dev)[0] == "fused"
 

@@ -8,7 +8,7 @@ import torch
 
 import workloads
 from _gpu import assert_bits_equal, expected, to_device, to_host, widened
-from oracle import numerics
+from oracle import numerics, schedules
 
 pytestmark = pytest.mark.gpu
 
@@ -380,3 +380,49 @@ def test_one_cta_and_per_step_executors_agree(g, algo, N, G, dims, dtype):
             for r in range(N):
                 got = to_host((outs if out_of_place else bufs)[r], dtype)
                 assert_bits_equal(got, want, f"{algo} L={L} rank {r} {'out' if out_of_place else 'in'}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("algo,coll,N,G,L", [
+    ("ring", "allreduce", 16, 0, 256), ("ring", "allreduce", 16, 0, 2048),
+    ("ring", "allreduce", 16, 0, 1280), ("ring", "allreduce", 16, 0, 1281), ("rabenseifner", "allreduce", 64, 0, 64),
+    ("rabenseifner", "allreduce", 8, 0, 100), ("hier", "allreduce", 8, 4, 300), ("dbtree", "allreduce", 6, 0, 77),
+    ("ring", "reduce_scatter", 16, 0, 1000), ("ring", "allgather", 16, 0, 999)])
+def test_one_cta_plans_on_and_off_chip(g, dtype, algo, coll, N, G, L):
+    """Plans whose steps all fit one CTA run with their buffers in shared
+    memory when 8 bytes per element and rank fit in 160 KiB (16 x 1280
+    elements does, 16 x 1281 does not), else from global memory. Either way:
+    the oracle's bits on every rank (a reduce-scatter: in the chunk each
+    rank owns), with even ranks in place and odd ranks out of place in one
+    call, and the odd ranks' inputs untouched."""
+    from oracle.chunks import chunk_bounds
+
+    x = workloads.all_ranks(workloads.small_spec(N, L, dtype, "normal", seed=N * 1000 + L))
+    plan = g.ar_plan(N, L, dtype, algo, group_size=G, scale=0.5 if coll == "allreduce" else 1.0, collective=coll)
+    assert plan.stats["launches"] == 1
+    devs = [to_device(x[r], dtype) for r in range(N)]
+    outs = [devs[r] if r % 2 == 0 else torch.full_like(devs[r], 7.0) for r in range(N)]
+    ws = g.workspace_for(plan)
+    g.ar_execute(plan, devs, outs=outs, workspace=ws)
+    torch.cuda.synchronize()
+    xf = widened(x, dtype)
+    b = chunk_bounds(L, N)
+    if coll == "allreduce":
+        want = expected(algo, "ring", x, dtype, group_size=G, scale=0.5)
+        rows = [want] * N
+    elif coll == "reduce_scatter":
+        finish = schedules.finish_bf16(1.0) if dtype == "bf16" else None
+        out, _ = schedules.ring_reduce_scatter(xf, finish=finish)
+        rows = [numerics.f32_to_bf16_rne(out[r]) if dtype == "bf16" else out[r] for r in range(N)]
+    else:
+        out, _ = schedules.ring_allgather(x if dtype == "f32" else x)
+        rows = [out[r] for r in range(N)]
+    for r in range(N):
+        got = to_host(outs[r], dtype)
+        if coll == "reduce_scatter":
+            seg = slice(b[r], b[r + 1])
+            assert_bits_equal(got[seg], rows[r][seg], f"rank {r}")  # the rest is unspecified
+        else:
+            assert_bits_equal(got, rows[r], f"rank {r}")
+        if r % 2:
+            assert_bits_equal(to_host(devs[r], dtype), x[r], f"input of rank {r}")
