@@ -289,7 +289,14 @@ __device__ __forceinline__ void tma_pipeline(Src& src, int n, float scale, const
         for (int pos = 0; pos < n; ++pos) bulk_load(const_cast<char*>(slot[s][pos]), src_ptr[pos] + lo * ES, bytes, &full[s]);
         ++it;
       }
-      if (*abort) {  // let the loads already issued land before shared memory goes away
+      if (*abort) {
+        // Let the loads already issued land before shared memory goes away:
+        // the last S issued are the only ones that can be in flight (a stage
+        // is refilled only after its previous load completed and was
+        // consumed), and a wait on a phase that already completed returns at
+        // once. A bulk load reads device memory the host validated, so it
+        // completes in microseconds; each poll may suspend the thread in
+        // hardware, so 2^16 polls per stage allow far longer than that.
         for (int k = it > S ? it - S : 0; k < it; ++k) {
           volatile int never = 0;
           mbar_wait(&full[k % S], uint32_t(k / S) & 1u, 1u << 16, &never);
@@ -484,9 +491,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 // lanes. Every wait is bounded as in the all-reduce pipeline.
 // ---------------------------------------------------------------------------
 // Shape: 3 stages of 32 KiB, 2 CTAs per SM. Measured on GB300 (16 ranks x 192
-// MiB fp32): 0.89 of HBM against 0.86 for the register pipeline's all-gather;
-// 4 x 16 KiB gave 0.87, 4 x 8 KiB with 4 CTAs 0.86, 2 x 32 KiB 0.90 at 16
-// ranks but 0.87 at 64.
+// MiB fp32, one call per timing): 0.89 of HBM against 0.86 for the register
+// pipeline's all-gather; 4 x 16 KiB gave 0.87, 4 x 8 KiB with 4 CTAs 0.86,
+// 2 x 32 KiB 0.90 at 16 ranks but 0.87 at 64. Refilling a stage one store
+// group later (two tiles' stores in flight) measured, calls back to back,
+// 0.941 -> 0.944 at 16 ranks and 0.86 -> 0.87 at 8; starting each tile's
+// stores at a rank that moves with the tile (AR_AGB_ROTATE) measured the
+// same as rank order, so it is off.
 #ifndef AR_AGB_STAGES
 #define AR_AGB_STAGES 3
 #endif
@@ -495,6 +506,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 #endif
 #ifndef AR_AGB_CTAS
 #define AR_AGB_CTAS 2
+#endif
+#ifndef AR_AGB_ROTATE
+#define AR_AGB_ROTATE 0
 #endif
 constexpr int kAgbThreads = 32;
 static_assert(AR_AGB_STAGES >= 1 && AR_AGB_STAGES <= kMaxStages, "stage count");
@@ -586,36 +600,68 @@ __global__ void __launch_bounds__(kAgbThreads)
     bulk_load(smem + size_t(s) * T, static_cast<const char*>(p.in[tile_seg[s]]) + tile_lo[s] * ES, bytes, &full[s]);
   };
 
+  // `live`: stages holding a tile whose stores are not issued yet; bit s of
+  // `inflight`: stage s has a load issued and not yet seen complete. A
+  // stage's stores are issued as soon as its load lands; the stage is
+  // refilled one tile later, once those stores have read it (the store group
+  // before the newest has completed its reads), so the stores of two tiles
+  // are in flight at once.
   int live = 0;
+  uint32_t inflight = 0;
   for (int s = 0; s < S; ++s) {
     if (next(s)) {
       load(s);
       ++live;
+      inflight |= 1u << s;
     }
   }
   uint32_t parity = 0;  // bit s: the parity of stage s's next completion
-  for (int it = 0; live > 0; ++it) {
-    const int s = it % S;
-    if (tile_elems[s] < 0) continue;
-    if (!mbar_wait(&full[s], (parity >> s) & 1u, kWaitPolls, abort)) break;
-    parity ^= 1u << s;
-    const uint32_t bytes = uint32_t(tile_elems[s] * ES);
-    const void* stage = smem + size_t(s) * T;
-    const void* owner = p.in[tile_seg[s]];
-    for (int r = 0; r < n; ++r)
-      if (p.out[r] != owner) bulk_store(static_cast<char*>(p.out[r]) + tile_lo[s] * ES, stage, bytes);
-    bulk_commit();
-    bulk_wait_read<0>();  // the stores have read the stage: it can be refilled
-    --live;
+  int pending = -1;     // the stage whose stores were issued last, not refilled yet
+  auto refill = [&](int s) {
     if (next(s)) {
       load(s);
       ++live;
+      inflight |= 1u << s;
+    } else {
+      tile_elems[s] = -1;
     }
+  };
+  for (int it = 0; live > 0 || pending >= 0;) {
+    if (live == 0) {  // nothing else to store: the last stage's refill cannot wait for a later tile
+      bulk_wait_read<0>();
+      refill(pending);
+      pending = -1;
+      continue;
+    }
+    const int s = it++ % S;
+    if (tile_elems[s] < 0 || s == pending) continue;
+    if (!mbar_wait(&full[s], (parity >> s) & 1u, kWaitPolls, abort)) break;
+    parity ^= 1u << s;
+    inflight &= ~(1u << s);
+    const uint32_t bytes = uint32_t(tile_elems[s] * ES);
+    const void* stage = smem + size_t(s) * T;
+    const void* owner = p.in[tile_seg[s]];
+    // the N ranks in turn from a rank that moves with the tile, so that the
+    // CTAs' stores spread over the destination buffers
+    const int r0 = AR_AGB_ROTATE ? int(tile_lo[s] / te % n) : 0;
+    for (int i = 0, r = r0; i < n; ++i, r = r + 1 < n ? r + 1 : 0)
+      if (p.out[r] != owner) bulk_store(static_cast<char*>(p.out[r]) + tile_lo[s] * ES, stage, bytes);
+    bulk_commit();
+    --live;
+    if (pending >= 0) {
+      bulk_wait_read<1>();  // the stores before this tile's have read their stage
+      refill(pending);
+    }
+    pending = s;
   }
-  if (*abort) {  // let every load still in flight land before shared memory goes away
+  if (*abort) {
+    // Let every load still in flight land before shared memory goes away. A
+    // bulk load reads device memory the host validated, so it completes in
+    // microseconds; each poll of the wait may suspend the thread in hardware,
+    // so 2^16 polls per stage allow far longer than any such load takes.
     volatile int never = 0;
     for (int s = 0; s < S; ++s)
-      if (tile_elems[s] >= 0) mbar_wait(&full[s], (parity >> s) & 1u, 1u << 16, &never);
+      if ((inflight >> s) & 1u) mbar_wait(&full[s], (parity >> s) & 1u, 1u << 16, &never);
   }
   bulk_wait_all();  // every store has completed before the CTA exits
 }
