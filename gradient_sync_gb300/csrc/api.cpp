@@ -579,7 +579,7 @@ ar_status execute_fused(const ar_plan_t* p, void* const* bufs, void* const* outs
     fused_tiling(d, fp, tile_bytes / int64_t(esize(d.dtype)), d.dtype == AR_BF16 ? 8 : 4);
     return from_cuda(launch_fused_tma(fp, d.dtype, stages, tile_bytes, d.sm_budget, stream));
   }
-  fused_tiling(d, fp, fused_tile_elems(d.dtype, d.n_ranks, d.order, d.collective, false),
+  fused_tiling(d, fp, fused_tile_elems(d.dtype, d.n_ranks, d.order, d.collective, false, budgeted(d.sm_budget)),
                fused_vec_elems(d.dtype, false));
   return from_cuda(launch_fused(fp, d.dtype, d.sm_budget, stream));
 }
@@ -1359,7 +1359,8 @@ ar_status ar_bucket_allreduce(int n_ranks, void* const* tensors, const size_t* c
   if (tma && !tma_shape(N, stages, tile_bytes)) return AR_EUNSUPPORTED;
   s = status_guard(nullptr);
   if (s != AR_OK) return s;
-  const int64_t tile = tma ? tile_bytes / int64_t(esize(dtype)) : fused_tile_elems(dtype, N, AR_ORDER_RING, AR_ALLREDUCE, v8);
+  const int64_t tile = tma ? tile_bytes / int64_t(esize(dtype))
+                           : fused_tile_elems(dtype, N, AR_ORDER_RING, AR_ALLREDUCE, v8, budgeted(sm_budget));
   const int max_group = std::min(AR_MAX_BUCKET_TENSORS, kMaxBucketPtrs / N);
   static thread_local BucketFusedParams bp;
   std::memset(&bp, 0, sizeof(bp));

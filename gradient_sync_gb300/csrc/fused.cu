@@ -353,17 +353,21 @@ cudaError_t launch_persistent(void (*kernel)(P), const P& p, int64_t tiles, int 
 // (0.85 with 4 vectors; 8 measured the same).
 constexpr int kRsNB = 8, kRsVPT = 2, kAgVPT = 4;
 
-int fused_vpt(int n, int order, int collective) {
+// `deep` (a budgeted launch, see budgeted()): the all-reduce in ring, rank or
+// hierarchical order over more than 4 ranks takes 2 vectors per thread with
+// 8 ranks per batch, 16 loads in flight per thread.
+int fused_vpt(int n, int order, int collective, bool deep) {
   if (collective == AR_ALLGATHER) return kAgVPT;
   if (collective == AR_REDUCE_SCATTER && order != AR_ORDER_TREE && n > 4) return kRsVPT;
   if (order == AR_ORDER_TREE) return 1;
+  if (deep && n > 4) return 2;
   return n <= 2 ? 4 : n <= 4 ? 2 : 1;
 }
 
 int fused_vec_elems(ar_dtype dtype, bool v8) { return (dtype == AR_BF16 ? 8 : 4) * (v8 ? 2 : 1); }
 
-int64_t fused_tile_elems(ar_dtype dtype, int n, int order, int collective, bool v8) {
-  return int64_t(kThreads) * fused_vec_elems(dtype, v8) * (v8 ? 1 : fused_vpt(n, order, collective));
+int64_t fused_tile_elems(ar_dtype dtype, int n, int order, int collective, bool v8, bool deep) {
+  return int64_t(kThreads) * fused_vec_elems(dtype, v8) * (v8 ? 1 : fused_vpt(n, order, collective, deep));
 }
 
 // Every order but the hierarchical one (rotations of the rank list). The
@@ -378,9 +382,11 @@ cudaError_t launch_fused_rot(const FusedParams& p, int64_t tiles, int sm_budget,
                              stream);
   if (p.collective == AR_ALLGATHER)
     return launch_persistent(fused_flat_kernel<BF16, false, kSeqRotated, 1, kAgVPT>, p, tiles, sm_budget, stream);
-  switch (fused_vpt(p.n, p.order, p.collective)) {
+  switch (fused_vpt(p.n, p.order, p.collective, budgeted(sm_budget))) {
     case 4: return launch_persistent(fused_flat_kernel<BF16, false, kSeqRotated, 2, 4>, p, tiles, sm_budget, stream);
-    case 2: return launch_persistent(fused_flat_kernel<BF16, false, kSeqRotated, 4, 2>, p, tiles, sm_budget, stream);
+    case 2:
+      return p.n > 4 ? launch_persistent(fused_flat_kernel<BF16, false, kSeqRotated, 8, 2>, p, tiles, sm_budget, stream)
+                     : launch_persistent(fused_flat_kernel<BF16, false, kSeqRotated, 4, 2>, p, tiles, sm_budget, stream);
     default:
       return p.n > 16 ? launch_persistent(fused_flat_kernel<BF16, false, kSeqRotatedPos, 8, 1>, p, tiles, sm_budget, stream)
                       : launch_persistent(fused_flat_kernel<BF16, false, kSeqRotated, 8, 1>, p, tiles, sm_budget, stream);
@@ -392,9 +398,11 @@ cudaError_t launch_fused_rot(const FusedParams& p, int64_t tiles, int sm_budget,
 template <bool BF16>
 cudaError_t launch_fused_t(const FusedParams& p, int64_t tiles, int sm_budget, cudaStream_t stream) {
   if (p.order == AR_ORDER_HIER && p.collective == AR_ALLREDUCE) {  // the planner allows it for all-reduce only
-    switch (fused_vpt(p.n, p.order, p.collective)) {
+    switch (fused_vpt(p.n, p.order, p.collective, budgeted(sm_budget))) {
       case 4: return launch_persistent(fused_flat_kernel<BF16, false, kSeqWritten, 2, 4>, p, tiles, sm_budget, stream);
-      case 2: return launch_persistent(fused_flat_kernel<BF16, false, kSeqWritten, 4, 2>, p, tiles, sm_budget, stream);
+      case 2:
+        return p.n > 4 ? launch_persistent(fused_flat_kernel<BF16, false, kSeqWritten, 8, 2>, p, tiles, sm_budget, stream)
+                       : launch_persistent(fused_flat_kernel<BF16, false, kSeqWritten, 4, 2>, p, tiles, sm_budget, stream);
       default: return launch_persistent(fused_flat_kernel<BF16, false, kSeqWritten, 8, 1>, p, tiles, sm_budget, stream);
     }
   }
@@ -411,10 +419,18 @@ cudaError_t launch_fused(const FusedParams& p, ar_dtype dtype, int sm_budget, cu
 // bytes, so a batch holds half as many ranks (the same bytes in flight).
 template <bool BF16>
 cudaError_t launch_bucket_t(const BucketFusedParams& p, int64_t tiles, int sm_budget, bool v8, cudaStream_t stream) {
-  if (v8) return launch_persistent(fused_bucket_kernel<BF16, true, 4, 1>, p, tiles, sm_budget, stream);
-  switch (fused_vpt(p.n, AR_ORDER_RING, AR_ALLREDUCE)) {
+  const bool deep = budgeted(sm_budget);
+  // budgeted: 8 ranks per batch (8 32-byte loads in flight per thread); 6
+  // for bf16, whose 16-element lanes spilled registers at 8
+  constexpr int kDeepNB = BF16 ? 6 : 8;
+  if (v8)
+    return deep ? launch_persistent(fused_bucket_kernel<BF16, true, kDeepNB, 1>, p, tiles, sm_budget, stream)
+                : launch_persistent(fused_bucket_kernel<BF16, true, 4, 1>, p, tiles, sm_budget, stream);
+  switch (fused_vpt(p.n, AR_ORDER_RING, AR_ALLREDUCE, deep)) {
     case 4: return launch_persistent(fused_bucket_kernel<BF16, false, 2, 4>, p, tiles, sm_budget, stream);
-    case 2: return launch_persistent(fused_bucket_kernel<BF16, false, 4, 2>, p, tiles, sm_budget, stream);
+    case 2:
+      return p.n > 4 ? launch_persistent(fused_bucket_kernel<BF16, false, 8, 2>, p, tiles, sm_budget, stream)
+                     : launch_persistent(fused_bucket_kernel<BF16, false, 4, 2>, p, tiles, sm_budget, stream);
     default: return launch_persistent(fused_bucket_kernel<BF16, false, 8, 1>, p, tiles, sm_budget, stream);
   }
 }

@@ -5,6 +5,8 @@
 #include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
+#include <utility>
 #include <vector>
 
 #include <cuda_runtime.h>
@@ -213,6 +215,31 @@ struct CompressParams {
   float scale;                  // multiplies the complete fp32 sum once
 };
 
+// The current device's SM count (cached per device).
+inline int device_sms() {
+  static std::mutex mu;
+  static std::vector<std::pair<int, int>> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (const auto& e : cache)
+      if (e.first == dev) return e.second;
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 1;
+  std::lock_guard<std::mutex> lock(mu);
+  cache.push_back({dev, sms});
+  return sms;
+}
+
+// A launch held to fewer SMs than the GPU has. Its CTAs land on different
+// SMs (the scheduler spreads them), each with the whole SM's memory path to
+// itself, so they run the variants that keep twice the loads in flight per
+// thread: a copy kernel on 64 CTAs measured 4.0 TB/s with 8 16-byte loads in
+// flight per thread and 5.1 TB/s with 16 (GB300, one CTA per SM).
+inline bool budgeted(int sm_budget) { return sm_budget > 0 && sm_budget < device_sms(); }
+
 // ---- launchers (defined in the .cu files) ----
 // Tile sizes the launchers and the host planner agree on (elements).
 constexpr int kThreads = 256;
@@ -234,7 +261,7 @@ cudaError_t launch_small_steps_smem(const SmallParams& p, ar_dtype dtype, cudaSt
 // Register pipeline: elements per vector (v8: 32-byte vectors, bucket kernel
 // only, N > 4 and every pointer 32-byte aligned) and per tile.
 int fused_vec_elems(ar_dtype dtype, bool v8);
-int64_t fused_tile_elems(ar_dtype dtype, int n, int order, int collective, bool v8);
+int64_t fused_tile_elems(ar_dtype dtype, int n, int order, int collective, bool v8, bool deep);
 cudaError_t launch_bucket_fused(const BucketFusedParams& p, ar_dtype dtype, int sm_budget, bool v8, cudaStream_t stream);
 cudaError_t launch_pack(const PackParams& p, ar_dtype dtype, bool unpack, cudaStream_t stream);
 cudaError_t read_device_status(unsigned int* value, bool clear);
