@@ -632,21 +632,22 @@ def bucket_sync(grads, counts, n, path, stream_handle, cap_bytes=25 * MiB):
     return sync, hbm, launches, len(ranges), keep
 
 
-def time_buckets(n=8, path="fused", iters=5, warmup=2, cap_bytes=25 * MiB):
-    """Time one bucketed gradient sync of the 16-layer transformer (hidden 2048,
-    FFN 8192, vocab 32000; bf16 gradients; 25 MiB buckets in reverse layer
-    order; sum scaled by 1/n) on device-filled gradients."""
+def time_buckets(n=8, path="fused", iters=5, warmup=2, cap_bytes=25 * MiB, layers=16):
+    """Time one bucketed gradient sync of the transformer (16 layers unless
+    `layers`; hidden 2048, FFN 8192, vocab 32000; bf16 gradients; 25 MiB
+    buckets in reverse layer order; sum scaled by 1/n) on device-filled
+    gradients."""
     import torch
 
     import workloads
 
-    counts = [c for _, c in workloads.transformer_tensors()]
+    counts = [c for _, c in workloads.transformer_tensors(layers=layers)]
     grads = [[torch.randn(c, device="cuda").to(torch.bfloat16) for c in counts] for _ in range(n)]
     stream = torch.cuda.current_stream()
     sync, hbm, launches, nb, keep = bucket_sync(grads, counts, n, path, int(stream.cuda_stream), cap_bytes)
     ms = event_ms(sync, stream, iters, warmup)
     S = sum(counts) * 2
-    res = {"workload": "bucketed 16-layer transformer", "n": n, "path": path, "buckets": nb,
+    res = {"workload": f"bucketed {layers}-layer transformer", "n": n, "path": path, "buckets": nb,
            "bytes_per_rank": S, "launches": launches}
     res.update(figures(ms, n, S, hbm, measured_peaks()[0]))
     del grads, keep
@@ -1094,7 +1095,7 @@ def run_single(a):
         print(json.dumps(time_compressed(a.n, a.count, a.dtype, a.block, a.compressed, not a.no_ef,
                                          a.iters, a.warmup)))
     elif a.buckets:
-        print(json.dumps(time_buckets(path=a.buckets, iters=a.iters, warmup=min(a.warmup, 3))))
+        print(json.dumps(time_buckets(path=a.buckets, iters=a.iters, warmup=min(a.warmup, 3), layers=a.layers)))
     elif a.overlap:
         from gradient_sync_gb300.overlap import time_overlap
 
@@ -1133,6 +1134,7 @@ def main(argv=None):
     single.add_argument("--graph", action="store_true", help="replay the timed calls from a CUDA graph")
     single.add_argument("--bound", action="store_true", help="bind the plan once (ar_bind) and time ar_execute_bound")
     single.add_argument("--tokens", type=int, default=4096)
+    single.add_argument("--layers", type=int, default=16, help="transformer layers for --buckets")
     single.add_argument("--sm-budget", type=int, default=0)
     single.add_argument("--kernel", default="auto", choices=["auto", "loads", "bulk"])
     single.add_argument("--dims", default="0,0,0", help="torus dimensions X,Y[,Z] for --algo torus")
