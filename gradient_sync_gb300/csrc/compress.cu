@@ -18,13 +18,16 @@
 //
 // Kernels:
 //  compress_kernel              g, e -> codes, scales, e'   (the message of every rank)
-//  compress_pipe_kernel         g -> codes, scales          (the same without feedback)
+//  compress_packed_kernel       g -> codes, scales          (the same without feedback)
 //  compressed_reduce_kernel     codes, scales -> out        (the receiving side)
 //  compressed_allreduce_kernel  g, e -> e', out             (both in one pass; no message
 //                                                            is materialised)
-//  compressed_allreduce_bf16_kernel  g -> out               (the same, bf16 without feedback)
-// The two kernels without feedback keep the loads of the ranks ahead in
-// flight (pipelined loads, below).
+//  compressed_allreduce_bf16_packed_kernel  g -> out        (the same, bf16 without feedback,
+//                                                            even rank counts)
+//  compressed_allreduce_bf16_kernel  g -> out               (the same, odd rank counts)
+// The kernels without feedback keep the loads of the ranks ahead in flight
+// (pipelined loads, below); the packed ones decide codes with fewer
+// instructions (see "bf16 without feedback, packed").
 //
 // Tiling: a CTA of 256 threads takes a tile of 256 * E consecutive elements,
 // the same tile of every rank, E per thread (thread t: elements E*t..E*t+E-1;
@@ -91,12 +94,6 @@ __host__ __device__ constexpr int ept() { return BF16 ? 8 : 4; }
 // The fused pass keeps 8 (16 measured 0.75 against 0.81).
 template <bool BF16>
 __host__ __device__ constexpr int compress_ept() { return BF16 ? 16 : 4; }
-// The compressor without error feedback (pipelined loads) takes 8 elements
-// per thread of either type. Measured at 16 ranks x 192 MiB, block 128, two
-// calls: bf16 0.621 of its bytes (0.615 with 16 per thread), fp32 0.874
-// (0.674 with 4), against 0.513 and 0.729 without the pipeline.
-template <bool BF16>
-__host__ __device__ constexpr int compress_pipe_ept() { return 8; }
 // The reducer reads codes, not gradients: 8 (bf16 out) or 4 (fp32 out) per thread.
 template <bool BF16>
 __host__ __device__ constexpr int reduce_ept() { return BF16 ? 8 : 4; }
@@ -459,45 +456,6 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const __grid_constan
   }
 }
 
-// The compressor without error feedback, with the pipelined loads: the
-// message (codes and scales) of every rank from its gradients alone. (With
-// feedback the pipeline measured +1 % on fp32 and -1 % on bf16 at 16 ranks x
-// 192 MiB, so the batch compressor above serves that case.)
-template <bool BF16>
-__global__ void __launch_bounds__(kThreads) compress_pipe_kernel(const __grid_constant__ CompressParams p) {
-  constexpr int kEPT = compress_pipe_ept<BF16>();
-  constexpr int kTileElems = kEPT * kThreads;
-  using Raw = RawGroup<BF16, kEPT>;
-  __shared__ float wmax[2][kWarps];
-  grid_dependency_wait();
-  grid_dependents_launch();
-  const int64_t n_tiles = (p.count + kTileElems - 1) / kTileElems;
-  const int64_t lane_off = int64_t(kEPT) * threadIdx.x;
-  const int shift = __ffs(p.block) - 1;  // block is a power of two
-  Raw ring[kAhead];
-#pragma unroll
-  for (int k = 0; k < kAhead; ++k) fetch_ahead<BF16, kEPT>(p, n_tiles, lane_off, blockIdx.x, 0, k, ring[k]);
-  int phase = 0;
-  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-    const int64_t e = tile * kTileElems + lane_off;
-#pragma unroll 1
-    for (int r = 0; r < p.n; ++r) {
-      const Raw w = ring[0];
-#pragma unroll
-      for (int k = 0; k + 1 < kAhead; ++k) ring[k] = ring[k + 1];
-      fetch_ahead<BF16, kEPT>(p, n_tiles, lane_off, tile, r, kAhead, ring[kAhead - 1]);
-      float x[kEPT], c[kEPT];
-      widen_raw<BF16, kEPT>(w, x);
-      const float s = block_scale<kEPT, true>(x, p.block, wmax[phase]);
-      phase ^= 1;
-      if (e >= p.count) continue;  // after the block maximum, which every thread joins
-      if ((e & (p.block - 1)) == 0) p.s[r][e >> shift] = s;
-      quant_group<kEPT, true>(x, s, c);
-      store_codes<kEPT>(p.q[r], e, p.count, c);
-    }
-  }
-}
-
 // ---------------------------------------------------------------- reduce
 // The receiving side: for each tile, every rank's codes (kEPT bytes per thread)
 // and the scale of the thread's block are loaded NB ranks at a time, the
@@ -854,6 +812,150 @@ __global__ void __launch_bounds__(kThreads) compressed_allreduce_bf16_packed_ker
   }
 }
 
+// ---------------------------------------------------------------- compressor without feedback, packed
+// The message of every rank (codes, one byte each, and the block scales) with
+// the packed kernel's arithmetic, for either input type and any rank count:
+// the sum RN(x * rc + 1.5 * 2^23) is 1.5 * 2^23 + c, whose bit pattern is
+// that of 1.5 * 2^23 (low byte 0) plus c, so the code's two's-complement
+// byte is the sum's low byte; four codes pack into a word with three byte
+// permutes instead of four float-to-integer conversions. The (tile, rank)
+// pairs of a CTA are walked with a fetch cursor two pairs ahead of the one
+// being quantised, over two load buffers.
+
+// The message of one pair: x holds the 8 values at element e of rank r.
+template <int kLogBlock>
+__device__ __forceinline__ void packed_message(const float (&x)[8], float* wm, int8_t* q, float* sc, int64_t e) {
+  constexpr int kBlock = 1 << kLogBlock;
+  constexpr int kLanes = kBlock >= 32 * 8 ? 32 : kBlock / 8;
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  constexpr float kTie = 0.5f - 0x1p-14f;
+  float m = max3abs(x[0], x[1], x[2]);
+  m = max3abs(m, x[3], x[4]);
+  m = max3abs(m, x[5], x[6]);
+  m = fmaxf(m, fabsf(x[7]));
+  if constexpr (kLanes == 32) {  // full-warp reductions only (see the fused kernel)
+    m = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(m)));
+  } else if constexpr (kLanes == 16) {
+    const bool low = (threadIdx.x & 16) == 0;
+    const unsigned a = __reduce_max_sync(kFull, low ? __float_as_uint(m) : 0u);
+    const unsigned b = __reduce_max_sync(kFull, low ? 0u : __float_as_uint(m));
+    m = __uint_as_float(low ? a : b);
+  } else {
+#pragma unroll
+    for (int o = kLanes / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  }
+  if constexpr (kBlock > 32 * 8) {
+    constexpr int W = kBlock / (32 * 8);
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) wm[warp] = m;
+    __syncthreads();
+    const int w0 = warp & ~(W - 1);
+    m = wm[w0];
+#pragma unroll
+    for (int i = 1; i < W; ++i) m = fmaxf(m, wm[w0 + i]);
+  }
+  const float s = div127(m);
+  uint32_t yb[8];  // bits of 1.5 * 2^23 + code
+  if (s >= 0x1p-126f) {
+    const float rc = rcp_approx(s);
+    const uint64_t RC = pk2(rc, rc), MM = pk2(kMagic, kMagic);
+    float worst = 0.0f, dv[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint64_t X = pk2(x[2 * i], x[2 * i + 1]);
+      const uint64_t Y = fma2(X, RC, MM);           // 1.5 * 2^23 + the nearest integer to x * rc
+      const uint64_t D = fma2(X, RC, sub2(MM, Y));  // RN(x * rc - c)
+      float ylo, yhi;
+      upk2(Y, ylo, yhi);
+      yb[2 * i] = __float_as_uint(ylo);
+      yb[2 * i + 1] = __float_as_uint(yhi);
+      upk2(D, dv[2 * i], dv[2 * i + 1]);
+      worst = max3abs(worst, dv[2 * i], dv[2 * i + 1]);
+    }
+    if (worst >= kTie) {  // a quotient near a tie: the correctly rounded quotient decides
+#pragma unroll
+      for (int w = 0; w < 8; ++w)
+        if (fabsf(dv[w]) >= kTie) yb[w] = __float_as_uint(__fadd_rn(round_int(__fdiv_rn(x[w], s)), kMagic));
+    }
+  } else if (s > 0.0f) {  // a subnormal scale: exact quotients, clamped
+#pragma unroll
+    for (int w = 0; w < 8; ++w)
+      yb[w] = __float_as_uint(__fadd_rn(fminf(fmaxf(round_int(__fdiv_rn(x[w], s)), -127.0f), 127.0f), kMagic));
+  } else {
+#pragma unroll
+    for (int w = 0; w < 8; ++w) yb[w] = __float_as_uint(kMagic);
+  }
+  // low bytes of the 8 words, in element order
+  const uint32_t lo = __byte_perm(__byte_perm(yb[0], yb[1], 0x0040), __byte_perm(yb[2], yb[3], 0x0040), 0x5410);
+  const uint32_t hi = __byte_perm(__byte_perm(yb[4], yb[5], 0x0040), __byte_perm(yb[6], yb[7], 0x0040), 0x5410);
+  __stcs(reinterpret_cast<uint2*>(q + e), make_uint2(lo, hi));
+  if ((e & (kBlock - 1)) == 0) sc[e >> kLogBlock] = s;
+}
+
+template <bool BF16, int kLogBlock>
+__global__ void __launch_bounds__(kThreads) compress_packed_kernel(const __grid_constant__ CompressParams p) {
+  constexpr int kEPT = 8;
+  constexpr int kTileElems = kEPT * kThreads;
+  constexpr int kBlock = 1 << kLogBlock;
+  using Raw = RawGroup<BF16, kEPT>;
+  __shared__ float wmax[2][kWarps];
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int n = p.n;
+  const int64_t n_full = p.count / kTileElems;
+  const int64_t lane_off = int64_t(kEPT) * threadIdx.x;
+  const int64_t stride = int64_t(gridDim.x) * kTileElems;
+  const int64_t end = n_full * kTileElems;
+  // fetch and quantise cursors: element offset and rank of the next pair
+  int64_t f_off = int64_t(blockIdx.x) * kTileElems + lane_off, c_off = f_off;
+  int f_r = 0, c_r = 0;
+  auto fetch = [&](Raw& w) {
+    if (f_off < end) load_raw<BF16, kEPT>(p.g[f_r], f_off, p.count, w);
+    if (++f_r == n) {
+      f_r = 0;
+      f_off += stride;
+    }
+  };
+  Raw X0, X1;
+#pragma unroll
+  for (int i = 0; i < Raw::kWords / 4; ++i) X0.v[i] = X1.v[i] = make_uint4(0u, 0u, 0u, 0u);
+  fetch(X0);
+  fetch(X1);
+  int phase = 0;
+  auto step = [&](Raw& w) {
+    float x[kEPT];
+    widen_raw<BF16, kEPT>(w, x);
+    fetch(w);
+    packed_message<kLogBlock>(x, wmax[phase], p.q[c_r], p.s[c_r], c_off);
+    phase ^= 1;
+    if (++c_r == n) {
+      c_r = 0;
+      c_off += stride;
+    }
+  };
+  while (c_off < end) {  // the same number of steps in every thread of the CTA
+    step(X0);
+    if (c_off >= end) break;
+    step(X1);
+  }
+  // the ragged end: one partial tile, by the last CTA with bounds
+  if (blockIdx.x == gridDim.x - 1 && end < p.count) {
+    const int64_t e = end + lane_off;
+    const int shift = kLogBlock;
+#pragma unroll 1
+    for (int r = 0; r < n; ++r) {
+      float x[kEPT], c[kEPT];
+      load_group<BF16, kEPT>(p.g[r], e, p.count, x);
+      const float s = block_scale<kEPT, true>(x, kBlock, wmax[phase]);
+      phase ^= 1;
+      if (e >= p.count) continue;  // after the block maximum, which every thread joins
+      if ((e & (kBlock - 1)) == 0) p.s[r][e >> shift] = s;
+      quant_group<kEPT, true>(x, s, c);
+      store_codes<kEPT>(p.q[r], e, p.count, c);
+    }
+  }
+}
+
 // Each tile, ranks in order: quantise rank r's block, add its reconstruction
 // to the running sum and store its residual; then write the scaled sum to
 // every rank. No message leaves the registers.
@@ -945,13 +1047,30 @@ int64_t n_tiles(int64_t count, int elems_per_thread) {
 
 }  // namespace
 
+// The packed compressor for each block size, 16 (2^4) to 1024 (2^10).
+template <bool BF16>
+Kern packed_compress_kernel(int block) {
+  switch (block) {
+    case 16: return compress_packed_kernel<BF16, 4>;
+    case 32: return compress_packed_kernel<BF16, 5>;
+    case 64: return compress_packed_kernel<BF16, 6>;
+    case 128: return compress_packed_kernel<BF16, 7>;
+    case 256: return compress_packed_kernel<BF16, 8>;
+    case 512: return compress_packed_kernel<BF16, 9>;
+    case 1024: return compress_packed_kernel<BF16, 10>;
+    default: return nullptr;
+  }
+}
+
 cudaError_t launch_compress(const CompressParams& p, ar_dtype dtype, cudaStream_t stream) {
   const bool bf = dtype == AR_BF16;
-  const Kern k = bf ? (p.ef ? compress_kernel<true, true> : compress_pipe_kernel<true>)
-                    : (p.ef ? compress_kernel<false, true> : compress_pipe_kernel<false>);
-  const int ept = p.ef ? (bf ? compress_ept<true>() : compress_ept<false>())
-                       : (bf ? compress_pipe_ept<true>() : compress_pipe_ept<false>());
-  return launch(k, n_tiles(p.count, ept), p, stream);
+  if (!p.ef) {  // the block is a power of two from 16 to 1024 (checked by the host)
+    const Kern k = bf ? packed_compress_kernel<true>(p.block) : packed_compress_kernel<false>(p.block);
+    if (k == nullptr) return cudaErrorInvalidValue;
+    return launch(k, n_tiles(p.count, 8), p, stream);
+  }
+  const Kern k = bf ? compress_kernel<true, true> : compress_kernel<false, true>;
+  return launch(k, n_tiles(p.count, bf ? compress_ept<true>() : compress_ept<false>()), p, stream);
 }
 
 cudaError_t launch_compressed_reduce(const CompressParams& p, ar_dtype out_dtype, cudaStream_t stream) {
