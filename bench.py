@@ -538,8 +538,9 @@ def time_case(n, count, dtype="f32", algo="fused", order="ring", group_size=0, i
     ws = g.workspace_for(plan)
     st = plan.stats
     nbytes = n * count * esz
-    if reps is None:  # calls per timing: enough work to resolve the time of small cases
-        reps = max(1, min(1000, (256 * MiB) // max(1, 2 * nbytes), 4000 // max(1, st["launches"])))
+    if reps is None:  # calls per timing: enough work to resolve the time of small cases, and
+        # at least 3 back to back, so that one call's launch from Python is not timed alone
+        reps = max(3, min(1000, (256 * MiB) // max(1, 2 * nbytes), 4000 // max(1, st["launches"])))
     stream = torch.cuda.current_stream()
     handle = int(stream.cuda_stream)
 
@@ -645,7 +646,7 @@ def time_buckets(n=8, path="fused", iters=5, warmup=2, cap_bytes=25 * MiB, layer
     grads = [[torch.randn(c, device="cuda").to(torch.bfloat16) for c in counts] for _ in range(n)]
     stream = torch.cuda.current_stream()
     sync, hbm, launches, nb, keep = bucket_sync(grads, counts, n, path, int(stream.cuda_stream), cap_bytes)
-    ms = event_ms(sync, stream, iters, warmup)
+    ms = event_ms(sync, stream, iters, warmup, 2)
     S = sum(counts) * 2
     res = {"workload": f"bucketed {layers}-layer transformer", "n": n, "path": path, "buckets": nb,
            "bytes_per_rank": S, "launches": launches}
@@ -707,7 +708,7 @@ def time_compressed(n=16, count=50_331_648, dtype="f32", block=128, path="fused"
     stream = torch.cuda.current_stream()
     call = compressed_call(grads, outs, block, dtype, res, n, path, int(stream.cuda_stream), codes, scales)
     hbm = compressed_hbm_bytes(n, count, dtype, block, path, ef)
-    reps = max(1, min(200, (256 * MiB) // max(1, hbm)))
+    reps = max(3, min(200, (256 * MiB) // max(1, hbm)))
     ms = event_ms(call, stream, iters, warmup, reps)
     S = count * (4 if dtype == "f32" else 2)
     out = {"workload": "blockwise INT8 compressed all-reduce", "n": n, "count": count, "dtype": dtype,
@@ -770,7 +771,7 @@ def run_workloads(dev, stream, peak, k_big: int, warmup: int):
     handle = int(stream.cuda_stream)
     out, tasks = {}, []
 
-    def plan_path(plan, bufs, outs, n, S, iters, reps=1, ws=None, **extra):
+    def plan_path(plan, bufs, outs, n, S, iters, reps=3, ws=None, **extra):
         ws = g.workspace_for(plan) if ws is None else ws
         st = plan.stats
         ms = event_ms(lambda: g.ar_execute(plan, bufs, outs=outs, workspace=ws, stream=handle), stream,
@@ -804,7 +805,8 @@ def run_workloads(dev, stream, peak, k_big: int, warmup: int):
     out["hier_2x8_bf16"] = {
         "workload": spec.name, "n_ranks": N, "group_size": G, "count_per_rank": L, "bytes_per_rank": S,
         "inputs": "device-filled: torch.randn on the GPU (seed = rank) x 1e-3, rounded to bf16",
-        "timing": f"median of {k_big} calls after {warmup} warm-ups, out of place; traffic > 40x the L2",
+        "timing": f"median of {k_big} timings of 3 calls back to back, after {warmup} warm-ups, out of place; "
+                  "traffic > 40x the L2",
         "paths": {
             "hier_steps": plan_path(g.ar_plan(N, L, "bf16", "hier", group_size=G), bufs, outs, N, S, k_big),
             "fused_hier_order": plan_path(g.ar_plan(N, L, "bf16", "fused", group_size=G, order="hier"), bufs,
@@ -819,7 +821,7 @@ def run_workloads(dev, stream, peak, k_big: int, warmup: int):
     scales = [torch.empty(n_sc, dtype=torch.float32, device=dev) for _ in range(N)]
     for name, path in (("compressed_int8_fused", "fused"), ("compressed_int8_two_calls", "two")):
         fn = compressed_call(bufs, outs, block, "bf16", None, N, path, handle, codes, scales)
-        ms = event_ms(fn, stream, k_big, warmup)
+        ms = event_ms(fn, stream, k_big, warmup, 3)
         out["hier_2x8_bf16"]["paths"][name] = figures(
             ms, N, S, compressed_hbm_bytes(N, L, "bf16", block, path, False), peak, block=block,
             error_feedback=False, launches=1 if path == "fused" else 2)
@@ -838,7 +840,7 @@ def run_workloads(dev, stream, peak, k_big: int, warmup: int):
     paths = {}
     for path in ("fused", "pack"):
         sync, hbm, launches, nb, keep = bucket_sync(grads, counts, N, path, handle)
-        ms = event_ms(sync, stream, max(3, k_big // 2), min(warmup, 3))
+        ms = event_ms(sync, stream, max(3, k_big // 2), min(warmup, 3), 2)
         paths["fused_no_pack" if path == "fused" else "pack_ring_unpack"] = figures(
             ms, N, S, hbm, peak, buckets=nb, launches=launches)
         del keep
@@ -846,7 +848,8 @@ def run_workloads(dev, stream, peak, k_big: int, warmup: int):
         "workload": spec.name, "n_ranks": N, "tensors": len(counts), "count_per_rank": sum(counts),
         "bytes_per_rank": S,
         "inputs": "device-filled: torch.randn on the GPU (one seed per rank and tensor) x 1e-3, rounded to bf16",
-        "timing": f"median of {max(3, k_big // 2)} whole syncs (every bucket, in place) after warm-up",
+        "timing": f"median of {max(3, k_big // 2)} timings of 2 whole syncs back to back (every bucket, in "
+                  "place) after warm-up",
         "paths": paths}
     task, sample = _bucket_task()
     tasks.append(("buckets_n8_transformer", task, sample))
@@ -867,7 +870,8 @@ def run_workloads(dev, stream, peak, k_big: int, warmup: int):
                            ("ring_steps", g.ar_plan(n, L, "f32", "ring")),
                            ("rabenseifner_steps", g.ar_plan(n, L, "f32", "rabenseifner"))):
             paths[name] = plan_path(plan, bufs, outs, n, GiB, k)
-        sweep_out[f"n{n}_1gib"] = {"n_ranks": n, "bytes_per_rank": GiB, "timing": f"median of {k} calls",
+        sweep_out[f"n{n}_1gib"] = {"n_ranks": n, "bytes_per_rank": GiB,
+                                   "timing": f"median of {k} timings of 3 calls back to back",
                                    "paths": paths}
         task, sample = _sweep_task(n, L)
         tasks.append((f"sweep_n{n}_1gib", task, sample))

@@ -13,7 +13,10 @@
 // holds until the process exits.
 //
 // It runs exactly the same kernels as ar_execute; only the workspace pointer
-// differs.
+// differs. The first call on a device that needs the array looks up its
+// address there; with lazy module loading that is when the module is loaded
+// on the device and the array reserved, so callers make one warm-up call at
+// start-up, before a pool takes the device's memory and before any capture.
 #include <mutex>
 
 #include "internal.h"

@@ -294,9 +294,16 @@ ar_status ar_execute_host(const ar_plan_t* plan, const void* const* host_in, voi
  *    is rejected with AR_EINVAL before anything is enqueued (use ar_execute
  *    with your own workspace for it). Plans that need no workspace run as
  *    with ar_execute.
- *  - The first call on each device looks up the array's device address on
- *    that device (a CUDA runtime query, not an allocation); make that first
- *    call before any stream capture begins.
+ *  - The first call on each device that needs the array looks up its
+ *    device address there. With lazy module loading (the CUDA default) that
+ *    lookup is also the moment the library's module is loaded on the device,
+ *    which reserves the AR_STATIC_WORKSPACE_BYTES array in device memory; and
+ *    the first executing call on a device pins the 4-byte host status word.
+ *    Either can synchronise, and on a device whose memory another pool has
+ *    already taken, the module load can fail (AR_ECUDA). So make one warm-up
+ *    call per device at start-up, with a plan that needs the workspace,
+ *    before any pool takes the device's memory and before any stream capture
+ *    begins.
  *  - All calls share the one array, and it keeps whatever the previous call
  *    left in it. That is harmless: the kernels write every workspace word
  *    before they read it within the same call, so nothing has to start at
