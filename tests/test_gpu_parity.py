@@ -254,6 +254,28 @@ def test_fused_bulk_copy_pipeline_matches_oracle(g, dtype, order, N, L, sm_budge
         assert_bits_equal(to_host((outs or devs)[r], dtype), want, f"rank {r}")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("order", ["ring", "rank", "hier"])
+@pytest.mark.parametrize("N,L", [(5, 4099), (8, 20003), (16, 100003), (64, 5001)])
+def test_fused_register_pipeline_with_sm_budget(g, dtype, order, N, L):
+    """A launch held to fewer SMs than the GPU has runs the variants with twice
+    the loads in flight per thread (2 vectors x 8 ranks for more than 4
+    ranks); their result is the oracle's, bit for bit, in and out of place."""
+    if order == "hier" and N % 2:
+        pytest.skip("the hierarchical order needs a group size that divides N")
+    G = _group(N) if order == "hier" else 0
+    x = workloads.all_ranks(workloads.small_spec(N, L, dtype, "normal", seed=N * 5 + L))
+    want = expected("fused", order, x, dtype, G, 0.5)
+    for out_of_place in (False, True):
+        devs = [to_device(x[r], dtype) for r in range(N)]
+        outs = [torch.empty_like(d) for d in devs] if out_of_place else None
+        plan = g.ar_plan(N, L, dtype, "fused", group_size=G, order=order, scale=0.5, sm_budget=7, kernel="loads")
+        g.ar_execute(plan, devs, outs=outs)
+        torch.cuda.synchronize()
+        for r in range(N):
+            assert_bits_equal(to_host((outs or devs)[r], dtype), want, f"rank {r}")
+
+
 @pytest.mark.parametrize("kernel", ["auto", "loads", "bulk"])
 @pytest.mark.parametrize("sm_budget", [0, 9])
 def test_bucket_paths_with_sm_budget(g, sm_budget, kernel):
