@@ -579,7 +579,7 @@ ar_status execute_fused(const ar_plan_t* p, void* const* bufs, void* const* outs
     fused_tiling(d, fp, tile_bytes / int64_t(esize(d.dtype)), d.dtype == AR_BF16 ? 8 : 4);
     return from_cuda(launch_fused_tma(fp, d.dtype, stages, tile_bytes, d.sm_budget, stream));
   }
-  fused_tiling(d, fp, fused_tile_elems(d.dtype, d.n_ranks, d.order, d.collective, false, budgeted(d.sm_budget)),
+  fused_tiling(d, fp, fused_tile_elems(d.dtype, d.n_ranks, d.order, d.collective, budgeted(d.sm_budget)),
                fused_vec_elems(d.dtype, false));
   return from_cuda(launch_fused(fp, d.dtype, d.sm_budget, stream));
 }
@@ -1360,7 +1360,7 @@ ar_status ar_bucket_allreduce(int n_ranks, void* const* tensors, const size_t* c
   s = status_guard(nullptr);
   if (s != AR_OK) return s;
   const int64_t tile = tma ? tile_bytes / int64_t(esize(dtype))
-                           : fused_tile_elems(dtype, N, AR_ORDER_RING, AR_ALLREDUCE, v8, budgeted(sm_budget));
+                           : bucket_tile_elems(dtype, N, v8, budgeted(sm_budget));
   const int max_group = std::min(AR_MAX_BUCKET_TENSORS, kMaxBucketPtrs / N);
   static thread_local BucketFusedParams bp;
   std::memset(&bp, 0, sizeof(bp));

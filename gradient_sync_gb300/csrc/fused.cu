@@ -233,6 +233,285 @@ __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_flat_kernel(con
   }
 }
 
+// Budgeted launches (a few SMs, one CTA on each): a CTA alone on an SM has
+// too few loads in flight to cover HBM latency, and in the kernels above none
+// are in flight while a tile's N stores issue. The deep kernels below issue
+// the next tile's first batch of loads (NB ranks x VPT vectors) before this
+// tile's stores, into the registers the batch has just been added from, so
+// those loads' latency overlaps the stores. With NB x VPT covering all the
+// ranks of a tile, a CTA always has a whole tile's loads in flight. The
+// summation order per element is fold_single's: the same bits as the kernels
+// above.
+
+// Adds batch `base` (ranks base..base+NB-1 of the fold, already loaded into
+// v) into the running sums.
+template <class L, int NB, int VPT>
+__device__ __forceinline__ void add_batch(float (&part)[VPT][L::W], const typename L::raw_t (&v)[NB][VPT],
+                                          int base, int n, const bool (&ok)[VPT]) {
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    if (base + b < n) {
+#pragma unroll
+      for (int q = 0; q < VPT; ++q) {
+        if (!ok[q]) continue;
+        float f[L::W];
+        L::widen(v[b][q], f);
+        if (base + b == 0) {
+#pragma unroll
+          for (int w = 0; w < L::W; ++w) part[q][w] = f[w];
+        } else {
+#pragma unroll
+          for (int w = 0; w < L::W; ++w) part[q][w] = fadd(part[q][w], f[w]);
+        }
+      }
+    }
+  }
+}
+
+template <class L, int NB, int VPT>
+__device__ __forceinline__ void load_batch(typename L::raw_t (&v)[NB][VPT], const char* const* seq, int base, int n,
+                                           const int64_t (&e)[VPT], const bool (&ok)[VPT]) {
+#pragma unroll
+  for (int b = 0; b < NB; ++b)
+#pragma unroll
+    for (int q = 0; q < VPT; ++q)
+      if (base + b < n && ok[q]) v[b][q] = L::load(seq[base + b], e[q]);
+}
+
+// The element-by-element head [clo, min(a0, chi)) and tail [a1, chi) of a
+// segment, done by the CTA that takes its first tile.
+template <class LS, int W>
+__device__ __forceinline__ void ragged_ends(const char* const* seq, char* const* out, int n, float scale,
+                                            int64_t clo, int64_t chi, int64_t a0, int64_t a1) {
+  int64_t es = -1;
+  const int64_t head_end = a0 < chi ? a0 : chi;
+  if (threadIdx.x < W - 1) {
+    es = clo + threadIdx.x;
+    if (es >= head_end) es = -1;
+  } else if (threadIdx.x >= 32 && threadIdx.x < 32 + W - 1) {
+    es = a1 + (threadIdx.x - 32);
+    if (es >= chi) es = -1;
+  }
+  if (es >= 0) {
+    float acc[1][1];
+    const int64_t es1[1] = {es};
+    const bool ok1[1] = {true};
+    fold_single<LS, 8, 1>(acc, seq, n, es1, ok1);
+    acc[0][0] = fmul(acc[0][0], scale);
+    const typename LS::raw_t r = LS::narrow(acc[0]);
+    for (int q = 0; q < n; ++q) LS::store(out[q], es, r);
+  }
+}
+
+// Ring and rank order of the all-reduce (rotations of the rank list).
+template <bool BF16, int NB, int VPT>
+__global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_deep_kernel(const __grid_constant__ FusedParams p) {
+  using LV = Lane<BF16, true>;
+  using LS = Lane<BF16, false>;
+  constexpr int W = LV::W;
+  constexpr int64_t kTile = int64_t(kThreads) * W * VPT;
+  __shared__ const char* s_seq[2 * AR_MAX_RANKS];  // the ranks' inputs in order, twice
+  __shared__ char* s_out[AR_MAX_RANKS];
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int n = p.n;
+  if (threadIdx.x < n) {
+    s_out[threadIdx.x] = static_cast<char*>(p.out[threadIdx.x]);
+    s_seq[threadIdx.x] = s_seq[threadIdx.x + n] = static_cast<const char*>(p.in[threadIdx.x]);
+  }
+  const int64_t total = int64_t(p.n_seg) * p.tiles_per_seg;
+  int64_t t = blockIdx.x;
+  if (t >= total) return;  // uniform across the CTA
+  __syncthreads();
+
+  // Where tile t lies: its segment, its index in the segment, the segment's
+  // element range clipped to [e_lo, e_hi) and its aligned body [a0, a1).
+  struct Where {
+    int seg;
+    int64_t tt, clo, chi, a0, a1;
+  };
+  auto locate = [&](int64_t tile) {
+    Where w;
+    w.seg = int(tile / p.tiles_per_seg);
+    w.tt = tile - int64_t(w.seg) * p.tiles_per_seg;
+    int64_t lo, hi;
+    seg_range(p, w.seg, lo, hi);
+    w.clo = lo > p.e_lo ? lo : p.e_lo;
+    w.chi = hi < p.e_hi ? hi : p.e_hi;
+    w.a0 = round_up(w.clo, W);
+    w.a1 = round_down(w.chi, W);
+    if (w.a1 < w.a0) w.a1 = w.a0;
+    return w;
+  };
+  auto vectors = [&](const Where& w, int64_t (&e)[VPT], bool (&ok)[VPT]) {
+#pragma unroll
+    for (int q = 0; q < VPT; ++q) {
+      e[q] = w.a0 + w.tt * kTile + (int64_t(q) * kThreads + threadIdx.x) * W;
+      ok[q] = w.clo < w.chi && e[q] < w.a1;
+    }
+  };
+
+  typename LV::raw_t v[NB][VPT];
+  Where c = locate(t);
+  int64_t e[VPT];
+  bool ok[VPT];
+  vectors(c, e, ok);
+  load_batch<LV, NB, VPT>(v, s_seq + seg_rotation(p, c.seg), 0, n, e, ok);
+  for (;;) {
+    const char* const* seq = s_seq + seg_rotation(p, c.seg);
+    float part[VPT][W];
+    add_batch<LV, NB, VPT>(part, v, 0, n, ok);
+#pragma unroll 1
+    for (int base = NB; base < n; base += NB) {
+      load_batch<LV, NB, VPT>(v, seq, base, n, e, ok);
+      add_batch<LV, NB, VPT>(part, v, base, n, ok);
+    }
+    typename LV::raw_t r[VPT];
+#pragma unroll
+    for (int q = 0; q < VPT; ++q) {
+#pragma unroll
+      for (int w = 0; w < W; ++w) part[q][w] = fmul(part[q][w], p.scale);
+      r[q] = LV::narrow(part[q]);
+    }
+    // the next tile's first batch, before this tile's stores
+    const int64_t t2 = t + gridDim.x;
+    Where c2 = c;
+    int64_t e2[VPT];
+    bool ok2[VPT];
+    if (t2 < total) {
+      c2 = locate(t2);
+      if (c2.seg != c.seg) __syncthreads();  // keeps the warps of a CTA on one tile
+      vectors(c2, e2, ok2);
+      load_batch<LV, NB, VPT>(v, s_seq + seg_rotation(p, c2.seg), 0, n, e2, ok2);
+    }
+#pragma unroll 2
+    for (int d = 0; d < n; ++d)
+#pragma unroll
+      for (int q = 0; q < VPT; ++q)
+        if (ok[q]) LV::store(s_out[d], e[q], r[q]);
+    if (c.tt == 0 && c.clo < c.chi) ragged_ends<LS, W>(seq, s_out, n, p.scale, c.clo, c.chi, c.a0, c.a1);
+    if (t2 >= total) break;
+    t = t2;
+    c = c2;
+#pragma unroll
+    for (int q = 0; q < VPT; ++q) {
+      e[q] = e2[q];
+      ok[q] = ok2[q];
+    }
+  }
+}
+
+// The bucket kernel's deep variant (below): a segment's pointers are written
+// to one of two shared-memory slots, so the next segment's can be published
+// while this tile's stores still read the current ones.
+template <bool BF16, bool V8, int NB, int VPT>
+__global__ void __launch_bounds__(kThreads, AR_FUSED_MINB)
+    fused_bucket_deep_kernel(const __grid_constant__ BucketFusedParams p) {
+  using LV = typename std::conditional<V8, Lane32<BF16>, Lane<BF16, true>>::type;
+  using LS = Lane<BF16, false>;
+  constexpr int W = LV::W;
+  constexpr int64_t kTile = int64_t(kThreads) * W * VPT;
+  __shared__ const char* s_seq[2][AR_MAX_RANKS];  // the fold's inputs from the chunk's rank
+  __shared__ char* s_out[2][AR_MAX_RANKS];
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int n = p.n;
+  const int total = p.tile_start[p.n_seg];
+  int t = blockIdx.x;
+  if (t >= total) return;  // uniform across the CTA
+  auto publish = [&](int s, int slot) {
+    if (threadIdx.x < n) {
+      const BucketSeg& sg = p.seg[s];
+      int r = sg.rot + threadIdx.x;
+      if (r >= n) r -= n;
+      s_seq[slot][threadIdx.x] = static_cast<const char*>(p.ptr[sg.t * n + r]);
+      s_out[slot][threadIdx.x] = static_cast<char*>(p.ptr[sg.t * n + threadIdx.x]);
+    }
+  };
+  struct Where {
+    int64_t tt, lo, hi, a0, a1;
+  };
+  auto locate = [&](int s, int tile) {
+    Where w;
+    w.tt = tile - p.tile_start[s];
+    w.lo = p.seg[s].lo;
+    w.hi = p.seg[s].hi;
+    w.a0 = round_up(w.lo, W);
+    w.a1 = round_down(w.hi, W);
+    if (w.a1 < w.a0) w.a1 = w.a0;
+    return w;
+  };
+  auto vectors = [&](const Where& w, int64_t (&e)[VPT], bool (&ok)[VPT]) {
+#pragma unroll
+    for (int q = 0; q < VPT; ++q) {
+      e[q] = w.a0 + w.tt * kTile + (int64_t(q) * kThreads + threadIdx.x) * W;
+      ok[q] = e[q] < w.a1;
+    }
+  };
+
+  int s = 0;
+  while (p.tile_start[s + 1] <= t) ++s;
+  int slot = 0;
+  publish(s, slot);
+  __syncthreads();
+  typename LV::raw_t v[NB][VPT];
+  Where c = locate(s, t);
+  int64_t e[VPT];
+  bool ok[VPT];
+  vectors(c, e, ok);
+  load_batch<LV, NB, VPT>(v, s_seq[slot], 0, n, e, ok);
+  for (;;) {
+    float part[VPT][W];
+    add_batch<LV, NB, VPT>(part, v, 0, n, ok);
+#pragma unroll 1
+    for (int base = NB; base < n; base += NB) {
+      load_batch<LV, NB, VPT>(v, s_seq[slot], base, n, e, ok);
+      add_batch<LV, NB, VPT>(part, v, base, n, ok);
+    }
+    typename LV::raw_t r[VPT];
+#pragma unroll
+    for (int q = 0; q < VPT; ++q) {
+#pragma unroll
+      for (int w = 0; w < W; ++w) part[q][w] = fmul(part[q][w], p.scale);
+      r[q] = LV::narrow(part[q]);
+    }
+    // the next tile's first batch, before this tile's stores
+    const int t2 = t + gridDim.x;
+    int s2 = s, slot2 = slot;
+    Where c2 = c;
+    int64_t e2[VPT];
+    bool ok2[VPT];
+    if (t2 < total) {
+      while (p.tile_start[s2 + 1] <= t2) ++s2;
+      if (s2 != s) {  // uniform across the CTA
+        slot2 = slot ^ 1;
+        __syncthreads();  // every warp is done with the tile before this one (the other slot)
+        publish(s2, slot2);
+        __syncthreads();
+      }
+      c2 = locate(s2, t2);
+      vectors(c2, e2, ok2);
+      load_batch<LV, NB, VPT>(v, s_seq[slot2], 0, n, e2, ok2);
+    }
+#pragma unroll 2
+    for (int d = 0; d < n; ++d)
+#pragma unroll
+      for (int q = 0; q < VPT; ++q)
+        if (ok[q]) LV::store(s_out[slot][d], e[q], r[q]);
+    if (c.tt == 0) ragged_ends<LS, W>(s_seq[slot], s_out[slot], n, p.scale, c.lo, c.hi, c.a0, c.a1);
+    if (t2 >= total) break;
+    t = t2;
+    s = s2;
+    slot = slot2;
+    c = c2;
+#pragma unroll
+    for (int q = 0; q < VPT; ++q) {
+      e[q] = e2[q];
+      ok[q] = ok2[q];
+    }
+  }
+}
+
 // Bucket variant: every rank's gradient tensors are read in place through a
 // (tensor, rank) pointer table; segments are the pieces of the tensors cut at
 // the ring's chunk boundaries over the packed bucket, so each segment is
@@ -353,21 +632,42 @@ cudaError_t launch_persistent(void (*kernel)(P), const P& p, int64_t tiles, int 
 // (0.85 with 4 vectors; 8 measured the same).
 constexpr int kRsNB = 8, kRsVPT = 2, kAgVPT = 4;
 
-// `deep` (a budgeted launch, see budgeted()): the all-reduce in ring, rank or
-// hierarchical order over more than 4 ranks takes 2 vectors per thread with
-// 8 ranks per batch, 16 loads in flight per thread.
-int fused_vpt(int n, int order, int collective, bool deep) {
+// Budgeted deep kernels with 16-byte vectors: up to 16 loads per thread in
+// one batch, a whole tile's for up to 16 ranks: 16 ranks x 1 vector from
+// kDeepWideMin ranks up, 8 x 2 from 5 ranks, 4 x 4 for 3 and 4 ranks and
+// 2 x 5 for 2 (bf16, whose sums take twice the registers, 4 x 3 and 2 x 4:
+// more spills). At 32 SMs, 16 x 192 MiB fp32 measured 0.71 of HBM with
+// 16 x 1 against 0.60 with 8 x 2; 8 x 128 MiB bf16 0.55 with 8 x 2 against
+// 0.36 with 16 x 1; 10 and 12 ranks were faster with 16 x 1 too.
+constexpr int kDeepWideMin = 9;
+int deep_nb(int n) { return n >= kDeepWideMin ? 16 : n > 4 ? 8 : n > 2 ? 4 : 2; }
+int deep_vpt(int n, bool bf16) {
+  return n >= kDeepWideMin ? 1 : n > 4 ? 2 : n > 2 ? (bf16 ? 3 : 4) : (bf16 ? 4 : 5);
+}
+
+// `deep` (a budgeted launch, see budgeted()): the all-reduce in ring or rank
+// order takes the deep kernel's shape; the hierarchical order over more than
+// 4 ranks takes 2 vectors per thread with 8 ranks per batch.
+int fused_vpt(int n, int order, int collective, bool bf16, bool deep) {
   if (collective == AR_ALLGATHER) return kAgVPT;
   if (collective == AR_REDUCE_SCATTER && order != AR_ORDER_TREE && n > 4) return kRsVPT;
   if (order == AR_ORDER_TREE) return 1;
+  if (deep && collective == AR_ALLREDUCE && order != AR_ORDER_HIER) return deep_vpt(n, bf16);
   if (deep && n > 4) return 2;
   return n <= 2 ? 4 : n <= 4 ? 2 : 1;
 }
 
+// The bucket kernel's 16-byte path: the flat all-reduce's vectors per thread.
+int bucket_vpt(int n, bool bf16, bool deep) { return deep ? deep_vpt(n, bf16) : n <= 2 ? 4 : n <= 4 ? 2 : 1; }
+
 int fused_vec_elems(ar_dtype dtype, bool v8) { return (dtype == AR_BF16 ? 8 : 4) * (v8 ? 2 : 1); }
 
-int64_t fused_tile_elems(ar_dtype dtype, int n, int order, int collective, bool v8, bool deep) {
-  return int64_t(kThreads) * fused_vec_elems(dtype, v8) * (v8 ? 1 : fused_vpt(n, order, collective, deep));
+int64_t fused_tile_elems(ar_dtype dtype, int n, int order, int collective, bool deep) {
+  return int64_t(kThreads) * fused_vec_elems(dtype, false) * fused_vpt(n, order, collective, dtype == AR_BF16, deep);
+}
+
+int64_t bucket_tile_elems(ar_dtype dtype, int n, bool v8, bool deep) {
+  return int64_t(kThreads) * fused_vec_elems(dtype, v8) * (v8 ? 1 : bucket_vpt(n, dtype == AR_BF16, deep));
 }
 
 // Every order but the hierarchical one (rotations of the rank list). The
@@ -382,11 +682,17 @@ cudaError_t launch_fused_rot(const FusedParams& p, int64_t tiles, int sm_budget,
                              stream);
   if (p.collective == AR_ALLGATHER)
     return launch_persistent(fused_flat_kernel<BF16, false, kSeqRotated, 1, kAgVPT>, p, tiles, sm_budget, stream);
-  switch (fused_vpt(p.n, p.order, p.collective, budgeted(sm_budget))) {
+  if (budgeted(sm_budget) && p.collective == AR_ALLREDUCE) {  // ring or rank order
+    switch (deep_nb(p.n)) {
+      case 16: return launch_persistent(fused_deep_kernel<BF16, 16, 1>, p, tiles, sm_budget, stream);
+      case 8: return launch_persistent(fused_deep_kernel<BF16, 8, 2>, p, tiles, sm_budget, stream);
+      case 4: return launch_persistent(fused_deep_kernel<BF16, 4, BF16 ? 3 : 4>, p, tiles, sm_budget, stream);
+      default: return launch_persistent(fused_deep_kernel<BF16, 2, BF16 ? 4 : 5>, p, tiles, sm_budget, stream);
+    }
+  }
+  switch (fused_vpt(p.n, p.order, p.collective, BF16, false)) {
     case 4: return launch_persistent(fused_flat_kernel<BF16, false, kSeqRotated, 2, 4>, p, tiles, sm_budget, stream);
-    case 2:
-      return p.n > 4 ? launch_persistent(fused_flat_kernel<BF16, false, kSeqRotated, 8, 2>, p, tiles, sm_budget, stream)
-                     : launch_persistent(fused_flat_kernel<BF16, false, kSeqRotated, 4, 2>, p, tiles, sm_budget, stream);
+    case 2: return launch_persistent(fused_flat_kernel<BF16, false, kSeqRotated, 4, 2>, p, tiles, sm_budget, stream);
     default:
       return p.n > 16 ? launch_persistent(fused_flat_kernel<BF16, false, kSeqRotatedPos, 8, 1>, p, tiles, sm_budget, stream)
                       : launch_persistent(fused_flat_kernel<BF16, false, kSeqRotated, 8, 1>, p, tiles, sm_budget, stream);
@@ -398,7 +704,7 @@ cudaError_t launch_fused_rot(const FusedParams& p, int64_t tiles, int sm_budget,
 template <bool BF16>
 cudaError_t launch_fused_t(const FusedParams& p, int64_t tiles, int sm_budget, cudaStream_t stream) {
   if (p.order == AR_ORDER_HIER && p.collective == AR_ALLREDUCE) {  // the planner allows it for all-reduce only
-    switch (fused_vpt(p.n, p.order, p.collective, budgeted(sm_budget))) {
+    switch (fused_vpt(p.n, p.order, p.collective, BF16, budgeted(sm_budget))) {
       case 4: return launch_persistent(fused_flat_kernel<BF16, false, kSeqWritten, 2, 4>, p, tiles, sm_budget, stream);
       case 2:
         return p.n > 4 ? launch_persistent(fused_flat_kernel<BF16, false, kSeqWritten, 8, 2>, p, tiles, sm_budget, stream)
@@ -417,20 +723,27 @@ cudaError_t launch_fused(const FusedParams& p, ar_dtype dtype, int sm_budget, cu
 
 // 32-byte lanes (N > 4 only, one vector per thread): each load moves twice the
 // bytes, so a batch holds half as many ranks (the same bytes in flight).
+// Budgeted launches take the deep kernel: with 32-byte lanes 8 ranks per
+// batch (bf16 and fp32 alike), with 16-byte lanes the flat kernel's shapes.
 template <bool BF16>
 cudaError_t launch_bucket_t(const BucketFusedParams& p, int64_t tiles, int sm_budget, bool v8, cudaStream_t stream) {
   const bool deep = budgeted(sm_budget);
-  // budgeted: 8 ranks per batch (8 32-byte loads in flight per thread); 6
-  // for bf16, whose 16-element lanes spilled registers at 8
-  constexpr int kDeepNB = BF16 ? 6 : 8;
   if (v8)
-    return deep ? launch_persistent(fused_bucket_kernel<BF16, true, kDeepNB, 1>, p, tiles, sm_budget, stream)
+    return deep ? launch_persistent(fused_bucket_deep_kernel<BF16, true, 8, 1>, p, tiles, sm_budget, stream)
                 : launch_persistent(fused_bucket_kernel<BF16, true, 4, 1>, p, tiles, sm_budget, stream);
-  switch (fused_vpt(p.n, AR_ORDER_RING, AR_ALLREDUCE, deep)) {
+  if (deep) {
+    switch (deep_nb(p.n)) {
+      case 16: return launch_persistent(fused_bucket_deep_kernel<BF16, false, 16, 1>, p, tiles, sm_budget, stream);
+      case 8: return launch_persistent(fused_bucket_deep_kernel<BF16, false, 8, 2>, p, tiles, sm_budget, stream);
+      case 4:
+        return launch_persistent(fused_bucket_deep_kernel<BF16, false, 4, BF16 ? 3 : 4>, p, tiles, sm_budget, stream);
+      default:
+        return launch_persistent(fused_bucket_deep_kernel<BF16, false, 2, BF16 ? 4 : 5>, p, tiles, sm_budget, stream);
+    }
+  }
+  switch (bucket_vpt(p.n, BF16, false)) {
     case 4: return launch_persistent(fused_bucket_kernel<BF16, false, 2, 4>, p, tiles, sm_budget, stream);
-    case 2:
-      return p.n > 4 ? launch_persistent(fused_bucket_kernel<BF16, false, 8, 2>, p, tiles, sm_budget, stream)
-                     : launch_persistent(fused_bucket_kernel<BF16, false, 4, 2>, p, tiles, sm_budget, stream);
+    case 2: return launch_persistent(fused_bucket_kernel<BF16, false, 4, 2>, p, tiles, sm_budget, stream);
     default: return launch_persistent(fused_bucket_kernel<BF16, false, 8, 1>, p, tiles, sm_budget, stream);
   }
 }

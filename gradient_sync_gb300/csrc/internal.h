@@ -261,7 +261,8 @@ cudaError_t launch_small_steps_smem(const SmallParams& p, ar_dtype dtype, cudaSt
 // Register pipeline: elements per vector (v8: 32-byte vectors, bucket kernel
 // only, N > 4 and every pointer 32-byte aligned) and per tile.
 int fused_vec_elems(ar_dtype dtype, bool v8);
-int64_t fused_tile_elems(ar_dtype dtype, int n, int order, int collective, bool v8, bool deep);
+int64_t fused_tile_elems(ar_dtype dtype, int n, int order, int collective, bool deep);
+int64_t bucket_tile_elems(ar_dtype dtype, int n, bool v8, bool deep);
 cudaError_t launch_bucket_fused(const BucketFusedParams& p, ar_dtype dtype, int sm_budget, bool v8, cudaStream_t stream);
 cudaError_t launch_pack(const PackParams& p, ar_dtype dtype, bool unpack, cudaStream_t stream);
 cudaError_t read_device_status(unsigned int* value, bool clear);

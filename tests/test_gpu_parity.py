@@ -256,11 +256,13 @@ def test_fused_bulk_copy_pipeline_matches_oracle(g, dtype, order, N, L, sm_budge
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("order", ["ring", "rank", "hier"])
-@pytest.mark.parametrize("N,L", [(5, 4099), (8, 20003), (16, 100003), (64, 5001)])
+@pytest.mark.parametrize("N,L", [(2, 70001), (3, 1001), (4, 12345), (5, 4099), (8, 20003), (12, 33333),
+                                 (16, 100003), (64, 5001)])
 def test_fused_register_pipeline_with_sm_budget(g, dtype, order, N, L):
-    """A launch held to fewer SMs than the GPU has runs the variants with twice
-    the loads in flight per thread (2 vectors x 8 ranks for more than 4
-    ranks); their result is the oracle's, bit for bit, in and out of place."""
+    """A launch held to fewer SMs than the GPU has runs the variants with more
+    loads in flight per thread (for more than 4 ranks in ring or rank order,
+    the next tile's first batch is loaded during this tile's stores); their
+    result is the oracle's, bit for bit, in and out of place."""
     if order == "hier" and N % 2:
         pytest.skip("the hierarchical order needs a group size that divides N")
     G = _group(N) if order == "hier" else 0
@@ -274,6 +276,23 @@ def test_fused_register_pipeline_with_sm_budget(g, dtype, order, N, L):
         torch.cuda.synchronize()
         for r in range(N):
             assert_bits_equal(to_host((outs or devs)[r], dtype), want, f"rank {r}")
+
+
+@pytest.mark.parametrize("order", ["ring", "rank"])
+def test_execute_host_slabs_with_sm_budget(g, order):
+    """Pageable host buffers go through the device in slabs, one launch per
+    element range; the ranges cut the ring's chunks mid-way, and the launches
+    held to a few SMs still give the oracle's bits."""
+    N, L = 8, 5 * (1 << 20) + 3
+    x = workloads.all_ranks(workloads.small_spec(N, L, "f32", "normal", seed=21))
+    host_in = [torch.from_numpy(x[r].copy()) for r in range(N)]
+    host_out = [torch.empty(L, dtype=torch.float32) for _ in range(N)]
+    dev = [torch.empty(L, dtype=torch.float32, device="cuda") for _ in range(N)]
+    plan = g.ar_plan(N, L, "f32", "fused", order=order, sm_budget=6, kernel="loads")
+    g.ar_execute_host(plan, host_in, host_out, dev)
+    want = expected("fused", order, x, "f32")
+    for r in range(N):
+        assert_bits_equal(host_out[r].numpy(), want, f"rank {r}")
 
 
 @pytest.mark.parametrize("kernel", ["auto", "loads", "bulk"])
@@ -323,22 +342,25 @@ def test_step_executor_on_16_byte_aligned_buffers(g, dtype, algo):
         assert_bits_equal(to_host(devs[r].contiguous(), dtype), want, f"rank {r}")
 
 
+@pytest.mark.parametrize("sm_budget", [0, 5])
+@pytest.mark.parametrize("N,dtype", [(8, "bf16"), (12, "f32"), (5, "bf16"), (2, "f32"), (4, "bf16")])
 @pytest.mark.parametrize("aligned32", [True, False])
-def test_bucket_allreduce_vector_widths(g, aligned32):
+def test_bucket_allreduce_vector_widths(g, aligned32, N, dtype, sm_budget):
     """The fused bucket pass moves 32-byte vectors when every tensor is
-    32-byte aligned (8 ranks) and 16-byte vectors otherwise (tensors placed 16
-    bytes into larger allocations); both give the oracle's bits, ragged tensor
-    sizes included."""
+    32-byte aligned (more than 4 ranks) and 16-byte vectors otherwise
+    (tensors placed 16 bytes into larger allocations); both give the oracle's
+    bits, ragged tensor sizes included, at full width and held to a few SMs
+    (the kernels that load the next tile during this tile's stores)."""
     from oracle import buckets as ob
 
-    N, dtype = 8, "bf16"
     counts = [5, 1000, 37, 4096, 9, 2051, 777, 64, 3, 30_011]
     scale = 1.0 / N
-    rng = np.random.default_rng(17)
-    host = [[numerics.f32_to_bf16_rne((rng.standard_normal(c) * 1e-3).astype(np.float32)) for c in counts]
-            for _ in range(N)]
-    tdt = torch.bfloat16
-    shift = 0 if aligned32 else 8  # 16 bytes of bf16
+    rng = np.random.default_rng(17 + N)
+    host = [[(rng.standard_normal(c) * 1e-3).astype(np.float32) for c in counts] for _ in range(N)]
+    if dtype == "bf16":
+        host = [[numerics.f32_to_bf16_rne(a) for a in row] for row in host]
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    shift = 0 if aligned32 else 16 // (2 if dtype == "bf16" else 4)  # 16 bytes
     keep, dev = [], []
     for r in range(N):
         row = []
@@ -351,9 +373,21 @@ def test_bucket_allreduce_vector_widths(g, aligned32):
             row.append(v)
         dev.append(row)
     lo, hi = 0, len(counts)
-    g.ar_bucket_allreduce(dev, counts, lo, hi, dtype, scale)
+    g.ar_bucket_allreduce(dev, counts, lo, hi, dtype, scale, sm_budget=sm_budget)
     torch.cuda.synchronize()
-    want = ob.sync_bucket(host, list(range(lo, hi)), counts, scale)
+    bucket = list(range(hi - 1, lo - 1, -1))  # packed in reverse forward order
+    if dtype == "bf16":
+        want = ob.sync_bucket(host, bucket, counts, scale)
+    else:  # fp32 packs as is: the ring all-reduce of the packed bucket, times the scale
+        offs = ob.bucket_offsets(bucket, counts)
+        Lb = sum(counts[t] for t in bucket)
+        packed = np.zeros((N, Lb), np.float32)
+        for r in range(N):
+            for t in bucket:
+                packed[r, offs[t]:offs[t] + counts[t]] = host[r][t]
+        reduced, _ = schedules.ring_allreduce(packed)
+        out = reduced * np.float32(scale)
+        want = {(t, 0): out[:, offs[t]:offs[t] + counts[t]] for t in bucket}
     for t in range(lo, hi):
         for r in range(N):
             assert_bits_equal(to_host(dev[r][t].contiguous(), dtype), want[(t, 0)][r], f"t={t} r={r}")
