@@ -575,7 +575,10 @@ def time_case(n, count, dtype="f32", algo="fused", order="ring", group_size=0, i
            "timing": "cuda graph" if graph else ("bound, replayed from python" if bound else "launched from python"),
            "group_size": group_size or None, "torus_dims": list(torus_dims) if algo == "torus" else None,
            "us": round(ms * 1e3, 2), "steps": st["steps"], "launches": st["launches"]}
-    f = figures(ms, n, S, st["hbm_bytes"], measured_peaks()[0], collective)
+    hbm = st["hbm_bytes"]
+    if algo != "fused" and collective == "allgather" and n > 1:  # out of place: each rank's own chunk
+        hbm += count * esz * (2 if st["launches"] == 1 else 1)  # also goes to its output (ar.h)
+    f = figures(ms, n, S, hbm, measured_peaks()[0], collective)
     res.update({k: v for k, v in f.items() if k not in ("ms", "us")})
     res["hbm_frac"] = res.pop("frac_of_hbm")
     del bufs, outs, ws

@@ -619,7 +619,8 @@ ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs
     return from_cuda(launch_step(sp, d.dtype, OP_FINISH, sp.tile_start[1], false, d.sm_budget, v8, stream));
   }
   // out of place all-gather: every rank's own chunk is copied to its output
-  // first (the ring delivers only the other N-1 chunks)
+  // (the ring delivers only the other N-1 chunks): first, in a one-CTA plan;
+  // by the first ring step otherwise (below)
   Step own{OP_COPY, {}};
   if (d.collective == AR_ALLGATHER && outs != nullptr) {
     const auto b = cuts(0, int64_t(d.count), N);
@@ -743,6 +744,28 @@ ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs
     if (smem) return from_cuda(launch_small_steps_smem(q, d.dtype, stream));
     return from_cuda(launch_small_steps(q, d.dtype, stream));
   }
+  // The own chunks ride on the all-gather's first step, which reads each of
+  // them from its rank's input to send it: that step also writes it to the
+  // sender's output (`pair`), saving a launch and a read of every chunk.
+  std::vector<uint8_t> pair_first;
+  if (!own.xfers.empty() && !p->steps.empty() && p->steps[0].op == OP_COPY) {
+    const Step& first = p->steps[0];
+    pair_first.assign(first.xfers.size(), 0);
+    size_t matched = 0;
+    for (const Transfer& o : own.xfers)
+      for (size_t x = 0; x < first.xfers.size(); ++x) {
+        const Transfer& t = first.xfers[x];
+        if (t.src == o.src && t.lo == o.lo && t.hi == o.hi && t.xs == RAW && t.ds == RES && !pair_first[x]) {
+          pair_first[x] = 1;
+          ++matched;
+          break;
+        }
+      }
+    if (matched == own.xfers.size())
+      own.xfers.clear();
+    else
+      pair_first.clear();
+  }
   if (!own.xfers.empty()) {
     sp.n_xfer = int(own.xfers.size());
     int tiles = 0;
@@ -766,6 +789,7 @@ ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs
       for (int x = 0; x < sp.n_xfer; ++x) {
         const Transfer& t = st.xfers[x0 + size_t(x)];
         sp.x[x] = t;
+        if (&st == &p->steps[0] && !pair_first.empty()) sp.x[x].pair = pair_first[x0 + size_t(x)];
         sp.tile_start[x] = tiles;
         const int64_t body = std::max<int64_t>(rdown(t.hi, kStepVec) - rup(t.lo, kStepVec), 0);
         tiles += int(std::max<int64_t>(1, (body + kStepTile - 1) / kStepTile));

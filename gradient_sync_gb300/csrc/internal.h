@@ -27,7 +27,9 @@ enum StepOp : int { OP_ADD = 0, OP_COPY = 1, OP_FINISH = 2 };
 // (a tree node receiving from two children in one step); final: times scale,
 // rounded to the output type. With `pair`, src receives the same sum in
 // D[src] (an exchange: fp32 addition commutes, so both partners hold the
-// same bits). COPY: D[dst] = X[src], operands of one type. FINISH (one
+// same bits). COPY: D[dst] = X[src], operands of one type; with `pair`,
+// also D[src] = X[src] (an out-of-place all-gather's first step writing the
+// sender's own chunk to its output as it sends it). FINISH (one
 // rank): RES[dst] = scale * X[src], rounded to the output type.
 struct Transfer {
   int16_t src, dst, src2;

@@ -193,7 +193,9 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
     const Operand Y = operand<BF16>(p, tr.ys, tr.dst);
     const Operand D = operand<BF16>(p, tr.ds, tr.dst);
     const bool two = OP == OP_ADD && tr.src2 >= 0;  // uniform over the transfer
-    const bool pair = OP == OP_ADD && tr.pair != 0;
+    // pair: an add's sum also goes to the sender's copy (an exchange); a copy
+    // also writes the sender's output (the all-gather's own chunk)
+    const bool pair = tr.pair != 0;
     const Operand X2 = operand<BF16>(p, tr.x2s, two ? tr.src2 : tr.dst);
     const Operand D2 = operand<BF16>(p, tr.ds, tr.src);
     const bool fin = tr.fin != 0;
@@ -218,8 +220,10 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
         if (OP == OP_COPY) {  // same type on both sides: move the bytes
           if (X.f32) {
             store_raw8<kStream, V8>(D.base, e[u], rx[u]);
+            if (pair) store_raw8<kStream, V8>(D2.base, e[u], rx[u]);
           } else {
             st16<kStream>(reinterpret_cast<uint4*>(D.base + e[u] * 2), rx[u].a);
+            if (pair) st16<kStream>(reinterpret_cast<uint4*>(D2.base + e[u] * 2), rx[u].a);
           }
         } else {
           float f[8];

@@ -215,7 +215,13 @@ typedef struct {
                                   schedule, in bytes of the payload type */
   size_t hbm_bytes;            /* algorithmic HBM bytes of one ar_execute:
                                   every element read or written counted once
-                                  per access, at its storage width */
+                                  per access, at its storage width. An
+                                  out-of-place all-gather by steps also
+                                  writes every rank's own chunk to its output:
+                                  count elements more, written by the first
+                                  step as it sends them (a plan run in one
+                                  CTA copies them first, reading them too);
+                                  these bytes are not included */
   size_t workspace_bytes;      /* device workspace ar_execute needs (0 = none) */
 } ar_stats;
 /* With one rank the schedule is empty (all fields 0 but workspace_bytes);

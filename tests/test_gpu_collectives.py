@@ -98,6 +98,26 @@ def test_allgather_bulk_copies(g, dtype, N, L, out_of_place):
             assert_bits_equal(got[r], want[r], f"rank {r} (sm_budget {sm_budget})")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N,L", [(3, 1000), (8, 20003), (16, 100003), (5, 3)])
+def test_ring_allgather_mixed_in_and_out_of_place(g, dtype, N, L):
+    """Even ranks in place, odd ranks into separate outputs, in one call: the
+    first ring step writes each sent chunk to the sender's own output only for
+    the ranks whose output is separate. Every output is the oracle's and every
+    separate input is left as it was."""
+    x = workloads.all_ranks(workloads.small_spec(N, L, dtype, "uniform", seed=N + L))
+    devs = [to_device(x[r], dtype) for r in range(N)]
+    outs = [d if r % 2 == 0 else torch.full_like(d, 7.0) for r, d in enumerate(devs)]
+    plan = g.ar_plan(N, L, dtype, "ring", collective="allgather")
+    g.ar_execute(plan, devs, outs=outs)
+    torch.cuda.synchronize()
+    want, _ = schedules.ring_allgather(x)
+    for r in range(N):
+        assert_bits_equal(to_host(outs[r], dtype), want[r], f"rank {r}")
+        if r % 2:
+            np.testing.assert_array_equal(to_host(devs[r], dtype), x[r])
+
+
 def test_allgather_bulk_from_host_slabs(g):
     """ar_execute_host on pageable memory runs the all-gather in element-range
     slabs: each slab's chunk pieces go through the bulk pipeline."""
