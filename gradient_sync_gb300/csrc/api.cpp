@@ -571,7 +571,10 @@ ar_status execute_fused(const ar_plan_t* p, void* const* bufs, void* const* outs
   fp.e_hi = e_hi;
   fp.scale = d.collective == AR_ALLGATHER ? 1.0f : d.scale;  // an all-gather only copies
   int stages = 0, tile_bytes = 0;
-  if (!host_memory && d.kernel != AR_KERNEL_LOADS && d.collective == AR_ALLGATHER && d.n_ranks > 1) {  // bulk: faster
+  // the all-gather's bulk copies: faster from 96 MiB per rank (ar.h, AR_KERNEL_AUTO)
+  const bool ag_bulk = d.kernel == AR_KERNEL_BULK ||
+                       (d.kernel == AR_KERNEL_AUTO && d.count * esize(d.dtype) >= (size_t(96) << 20));
+  if (!host_memory && ag_bulk && d.collective == AR_ALLGATHER && d.n_ranks > 1) {
     fused_tiling(d, fp, allgather_bulk_tile_elems(d.dtype), d.dtype == AR_BF16 ? 8 : 4);
     return from_cuda(launch_allgather_bulk(fp, d.dtype, d.sm_budget, stream));
   }

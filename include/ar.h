@@ -156,8 +156,10 @@ typedef enum { AR_ALLREDUCE = 0, AR_REDUCE_SCATTER = 1, AR_ALLGATHER = 2 } ar_co
  * in how bytes move between HBM and the SM.
  *  AR_KERNEL_AUTO:  the library's choice, the faster one measured: the
  *                   register pipeline for the all-reduce and reduce-scatter
- *                   (at every SM budget measured), bulk copies for the
- *                   all-gather (0.89 of HBM against 0.86).
+ *                   (at every SM budget measured); for the all-gather, bulk
+ *                   copies when a rank's buffer holds at least 96 MiB
+ *                   (16 x 192 MiB fp32: 0.93 of HBM against 0.90), the
+ *                   register pipeline below (64 x 4 MiB: 0.79 against 0.56).
  *  AR_KERNEL_LOADS: persistent register pipeline, 2 CTAs per SM; each thread
  *                   keeps a batch of 16-byte loads in flight.
  *  AR_KERNEL_BULK:  bulk copies (TMA) through shared memory.
