@@ -304,7 +304,15 @@ __device__ __forceinline__ void ragged_ends(const char* const* seq, char* const*
 }
 
 // Ring and rank order of the all-reduce (rotations of the rank list).
-template <bool BF16, int NB, int VPT>
+// kRegPtr: the first batch's input pointers are kept in registers, reloaded
+// when the CTA moves to another segment, instead of read from the
+// shared-memory table for every tile; the host sets it for fp32 when one
+// batch holds every rank (at 32 SMs, 16 x 192 MiB: 0.735 of HBM against
+// 0.714, 12 ranks 0.612 against 0.589, 8 ranks 0.679 against 0.647, 2 ranks
+// 0.556 against 0.551), except 3-4 ranks (4 x 4 vectors: 0.664 against
+// 0.682); bf16, whose sums take more registers, and 64 ranks measured about
+// 1 % slower with it.
+template <bool BF16, int NB, int VPT, bool kRegPtr>
 __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_deep_kernel(const __grid_constant__ FusedParams p) {
   using LV = Lane<BF16, true>;
   using LS = Lane<BF16, false>;
@@ -356,7 +364,18 @@ __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_deep_kernel(con
   int64_t e[VPT];
   bool ok[VPT];
   vectors(c, e, ok);
-  load_batch<LV, NB, VPT>(v, s_seq + seg_rotation(p, c.seg), 0, n, e, ok);
+  const char* p0[kRegPtr ? NB : 1];
+  auto first_ptrs = [&](int seg) {
+    const char* const* sq = s_seq + seg_rotation(p, seg);
+#pragma unroll
+    for (int b = 0; b < (kRegPtr ? NB : 1); ++b) p0[b] = b < n ? sq[b] : nullptr;
+  };
+  if constexpr (kRegPtr) {
+    first_ptrs(c.seg);
+    load_batch<LV, NB, VPT>(v, p0, 0, n, e, ok);
+  } else {
+    load_batch<LV, NB, VPT>(v, s_seq + seg_rotation(p, c.seg), 0, n, e, ok);
+  }
   for (;;) {
     const char* const* seq = s_seq + seg_rotation(p, c.seg);
     float part[VPT][W];
@@ -382,7 +401,12 @@ __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_deep_kernel(con
       c2 = locate(t2);
       if (c2.seg != c.seg) __syncthreads();  // keeps the warps of a CTA on one tile
       vectors(c2, e2, ok2);
-      load_batch<LV, NB, VPT>(v, s_seq + seg_rotation(p, c2.seg), 0, n, e2, ok2);
+      if constexpr (kRegPtr) {
+        if (c2.seg != c.seg) first_ptrs(c2.seg);
+        load_batch<LV, NB, VPT>(v, p0, 0, n, e2, ok2);
+      } else {
+        load_batch<LV, NB, VPT>(v, s_seq + seg_rotation(p, c2.seg), 0, n, e2, ok2);
+      }
     }
 #pragma unroll 2
     for (int d = 0; d < n; ++d)
@@ -683,11 +707,14 @@ cudaError_t launch_fused_rot(const FusedParams& p, int64_t tiles, int sm_budget,
   if (p.collective == AR_ALLGATHER)
     return launch_persistent(fused_flat_kernel<BF16, false, kSeqRotated, 1, kAgVPT>, p, tiles, sm_budget, stream);
   if (budgeted(sm_budget) && p.collective == AR_ALLREDUCE) {  // ring or rank order
+    const bool reg = !BF16 && p.n <= deep_nb(p.n);  // one batch holds every rank
     switch (deep_nb(p.n)) {
-      case 16: return launch_persistent(fused_deep_kernel<BF16, 16, 1>, p, tiles, sm_budget, stream);
-      case 8: return launch_persistent(fused_deep_kernel<BF16, 8, 2>, p, tiles, sm_budget, stream);
-      case 4: return launch_persistent(fused_deep_kernel<BF16, 4, BF16 ? 3 : 4>, p, tiles, sm_budget, stream);
-      default: return launch_persistent(fused_deep_kernel<BF16, 2, BF16 ? 4 : 5>, p, tiles, sm_budget, stream);
+      case 16:
+        return reg ? launch_persistent(fused_deep_kernel<BF16, 16, 1, !BF16>, p, tiles, sm_budget, stream)
+                   : launch_persistent(fused_deep_kernel<BF16, 16, 1, false>, p, tiles, sm_budget, stream);
+      case 8: return launch_persistent(fused_deep_kernel<BF16, 8, 2, !BF16>, p, tiles, sm_budget, stream);
+      case 4: return launch_persistent(fused_deep_kernel<BF16, 4, BF16 ? 3 : 4, false>, p, tiles, sm_budget, stream);
+      default: return launch_persistent(fused_deep_kernel<BF16, 2, BF16 ? 4 : 5, !BF16>, p, tiles, sm_budget, stream);
     }
   }
   switch (fused_vpt(p.n, p.order, p.collective, BF16, false)) {
