@@ -276,6 +276,45 @@ __device__ __forceinline__ float block_scale(const float (&x)[kEPT], int block, 
   return kLean ? div127(m) : __fdiv_rn(m, 127.0f);
 }
 
+// The scales of the NB ranks of a load batch (the first nb of them real),
+// with block_scale's arithmetic. For blocks that span warps, the warps'
+// maxima of all NB ranks go to shared memory together and one barrier serves
+// the batch instead of one per rank (wm: the batch's slot of NB x kWarps
+// floats; callers alternate two slots, as for block_scale).
+template <int kEPT, int NB>
+__device__ __forceinline__ void batch_scales(const float (&x)[NB][kEPT], int nb, int block, float* wm,
+                                             float (&s)[NB]) {
+  constexpr int kWarpElems = 32 * kEPT;
+  const int lanes = block < kWarpElems ? block / kEPT : 32;
+  float m[NB];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    m[b] = 0.0f;
+    if (b < nb) {
+#pragma unroll
+      for (int w = 0; w < kEPT; ++w) m[b] = fmaxf(m[b], fabsf(x[b][w]));
+    }
+    for (int o = lanes >> 1; o > 0; o >>= 1) m[b] = fmaxf(m[b], __shfl_xor_sync(kFull, m[b], o));
+  }
+  if (block > kWarpElems) {
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+      for (int b = 0; b < NB; ++b) wm[b * kWarps + warp] = m[b];
+    }
+    __syncthreads();
+    const int W = block / kWarpElems;
+    const int w0 = warp & ~(W - 1);
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      m[b] = wm[b * kWarps + w0];
+      for (int i = 1; i < W; ++i) m[b] = fmaxf(m[b], wm[b * kWarps + w0 + i]);
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < NB; ++b) s[b] = __fdiv_rn(m[b], 127.0f);
+}
+
 // Element-wise fp32 arithmetic, one IEEE operation per element rounded to
 // nearest even and never contracted into an FMA (the definition rounds every
 // product before it is summed).
@@ -407,12 +446,15 @@ __device__ __forceinline__ void store_codes(int8_t* q, int64_t e, int64_t count,
 // Each tile of every rank: codes (kEPT bytes per thread), the scale of each block
 // (written by the block's first thread) and, with error feedback, the new
 // residual.
-template <bool BF16, bool EF>
+// NB: ranks per load batch (fp32: 4, 1 or 2 measured slower). kBatch (fp32
+// blocks that span warps): the batch's scales from batch_scales, one barrier
+// per batch; block 1024 at 16 x 192 MiB, the two calls with error feedback
+// measured 0.941 of their bytes against 0.899.
+template <bool BF16, bool EF, int NB, bool kBatch>
 __global__ void __launch_bounds__(kThreads) compress_kernel(const __grid_constant__ CompressParams p) {
   constexpr int kEPT = compress_ept<BF16>();
   constexpr int kTileElems = kEPT * kThreads;
-  constexpr int NB = BF16 ? 1 : 4;  // ranks per load batch (fp32: 1 or 2 measured slower)
-  __shared__ float wmax[2][kWarps];
+  __shared__ float wmax[2][NB * kWarps];
   grid_dependency_wait();
   grid_dependents_launch();
   const int64_t n_tiles = (p.count + kTileElems - 1) / kTileElems;
@@ -422,33 +464,44 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const __grid_constan
     const int64_t e = tile * kTileElems + int64_t(kEPT) * threadIdx.x;
 #pragma unroll 1
     for (int r0 = 0; r0 < p.n; r0 += NB) {
-      float xg[NB][kEPT], xe[NB][kEPT];
+      const int nb = p.n - r0 < NB ? p.n - r0 : NB;  // uniform across the CTA
+      float x[NB][kEPT], xe[NB][kEPT];
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
-        if (r0 + b >= p.n) continue;
-        load_group<BF16, kEPT>(p.g[r0 + b], e, p.count, xg[b]);
+        if (b >= nb) continue;
+        load_group<BF16, kEPT>(p.g[r0 + b], e, p.count, x[b]);
         if (EF) load_group<false, kEPT>(p.e[r0 + b], e, p.count, xe[b]);
       }
+      if (EF) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+          if (b < nb) add_each(x[b], x[b], xe[b]);
+      }
+      float s[NB];
+      if constexpr (kBatch) {
+        batch_scales<kEPT, NB>(x, nb, p.block, wmax[phase], s);
+        phase ^= 1;
+      } else {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          if (b >= nb) continue;
+          s[b] = block_scale<kEPT>(x[b], p.block, wmax[phase]);
+          phase ^= 1;
+        }
+      }
+      if (e >= p.count) continue;
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
+        if (b >= nb) continue;
         const int r = r0 + b;
-        if (r >= p.n) continue;  // uniform across the CTA
-        float x[kEPT], c[kEPT];
-        if (EF)
-          add_each(x, xg[b], xe[b]);
-        else
-#pragma unroll
-          for (int w = 0; w < kEPT; ++w) x[w] = xg[b][w];
-        const float s = block_scale<kEPT>(x, p.block, wmax[phase]);
-        phase ^= 1;
-        if (e >= p.count) continue;
-        if ((e & (p.block - 1)) == 0) p.s[r][e >> shift] = s;
-        quant_group<kEPT>(x, s, c);
+        float c[kEPT];
+        if ((e & (p.block - 1)) == 0) p.s[r][e >> shift] = s[b];
+        quant_group<kEPT>(x[b], s[b], c);
         store_codes<kEPT>(p.q[r], e, p.count, c);
         if (EF) {
           float d[kEPT], res[kEPT];
-          mul_each(d, c, s);
-          sub_each(res, x, d);
+          mul_each(d, c, s[b]);
+          sub_each(res, x[b], d);
           store_group<false, kEPT>(p.e[r], e, p.count, res);
         }
       }
@@ -525,6 +578,21 @@ __global__ void __launch_bounds__(kThreads) compressed_reduce_kernel(const __gri
 // One rank's step of the fused pass for this thread's values x: quantise the
 // block, add the reconstruction d to the running sum (acc = d for rank 0)
 // and, with error feedback, return the residual x - d.
+template <int kEPT, bool EF, bool kLean = false>
+__device__ __forceinline__ void fold_scaled(const float (&x)[kEPT], int r, float s, float (&acc)[kEPT],
+                                            float (&res)[kEPT]) {
+  float c[kEPT], d[kEPT];
+  quant_group<kEPT, kLean>(x, s, c);
+  mul_each(d, c, s);
+  if (r == 0) {
+#pragma unroll
+    for (int w = 0; w < kEPT; ++w) acc[w] = d[w];
+  } else {
+    add_each(acc, acc, d);
+  }
+  if (EF) sub_each(res, x, d);
+}
+
 template <int kEPT, bool EF, bool kLean = false>
 __device__ __forceinline__ void fold_rank(const float (&x)[kEPT], int r, int block, float* wmax, float (&acc)[kEPT],
                                           float (&res)[kEPT]) {
@@ -959,16 +1027,21 @@ __global__ void __launch_bounds__(kThreads) compress_packed_kernel(const __grid_
 // Each tile, ranks in order: quantise rank r's block, add its reconstruction
 // to the running sum and store its residual; then write the scaled sum to
 // every rank. No message leaves the registers.
-template <bool BF16, bool EF>
+// NB: ranks per load batch. bf16 (with error feedback here; without, the
+// packed kernel above runs) takes one: fewer registers, more resident warps
+// (measured at 16 x 96 Mi: 0.97 of its bytes against 0.81 with two). fp32
+// keeps 2 / 4 (one or two measured 0-3 % slower). kBatch (blocks that span
+// warps): the batch's block scales come from batch_scales, one barrier per
+// batch instead of one per rank; at 16 x 192 MiB fp32, block 1024, 0.823 of
+// its bytes against 0.765 without error feedback, and with it 0.956 (4 ranks
+// per batch) against 0.918. Blocks within a warp keep block_scale per rank
+// (batch_scales measured 0.5 % slower there), and bf16 keeps one rank per
+// batch (two measured 0.73 against 0.88).
+template <bool BF16, bool EF, int NB, bool kBatch>
 __global__ void __launch_bounds__(kThreads) compressed_allreduce_kernel(const __grid_constant__ CompressParams p) {
   constexpr int kEPT = ept<BF16>();
   constexpr int kTileElems = kEPT * kThreads;
-  // Ranks per load batch. bf16 (with error feedback here; without, the
-  // pipelined kernel above runs) takes one: fewer registers, more resident
-  // warps (measured at 16 x 96 Mi: 0.97 of its bytes against 0.81 with two).
-  // fp32 keeps 2 / 4 (one or two measured 0-3 % slower).
-  constexpr int NB = BF16 ? 1 : (EF ? 2 : 4);
-  __shared__ float wmax[2][kWarps];
+  __shared__ float wmax[2][NB * kWarps];
   grid_dependency_wait();
   grid_dependents_launch();
   const int64_t n_tiles = (p.count + kTileElems - 1) / kTileElems;
@@ -978,26 +1051,44 @@ __global__ void __launch_bounds__(kThreads) compressed_allreduce_kernel(const __
     float acc[kEPT];
 #pragma unroll 1
     for (int r0 = 0; r0 < p.n; r0 += NB) {
-      float xg[NB][kEPT], xe[NB][kEPT];
+      const int nb = p.n - r0 < NB ? p.n - r0 : NB;  // uniform across the CTA
+      float x[NB][kEPT], xe[NB][kEPT];
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
-        if (r0 + b >= p.n) continue;
-        load_group<BF16, kEPT>(p.g[r0 + b], e, p.count, xg[b]);
+        if (b >= nb) continue;
+        load_group<BF16, kEPT>(p.g[r0 + b], e, p.count, x[b]);
         if (EF) load_group<false, kEPT>(p.e[r0 + b], e, p.count, xe[b]);
       }
+      if constexpr (kBatch) {
+        if (EF) {
 #pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        const int r = r0 + b;
-        if (r >= p.n) continue;  // uniform across the CTA
-        float x[kEPT], res[kEPT];
-        if (EF)
-          add_each(x, xg[b], xe[b]);
-        else
-#pragma unroll
-          for (int w = 0; w < kEPT; ++w) x[w] = xg[b][w];
-        fold_rank<kEPT, EF>(x, r, p.block, wmax[phase], acc, res);
+          for (int b = 0; b < NB; ++b)
+            if (b < nb) add_each(x[b], x[b], xe[b]);
+        }
+        float s[NB];
+        batch_scales<kEPT, NB>(x, nb, p.block, wmax[phase], s);
         phase ^= 1;
-        if (EF && e < p.count) store_group<false, kEPT>(p.e[r], e, p.count, res);
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          if (b >= nb) continue;
+          float res[kEPT];
+          fold_scaled<kEPT, EF>(x[b], r0 + b, s[b], acc, res);
+          if (EF && e < p.count) store_group<false, kEPT>(p.e[r0 + b], e, p.count, res);
+        }
+      } else {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          if (b >= nb) continue;
+          float xs[kEPT], res[kEPT];
+          if (EF)
+            add_each(xs, x[b], xe[b]);
+          else
+#pragma unroll
+            for (int w = 0; w < kEPT; ++w) xs[w] = x[b][w];
+          fold_rank<kEPT, EF>(xs, r0 + b, p.block, wmax[phase], acc, res);
+          phase ^= 1;
+          if (EF && e < p.count) store_group<false, kEPT>(p.e[r0 + b], e, p.count, res);
+        }
       }
     }
     if (e >= p.count) continue;
@@ -1069,7 +1160,9 @@ cudaError_t launch_compress(const CompressParams& p, ar_dtype dtype, cudaStream_
     if (k == nullptr) return cudaErrorInvalidValue;
     return launch(k, n_tiles(p.count, 8), p, stream);
   }
-  const Kern k = bf ? compress_kernel<true, true> : compress_kernel<false, true>;
+  const bool wide = p.block > 32 * compress_ept<false>();  // an fp32 block spans warps
+  const Kern k = bf ? compress_kernel<true, true, 1, false>
+                    : (wide ? compress_kernel<false, true, 4, true> : compress_kernel<false, true, 4, false>);
   return launch(k, n_tiles(p.count, bf ? compress_ept<true>() : compress_ept<false>()), p, stream);
 }
 
@@ -1098,8 +1191,13 @@ cudaError_t launch_compressed_allreduce(const CompressParams& p, ar_dtype dtype,
     const Kern k = packed_bf16_kernel(p.block);
     if (k != nullptr) return launch(k, n_tiles(p.count, ept<true>()), p, stream);
   }
-  const Kern k = bf ? (p.ef ? compressed_allreduce_kernel<true, true> : compressed_allreduce_bf16_kernel)
-                    : (p.ef ? compressed_allreduce_kernel<false, true> : compressed_allreduce_kernel<false, false>);
+  const bool wide = p.block > 32 * ept<false>();  // an fp32 block spans warps
+  Kern k = compressed_allreduce_bf16_kernel;
+  if (bf && p.ef)
+    k = compressed_allreduce_kernel<true, true, 1, false>;
+  else if (!bf)
+    k = p.ef ? (wide ? compressed_allreduce_kernel<false, true, 4, true> : compressed_allreduce_kernel<false, true, 2, false>)
+             : (wide ? compressed_allreduce_kernel<false, false, 4, true> : compressed_allreduce_kernel<false, false, 4, false>);
   return launch(k, n_tiles(p.count, bf ? ept<true>() : ept<false>()), p, stream);
 }
 
