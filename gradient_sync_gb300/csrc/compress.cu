@@ -25,6 +25,10 @@
 //  compressed_allreduce_bf16_packed_kernel  g -> out        (the same, bf16 without feedback,
 //                                                            even rank counts)
 //  compressed_allreduce_bf16_kernel  g -> out               (the same, odd rank counts)
+//  compressed_allreduce_warp_kernel  g, e -> e', out        (the fused pass with one block
+//                                                            per warp, for blocks that
+//                                                            span warps; see "one block
+//                                                            per warp")
 // The kernels without feedback keep the loads of the ranks ahead in flight
 // (pipelined loads, below); the packed ones decide codes with fewer
 // instructions (see "bf16 without feedback, packed").
@@ -1098,6 +1102,82 @@ __global__ void __launch_bounds__(kThreads) compressed_allreduce_kernel(const __
   }
 }
 
+// ---------------------------------------------------------------- one block per warp
+// Blocks of 256 or more fp32 values (512 or more bf16) span warps in the
+// kernels above, whose threads hold consecutive elements: the block maximum
+// then waits on a CTA barrier. Here a warp holds whole blocks: lane l takes
+// kVec vectors of kW elements, vector j at element j * 32 * kW + l * kW of
+// the block (each vector load of the warp is contiguous), so the block
+// maximum is one full-warp reduction and no barrier is needed. A CTA takes
+// kWarps blocks per tile. Per element the same operations in the same rank
+// order as the other kernels (block_scale, quant_group), so the same bits.
+// NB ranks per load batch.
+template <bool BF16, bool EF, int kVec, int NB>
+__global__ void __launch_bounds__(kThreads, 2) compressed_allreduce_warp_kernel(const __grid_constant__ CompressParams p) {
+  constexpr int kW = BF16 ? 8 : 4;
+  constexpr int kBlock = 32 * kW * kVec;
+  constexpr int64_t kTileElems = int64_t(kBlock) * kWarps;
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int64_t lane_off = int64_t(threadIdx.x >> 5) * kBlock + int64_t(threadIdx.x & 31) * kW;
+  const int64_t n_tiles = (p.count + kTileElems - 1) / kTileElems;
+  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const int64_t e0 = tile * kTileElems + lane_off;  // vector j at e0 + j * 32 * kW
+    float acc[kVec][kW];
+#pragma unroll 1
+    for (int r0 = 0; r0 < p.n; r0 += NB) {
+      float x[NB][kVec][kW], xe[EF ? NB : 1][EF ? kVec : 1][kW];
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        if (r0 + b >= p.n) continue;  // uniform across the CTA
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+          load_group<BF16, kW>(p.g[r0 + b], e0 + j * 32 * kW, p.count, x[b][j]);
+          if constexpr (EF) load_group<false, kW>(p.e[r0 + b], e0 + j * 32 * kW, p.count, xe[b][j]);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        const int r = r0 + b;
+        if (r >= p.n) continue;
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+          if constexpr (EF) add_each(x[b][j], x[b][j], xe[b][j]);
+#pragma unroll
+          for (int w = 0; w < kW; ++w) m = fmaxf(m, fabsf(x[b][j][w]));
+        }
+        // m >= 0: the unsigned maximum of the bits is the float maximum
+        m = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(m)));
+        const float s = div127(m);
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+          float c[kW], d[kW];
+          quant_group<kW, true>(x[b][j], s, c);
+          mul_each(d, c, s);
+          if (r == 0) {
+#pragma unroll
+            for (int w = 0; w < kW; ++w) acc[j][w] = d[w];
+          } else {
+            add_each(acc[j], acc[j], d);
+          }
+          if constexpr (EF) {
+            float res[kW];
+            sub_each(res, x[b][j], d);
+            store_group<false, kW>(p.e[r], e0 + j * 32 * kW, p.count, res);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) mul_each(acc[j], acc[j], p.scale);
+#pragma unroll 1
+    for (int r = 0; r < p.n; ++r)
+#pragma unroll
+      for (int j = 0; j < kVec; ++j) store_group<BF16, kW>(p.out[r], e0 + j * 32 * kW, p.count, acc[j]);
+  }
+}
+
 // The self-test of div127: every non-negative float bit pattern (finite,
 // +inf and NaN) against the IEEE division; the mismatches are counted.
 __device__ unsigned long long g_div127_mismatches;
@@ -1185,8 +1265,41 @@ Kern packed_bf16_kernel(int block) {
   }
 }
 
+// The one-block-per-warp kernel where it measured faster (nullptr
+// elsewhere). Gradient vectors per thread per load batch: fp32 16 (8 with
+// error feedback, whose residuals are loaded too), bf16 4 with error
+// feedback: every loaded value is held widened to fp32 until its rank is
+// folded. At 16 x 192 MiB (fp32) or 16 x 96 Mi (bf16), fraction of its bytes
+// against the kernels above: fp32 without error feedback, blocks 256 / 512 /
+// 1024: 0.929 / 0.886 / 0.922 against 0.858 / 0.843 / 0.823; fp32 with it,
+// block 1024: 0.977 against 0.957 (block 512 0.954 against 0.961, 256 the
+// same); bf16 with it, block 512: 0.787 against 0.772 (1024: 0.66 against
+// 0.77). bf16 without error feedback keeps the packed kernel (0.86 against
+// 0.40 here).
+template <bool BF16, bool EF>
+Kern warp_block_kernel(int block) {
+  if constexpr (!BF16 && !EF) {
+    if (block == 256) return compressed_allreduce_warp_kernel<false, false, 2, 8>;
+    if (block == 512) return compressed_allreduce_warp_kernel<false, false, 4, 4>;
+    if (block == 1024) return compressed_allreduce_warp_kernel<false, false, 8, 2>;
+  } else if constexpr (!BF16 && EF) {
+    if (block == 1024) return compressed_allreduce_warp_kernel<false, true, 8, 1>;
+  } else if constexpr (BF16 && EF) {
+    if (block == 512) return compressed_allreduce_warp_kernel<true, true, 2, 2>;
+  }
+  return nullptr;
+}
+
 cudaError_t launch_compressed_allreduce(const CompressParams& p, ar_dtype dtype, cudaStream_t stream) {
   const bool bf = dtype == AR_BF16;
+  {
+    const Kern k = bf ? (p.ef ? warp_block_kernel<true, true>(p.block) : warp_block_kernel<true, false>(p.block))
+                      : (p.ef ? warp_block_kernel<false, true>(p.block) : warp_block_kernel<false, false>(p.block));
+    if (k != nullptr) {
+      const int per_thread = p.block / 32;  // kVec vectors of kW elements
+      return launch(k, n_tiles(p.count, per_thread), p, stream);
+    }
+  }
   if (bf && !p.ef && p.n % 2 == 0) {
     const Kern k = packed_bf16_kernel(p.block);
     if (k != nullptr) return launch(k, n_tiles(p.count, ept<true>()), p, stream);
