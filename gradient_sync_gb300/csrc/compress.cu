@@ -1031,18 +1031,62 @@ __global__ void __launch_bounds__(kThreads) compress_packed_kernel(const __grid_
 // Each tile, ranks in order: quantise rank r's block, add its reconstruction
 // to the running sum and store its residual; then write the scaled sum to
 // every rank. No message leaves the registers.
-// NB: ranks per load batch. bf16 (with error feedback here; without, the
-// packed kernel above runs) takes one: fewer registers, more resident warps
-// (measured at 16 x 96 Mi: 0.97 of its bytes against 0.81 with two). fp32
-// keeps 2 / 4 (one or two measured 0-3 % slower). kBatch (blocks that span
-// warps): the batch's block scales come from batch_scales, one barrier per
-// batch instead of one per rank; at 16 x 192 MiB fp32, block 1024, 0.823 of
-// its bytes against 0.765 without error feedback, and with it 0.956 (4 ranks
-// per batch) against 0.918. Blocks within a warp keep block_scale per rank
-// (batch_scales measured 0.5 % slower there), and bf16 keeps one rank per
-// batch (two measured 0.73 against 0.88).
-template <bool BF16, bool EF, int NB, bool kBatch>
+template <bool BF16, bool EF>
 __global__ void __launch_bounds__(kThreads) compressed_allreduce_kernel(const __grid_constant__ CompressParams p) {
+  constexpr int kEPT = ept<BF16>();
+  constexpr int kTileElems = kEPT * kThreads;
+  // Ranks per load batch. bf16 (with error feedback here; without, the
+  // pipelined kernel above runs) takes one: fewer registers, more resident
+  // warps (measured at 16 x 96 Mi: 0.97 of its bytes against 0.81 with two).
+  // fp32 keeps 2 / 4 (one or two measured 0-3 % slower).
+  constexpr int NB = BF16 ? 1 : (EF ? 2 : 4);
+  __shared__ float wmax[2][kWarps];
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int64_t n_tiles = (p.count + kTileElems - 1) / kTileElems;
+  int phase = 0;
+  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const int64_t e = tile * kTileElems + int64_t(kEPT) * threadIdx.x;
+    float acc[kEPT];
+#pragma unroll 1
+    for (int r0 = 0; r0 < p.n; r0 += NB) {
+      float xg[NB][kEPT], xe[NB][kEPT];
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        if (r0 + b >= p.n) continue;
+        load_group<BF16, kEPT>(p.g[r0 + b], e, p.count, xg[b]);
+        if (EF) load_group<false, kEPT>(p.e[r0 + b], e, p.count, xe[b]);
+      }
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        const int r = r0 + b;
+        if (r >= p.n) continue;  // uniform across the CTA
+        float x[kEPT], res[kEPT];
+        if (EF)
+          add_each(x, xg[b], xe[b]);
+        else
+#pragma unroll
+          for (int w = 0; w < kEPT; ++w) x[w] = xg[b][w];
+        fold_rank<kEPT, EF>(x, r, p.block, wmax[phase], acc, res);
+        phase ^= 1;
+        if (EF && e < p.count) store_group<false, kEPT>(p.e[r], e, p.count, res);
+      }
+    }
+    if (e >= p.count) continue;
+    mul_each(acc, acc, p.scale);
+#pragma unroll 1
+    for (int r = 0; r < p.n; ++r) store_group<BF16, kEPT>(p.out[r], e, p.count, acc);
+  }
+}
+
+// The fused pass for fp32 blocks that span warps, where a block's maximum
+// needs a CTA barrier: the scales of a whole load batch of NB ranks come from
+// batch_scales, one barrier per batch instead of one per rank. Per element
+// the same operations in the same rank order as compressed_allreduce_kernel.
+// At 16 x 192 MiB fp32, block 1024 with error feedback (4 ranks per batch):
+// 0.956 of its bytes against 0.918; without it the warp kernel below runs.
+template <bool BF16, bool EF, int NB>
+__global__ void __launch_bounds__(kThreads) compressed_allreduce_batch_kernel(const __grid_constant__ CompressParams p) {
   constexpr int kEPT = ept<BF16>();
   constexpr int kTileElems = kEPT * kThreads;
   __shared__ float wmax[2][NB * kWarps];
@@ -1063,36 +1107,20 @@ __global__ void __launch_bounds__(kThreads) compressed_allreduce_kernel(const __
         load_group<BF16, kEPT>(p.g[r0 + b], e, p.count, x[b]);
         if (EF) load_group<false, kEPT>(p.e[r0 + b], e, p.count, xe[b]);
       }
-      if constexpr (kBatch) {
-        if (EF) {
+      if (EF) {
 #pragma unroll
-          for (int b = 0; b < NB; ++b)
-            if (b < nb) add_each(x[b], x[b], xe[b]);
-        }
-        float s[NB];
-        batch_scales<kEPT, NB>(x, nb, p.block, wmax[phase], s);
-        phase ^= 1;
+        for (int b = 0; b < NB; ++b)
+          if (b < nb) add_each(x[b], x[b], xe[b]);
+      }
+      float s[NB];
+      batch_scales<kEPT, NB>(x, nb, p.block, wmax[phase], s);
+      phase ^= 1;
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          if (b >= nb) continue;
-          float res[kEPT];
-          fold_scaled<kEPT, EF>(x[b], r0 + b, s[b], acc, res);
-          if (EF && e < p.count) store_group<false, kEPT>(p.e[r0 + b], e, p.count, res);
-        }
-      } else {
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          if (b >= nb) continue;
-          float xs[kEPT], res[kEPT];
-          if (EF)
-            add_each(xs, x[b], xe[b]);
-          else
-#pragma unroll
-            for (int w = 0; w < kEPT; ++w) xs[w] = x[b][w];
-          fold_rank<kEPT, EF>(xs, r0 + b, p.block, wmax[phase], acc, res);
-          phase ^= 1;
-          if (EF && e < p.count) store_group<false, kEPT>(p.e[r0 + b], e, p.count, res);
-        }
+      for (int b = 0; b < NB; ++b) {
+        if (b >= nb) continue;
+        float res[kEPT];
+        fold_scaled<kEPT, EF>(x[b], r0 + b, s[b], acc, res);
+        if (EF && e < p.count) store_group<false, kEPT>(p.e[r0 + b], e, p.count, res);
       }
     }
     if (e >= p.count) continue;
@@ -1307,10 +1335,10 @@ cudaError_t launch_compressed_allreduce(const CompressParams& p, ar_dtype dtype,
   const bool wide = p.block > 32 * ept<false>();  // an fp32 block spans warps
   Kern k = compressed_allreduce_bf16_kernel;
   if (bf && p.ef)
-    k = compressed_allreduce_kernel<true, true, 1, false>;
+    k = compressed_allreduce_kernel<true, true>;
   else if (!bf)
-    k = p.ef ? (wide ? compressed_allreduce_kernel<false, true, 4, true> : compressed_allreduce_kernel<false, true, 2, false>)
-             : (wide ? compressed_allreduce_kernel<false, false, 4, true> : compressed_allreduce_kernel<false, false, 4, false>);
+    k = p.ef ? (wide ? compressed_allreduce_batch_kernel<false, true, 4> : compressed_allreduce_kernel<false, true>)
+             : (wide ? compressed_allreduce_batch_kernel<false, false, 4> : compressed_allreduce_kernel<false, false>);
   return launch(k, n_tiles(p.count, bf ? ept<true>() : ept<false>()), p, stream);
 }
 
