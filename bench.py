@@ -28,6 +28,11 @@ Reported (one JSON line from rank 0):
                                  same gradients without error feedback)
                buckets_n8_transformer  8 ranks, 16-layer transformer bf16
                                  gradients in 25 MiB buckets, x1/8, bf16 out
+               sm_budget_n16_192mib  the headline's fused pass held to 32
+                                 and 64 SMs (sm_budget)
+               overlap_8192_tokens_32_sms  the bucketed sync of the 8-rank
+                                 transformer behind a synthetic backward
+                                 (exposed time, hidden fraction)
                sweep             2, 16 and 64 ranks x 1 GiB fp32, and
                                  16 ranks x 1 KiB (per-call latency)
   latency    small messages: the 16-rank ring and Rabenseifner at 1 KiB per
@@ -857,6 +862,34 @@ def run_workloads(dev, stream, peak, k_big: int, warmup: int):
     task, sample = _bucket_task()
     tasks.append(("buckets_n8_transformer", task, sample))
     del grads
+    torch.cuda.empty_cache()
+
+    # a launch held to a few SMs (sm_budget, what the overlap uses): the
+    # fused ring-order pass of the headline's size on 32 and 64 SMs' worth of
+    # CTAs, then the bucketed sync behind a synthetic backward (8 ranks, the
+    # 16-layer model's bf16 gradients, 8192 tokens, 32 SMs)
+    n, L = 16, 50_331_648
+    bufs = [device_uniform(L, r, dev) for r in range(n)]
+    outs = [torch.empty_like(b) for b in bufs]
+    k = max(3, k_big // 2)
+    paths = {}
+    for b in (32, 64):
+        plan = g.ar_plan(n, L, "f32", "fused", order="ring", sm_budget=b)
+        paths[f"fused_ring_order_{b}_sms"] = plan_path(plan, bufs, outs, n, L * 4, k, sm_budget=b)
+    out["sm_budget_n16_192mib"] = {
+        "workload": "fused ring-order all-reduce, 16 ranks x 192 MiB fp32, held to an SM budget", "n_ranks": n,
+        "count_per_rank": L, "bytes_per_rank": L * 4,
+        "inputs": "device-filled: torch.rand on the GPU (seed = rank), mapped to [-1, 1)",
+        "timing": f"median of {k} timings of 3 calls back to back", "paths": paths}
+    del bufs, outs
+    torch.cuda.empty_cache()
+    from gradient_sync_gb300.overlap import time_overlap
+
+    with torch.cuda.stream(stream):
+        ovl = time_overlap(n_ranks=8, tokens=8192, sm_budget=32, iters=5)
+    out["overlap_8192_tokens_32_sms"] = {
+        **ovl, "timing": "median of 5 timings each: the backward alone, the sync alone, both in sequence, "
+                         "both overlapped (sync on a second stream)"}
     torch.cuda.empty_cache()
 
     # the sweep's corners: 2, 16 and 64 ranks x 1 GiB fp32 (bandwidth) and
