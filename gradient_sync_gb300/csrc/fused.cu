@@ -281,8 +281,9 @@ __device__ __forceinline__ void load_batch(typename L::raw_t (&v)[NB][VPT], cons
 // The element-by-element head [clo, min(a0, chi)) and tail [a1, chi) of a
 // segment, done by the CTA that takes its first tile.
 template <class LS, int W>
+// owner >= 0: only that rank receives the result (the reduce-scatter).
 __device__ __forceinline__ void ragged_ends(const char* const* seq, char* const* out, int n, float scale,
-                                            int64_t clo, int64_t chi, int64_t a0, int64_t a1) {
+                                            int64_t clo, int64_t chi, int64_t a0, int64_t a1, int owner = -1) {
   int64_t es = -1;
   const int64_t head_end = a0 < chi ? a0 : chi;
   if (threadIdx.x < W - 1) {
@@ -299,11 +300,15 @@ __device__ __forceinline__ void ragged_ends(const char* const* seq, char* const*
     fold_single<LS, 8, 1>(acc, seq, n, es1, ok1);
     acc[0][0] = fmul(acc[0][0], scale);
     const typename LS::raw_t r = LS::narrow(acc[0]);
-    for (int q = 0; q < n; ++q) LS::store(out[q], es, r);
+    if (owner >= 0)
+      LS::store(out[owner], es, r);
+    else
+      for (int q = 0; q < n; ++q) LS::store(out[q], es, r);
   }
 }
 
-// Ring and rank order of the all-reduce (rotations of the rank list).
+// Ring and rank order of the all-reduce and of the reduce-scatter (rotations
+// of the rank list; the reduce-scatter stores only to the chunk's owner).
 // kRegPtr: the first batch's input pointers are kept in registers, reloaded
 // when the CTA moves to another segment, instead of read from the
 // shared-memory table for every tile; the host sets it for fp32 when one
@@ -408,12 +413,20 @@ __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_deep_kernel(con
         load_batch<LV, NB, VPT>(v, s_seq + seg_rotation(p, c2.seg), 0, n, e2, ok2);
       }
     }
-#pragma unroll 2
-    for (int d = 0; d < n; ++d)
+    if (p.collective == AR_REDUCE_SCATTER) {  // uniform across the grid
 #pragma unroll
       for (int q = 0; q < VPT; ++q)
-        if (ok[q]) LV::store(s_out[d], e[q], r[q]);
-    if (c.tt == 0 && c.clo < c.chi) ragged_ends<LS, W>(seq, s_out, n, p.scale, c.clo, c.chi, c.a0, c.a1);
+        if (ok[q]) LV::store(s_out[c.seg], e[q], r[q]);
+    } else {
+#pragma unroll 2
+      for (int d = 0; d < n; ++d)
+#pragma unroll
+        for (int q = 0; q < VPT; ++q)
+          if (ok[q]) LV::store(s_out[d], e[q], r[q]);
+    }
+    if (c.tt == 0 && c.clo < c.chi)
+      ragged_ends<LS, W>(seq, s_out, n, p.scale, c.clo, c.chi, c.a0, c.a1,
+                         p.collective == AR_REDUCE_SCATTER ? c.seg : -1);
     if (t2 >= total) break;
     t = t2;
     c = c2;
@@ -674,9 +687,9 @@ int deep_vpt(int n, bool bf16) {
 // 4 ranks takes 2 vectors per thread with 8 ranks per batch.
 int fused_vpt(int n, int order, int collective, bool bf16, bool deep) {
   if (collective == AR_ALLGATHER) return kAgVPT;
-  if (collective == AR_REDUCE_SCATTER && order != AR_ORDER_TREE && n > 4) return kRsVPT;
   if (order == AR_ORDER_TREE) return 1;
-  if (deep && collective == AR_ALLREDUCE && order != AR_ORDER_HIER) return deep_vpt(n, bf16);
+  if (deep && order != AR_ORDER_HIER) return deep_vpt(n, bf16);  // all-reduce or reduce-scatter
+  if (collective == AR_REDUCE_SCATTER && n > 4) return kRsVPT;
   if (deep && n > 4) return 2;
   return n <= 2 ? 4 : n <= 4 ? 2 : 1;
 }
@@ -701,12 +714,7 @@ template <bool BF16>
 cudaError_t launch_fused_rot(const FusedParams& p, int64_t tiles, int sm_budget, cudaStream_t stream) {
   if (p.order == AR_ORDER_TREE && p.collective != AR_ALLGATHER)
     return launch_persistent(fused_flat_kernel<BF16, true, kSeqRotated, 8, 1>, p, tiles, sm_budget, stream);
-  if (p.collective == AR_REDUCE_SCATTER && p.n > 4)
-    return launch_persistent(fused_flat_kernel<BF16, false, kSeqRotatedPos, kRsNB, kRsVPT>, p, tiles, sm_budget,
-                             stream);
-  if (p.collective == AR_ALLGATHER)
-    return launch_persistent(fused_flat_kernel<BF16, false, kSeqRotated, 1, kAgVPT>, p, tiles, sm_budget, stream);
-  if (budgeted(sm_budget) && p.collective == AR_ALLREDUCE) {  // ring or rank order
+  if (budgeted(sm_budget) && p.collective != AR_ALLGATHER) {  // ring or rank order
     const bool reg = !BF16 && p.n <= deep_nb(p.n);  // one batch holds every rank
     switch (deep_nb(p.n)) {
       case 16:
@@ -717,6 +725,11 @@ cudaError_t launch_fused_rot(const FusedParams& p, int64_t tiles, int sm_budget,
       default: return launch_persistent(fused_deep_kernel<BF16, 2, BF16 ? 4 : 5, !BF16>, p, tiles, sm_budget, stream);
     }
   }
+  if (p.collective == AR_REDUCE_SCATTER && p.n > 4)
+    return launch_persistent(fused_flat_kernel<BF16, false, kSeqRotatedPos, kRsNB, kRsVPT>, p, tiles, sm_budget,
+                             stream);
+  if (p.collective == AR_ALLGATHER)
+    return launch_persistent(fused_flat_kernel<BF16, false, kSeqRotated, 1, kAgVPT>, p, tiles, sm_budget, stream);
   switch (fused_vpt(p.n, p.order, p.collective, BF16, false)) {
     case 4: return launch_persistent(fused_flat_kernel<BF16, false, kSeqRotated, 2, 4>, p, tiles, sm_budget, stream);
     case 2: return launch_persistent(fused_flat_kernel<BF16, false, kSeqRotated, 4, 2>, p, tiles, sm_budget, stream);

@@ -45,14 +45,17 @@ def _run(g, x, dtype, algo, coll, order="ring", scale=1.0, out_of_place=False, k
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("algo,order", [("ring", "ring"), ("fused", "ring"), ("fused", "rank"), ("fused", "tree")])
+@pytest.mark.parametrize("algo,order,sm_budget", [("ring", "ring", 0), ("fused", "ring", 0), ("fused", "rank", 0),
+                                                  ("fused", "tree", 0), ("fused", "ring", 7), ("fused", "rank", 7)])
 @pytest.mark.parametrize("N,L", SIZES)
-def test_reduce_scatter(g, dtype, algo, order, N, L):
+def test_reduce_scatter(g, dtype, algo, order, sm_budget, N, L):
+    """Every rank's own chunk of the reduced sum; held to a few SMs the fused
+    pass runs the kernel that loads the next tile during this tile's store."""
     if order == "tree" and N & (N - 1):
         pytest.skip("tree order needs a power-of-two rank count")
     scale = 0.25 if L % 2 else 1.0
     x = workloads.all_ranks(workloads.small_spec(N, L, dtype, "normal", seed=N + 3 * L))
-    got = _run(g, x, dtype, algo, "reduce_scatter", order, scale, out_of_place=(N % 2 == 0))
+    got = _run(g, x, dtype, algo, "reduce_scatter", order, scale, out_of_place=(N % 2 == 0), sm_budget=sm_budget)
     xf = widened(x, dtype)
     if algo == "ring":
         finish = schedules.finish_bf16(scale) if dtype == "bf16" else schedules.finish_scale(scale)

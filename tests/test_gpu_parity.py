@@ -256,8 +256,8 @@ def test_fused_bulk_copy_pipeline_matches_oracle(g, dtype, order, N, L, sm_budge
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("order", ["ring", "rank", "hier"])
-@pytest.mark.parametrize("N,L", [(2, 70001), (3, 1001), (4, 12345), (5, 4099), (8, 20003), (12, 33333),
-                                 (16, 100003), (64, 5001)])
+@pytest.mark.parametrize("N,L", [(1, 9), (1, 40001), (2, 70001), (3, 1001), (4, 12345), (5, 4099), (8, 20003),
+                                 (12, 33333), (16, 100003), (64, 5001)])
 def test_fused_register_pipeline_with_sm_budget(g, dtype, order, N, L):
     """A launch held to fewer SMs than the GPU has runs the variants with more
     loads in flight per thread (for more than 4 ranks in ring or rank order,
