@@ -268,6 +268,39 @@ __device__ __forceinline__ void add_batch(float (&part)[VPT][L::W], const typena
   }
 }
 
+// The tree order's add of batch `base`: ranks arrive in index order and are
+// combined with fold_tree's binary counter (slot l holds a finished subtree
+// of 2^l ranks; before rank r arrives the occupied slots are the set bits of
+// r), so a batch at a time gives fold_tree's bits.
+template <class L, int NB, int kLevels>
+__device__ __forceinline__ void add_batch_tree(float (&slot)[kLevels][L::W], const typename L::raw_t (&v)[NB][1],
+                                               int base, int n, bool ok) {
+  if (!ok) return;
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    if (base + b < n) {
+      float carry[L::W];
+      L::widen(v[b][0], carry);
+      int bits = base + b;
+      bool placed = false;
+#pragma unroll
+      for (int l = 0; l < kLevels; ++l) {
+        if (!placed) {
+          if (bits & 1) {
+#pragma unroll
+            for (int w = 0; w < L::W; ++w) carry[w] = fadd(slot[l][w], carry[w]);
+            bits >>= 1;
+          } else {
+#pragma unroll
+            for (int w = 0; w < L::W; ++w) slot[l][w] = carry[w];
+            placed = true;
+          }
+        }
+      }
+    }
+  }
+}
+
 template <class L, int NB, int VPT>
 __device__ __forceinline__ void load_batch(typename L::raw_t (&v)[NB][VPT], const char* const* seq, int base, int n,
                                            const int64_t (&e)[VPT], const bool (&ok)[VPT]) {
@@ -279,9 +312,10 @@ __device__ __forceinline__ void load_batch(typename L::raw_t (&v)[NB][VPT], cons
 }
 
 // The element-by-element head [clo, min(a0, chi)) and tail [a1, chi) of a
-// segment, done by the CTA that takes its first tile.
-template <class LS, int W>
-// owner >= 0: only that rank receives the result (the reduce-scatter).
+// segment, done by the CTA that takes its first tile. owner >= 0: only that
+// rank receives the result (the reduce-scatter). TREE: the elements fold in
+// the tree order (fold_tree), else in sequence (fold_single).
+template <class LS, int W, bool TREE = false>
 __device__ __forceinline__ void ragged_ends(const char* const* seq, char* const* out, int n, float scale,
                                             int64_t clo, int64_t chi, int64_t a0, int64_t a1, int owner = -1) {
   int64_t es = -1;
@@ -297,7 +331,10 @@ __device__ __forceinline__ void ragged_ends(const char* const* seq, char* const*
     float acc[1][1];
     const int64_t es1[1] = {es};
     const bool ok1[1] = {true};
-    fold_single<LS, 8, 1>(acc, seq, n, es1, ok1);
+    if constexpr (TREE)
+      fold_tree<LS, 8>(acc[0], seq, n, es);
+    else
+      fold_single<LS, 8, 1>(acc, seq, n, es1, ok1);
     acc[0][0] = fmul(acc[0][0], scale);
     const typename LS::raw_t r = LS::narrow(acc[0]);
     if (owner >= 0)
@@ -317,8 +354,11 @@ __device__ __forceinline__ void ragged_ends(const char* const* seq, char* const*
 // 0.556 against 0.551), except 3-4 ranks (4 x 4 vectors: 0.664 against
 // 0.682); bf16, whose sums take more registers, and 64 ranks measured about
 // 1 % slower with it.
-template <bool BF16, int NB, int VPT, bool kRegPtr>
+// TREE: Rabenseifner's order (rank order, combined as fold_tree does; one
+// vector per thread, n a power of two below 2^kLevels).
+template <bool BF16, int NB, int VPT, bool kRegPtr, bool TREE = false, int kLevels = kTreeLevels>
 __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_deep_kernel(const __grid_constant__ FusedParams p) {
+  static_assert(!TREE || VPT == 1, "the tree order takes one vector per thread");
   using LV = Lane<BF16, true>;
   using LS = Lane<BF16, false>;
   constexpr int W = LV::W;
@@ -384,11 +424,27 @@ __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_deep_kernel(con
   for (;;) {
     const char* const* seq = s_seq + seg_rotation(p, c.seg);
     float part[VPT][W];
-    add_batch<LV, NB, VPT>(part, v, 0, n, ok);
+    if constexpr (TREE) {
+      float slot[kLevels][W];
+      add_batch_tree<LV, NB, kLevels>(slot, v, 0, n, ok[0]);
 #pragma unroll 1
-    for (int base = NB; base < n; base += NB) {
-      load_batch<LV, NB, VPT>(v, seq, base, n, e, ok);
-      add_batch<LV, NB, VPT>(part, v, base, n, ok);
+      for (int base = NB; base < n; base += NB) {
+        load_batch<LV, NB, VPT>(v, seq, base, n, e, ok);
+        add_batch_tree<LV, NB, kLevels>(slot, v, base, n, ok[0]);
+      }
+#pragma unroll
+      for (int l = 0; l < kLevels; ++l)  // n = 2^K: the whole tree sits in slot K
+        if ((1 << l) == n) {
+#pragma unroll
+          for (int w = 0; w < W; ++w) part[0][w] = slot[l][w];
+        }
+    } else {
+      add_batch<LV, NB, VPT>(part, v, 0, n, ok);
+#pragma unroll 1
+      for (int base = NB; base < n; base += NB) {
+        load_batch<LV, NB, VPT>(v, seq, base, n, e, ok);
+        add_batch<LV, NB, VPT>(part, v, base, n, ok);
+      }
     }
     typename LV::raw_t r[VPT];
 #pragma unroll
@@ -425,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_deep_kernel(con
           if (ok[q]) LV::store(s_out[d], e[q], r[q]);
     }
     if (c.tt == 0 && c.clo < c.chi)
-      ragged_ends<LS, W>(seq, s_out, n, p.scale, c.clo, c.chi, c.a0, c.a1,
+      ragged_ends<LS, W, TREE>(seq, s_out, n, p.scale, c.clo, c.chi, c.a0, c.a1,
                          p.collective == AR_REDUCE_SCATTER ? c.seg : -1);
     if (t2 >= total) break;
     t = t2;
@@ -712,8 +768,19 @@ int64_t bucket_tile_elems(ar_dtype dtype, int n, bool v8, bool deep) {
 // reduce-scatter, and read from shared memory otherwise (fold_single).
 template <bool BF16>
 cudaError_t launch_fused_rot(const FusedParams& p, int64_t tiles, int sm_budget, cudaStream_t stream) {
-  if (p.order == AR_ORDER_TREE && p.collective != AR_ALLGATHER)
+  if (p.order == AR_ORDER_TREE && p.collective != AR_ALLGATHER) {  // n is a power of two
+    // budgeted: the deep kernel, 16 ranks per batch (bf16, whose wider sums
+    // take twice the registers, 8, and only up to 16 ranks: 5 tree levels)
+    if (budgeted(sm_budget)) {
+      if constexpr (BF16) {
+        if (p.n <= 16) return launch_persistent(fused_deep_kernel<true, 8, 1, false, true, 5>, p, tiles, sm_budget, stream);
+      } else {
+        return p.n >= 16 ? launch_persistent(fused_deep_kernel<false, 16, 1, false, true>, p, tiles, sm_budget, stream)
+                         : launch_persistent(fused_deep_kernel<false, 8, 1, false, true>, p, tiles, sm_budget, stream);
+      }
+    }
     return launch_persistent(fused_flat_kernel<BF16, true, kSeqRotated, 8, 1>, p, tiles, sm_budget, stream);
+  }
   if (budgeted(sm_budget) && p.collective != AR_ALLGATHER) {  // ring or rank order
     const bool reg = !BF16 && p.n <= deep_nb(p.n);  // one batch holds every rank
     switch (deep_nb(p.n)) {

@@ -46,7 +46,8 @@ def _run(g, x, dtype, algo, coll, order="ring", scale=1.0, out_of_place=False, k
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("algo,order,sm_budget", [("ring", "ring", 0), ("fused", "ring", 0), ("fused", "rank", 0),
-                                                  ("fused", "tree", 0), ("fused", "ring", 7), ("fused", "rank", 7)])
+                                                  ("fused", "tree", 0), ("fused", "ring", 7), ("fused", "rank", 7),
+                                                  ("fused", "tree", 7)])
 @pytest.mark.parametrize("N,L", SIZES)
 def test_reduce_scatter(g, dtype, algo, order, sm_budget, N, L):
     """Every rank's own chunk of the reduced sum; held to a few SMs the fused

@@ -255,16 +255,18 @@ def test_fused_bulk_copy_pipeline_matches_oracle(g, dtype, order, N, L, sm_budge
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("order", ["ring", "rank", "hier"])
+@pytest.mark.parametrize("order", ["ring", "rank", "hier", "tree"])
 @pytest.mark.parametrize("N,L", [(1, 9), (1, 40001), (2, 70001), (3, 1001), (4, 12345), (5, 4099), (8, 20003),
-                                 (12, 33333), (16, 100003), (64, 5001)])
+                                 (12, 33333), (16, 100003), (32, 7777), (64, 5001)])
 def test_fused_register_pipeline_with_sm_budget(g, dtype, order, N, L):
     """A launch held to fewer SMs than the GPU has runs the variants with more
-    loads in flight per thread (for more than 4 ranks in ring or rank order,
-    the next tile's first batch is loaded during this tile's stores); their
-    result is the oracle's, bit for bit, in and out of place."""
+    loads in flight per thread (in ring, rank and tree order the next tile's
+    first batch is loaded during this tile's stores); their result is the
+    oracle's, bit for bit, in and out of place."""
     if order == "hier" and N % 2:
         pytest.skip("the hierarchical order needs a group size that divides N")
+    if order == "tree" and (N < 2 or N & (N - 1)):
+        pytest.skip("the tree order needs a power-of-two rank count")
     G = _group(N) if order == "hier" else 0
     x = workloads.all_ranks(workloads.small_spec(N, L, dtype, "normal", seed=N * 5 + L))
     want = expected("fused", order, x, dtype, G, 0.5)
