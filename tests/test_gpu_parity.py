@@ -280,7 +280,7 @@ def test_fused_register_pipeline_with_sm_budget(g, dtype, order, N, L):
             assert_bits_equal(to_host((outs or devs)[r], dtype), want, f"rank {r}")
 
 
-@pytest.mark.parametrize("order", ["ring", "rank"])
+@pytest.mark.parametrize("order", ["ring", "rank", "hier", "tree"])
 def test_execute_host_slabs_with_sm_budget(g, order):
     """Pageable host buffers go through the device in slabs, one launch per
     element range; the ranges cut the ring's chunks mid-way, and the launches
@@ -290,9 +290,10 @@ def test_execute_host_slabs_with_sm_budget(g, order):
     host_in = [torch.from_numpy(x[r].copy()) for r in range(N)]
     host_out = [torch.empty(L, dtype=torch.float32) for _ in range(N)]
     dev = [torch.empty(L, dtype=torch.float32, device="cuda") for _ in range(N)]
-    plan = g.ar_plan(N, L, "f32", "fused", order=order, sm_budget=6, kernel="loads")
+    G = 4 if order == "hier" else 0
+    plan = g.ar_plan(N, L, "f32", "fused", order=order, group_size=G, sm_budget=6, kernel="loads")
     g.ar_execute_host(plan, host_in, host_out, dev)
-    want = expected("fused", order, x, "f32")
+    want = expected("fused", order, x, "f32", G)
     for r in range(N):
         assert_bits_equal(host_out[r].numpy(), want, f"rank {r}")
 
