@@ -85,15 +85,16 @@ ALLREDUCE = [("ring", "ring", 0, None), ("rabenseifner", "ring", 0, None), ("hie
 @pytest.mark.parametrize("algo,order,G,dims", ALLREDUCE)
 def test_allreduce_stays_inside_its_buffers(g, algo, order, G, dims, dtype, align16):
     N = 8
-    kernels = ["loads", "bulk"] if algo == "fused" else ["auto"]
+    # the fused pass: register pipeline, bulk copies, and held to a few SMs
+    kernels = [("loads", 0), ("bulk", 0), ("loads", 7)] if algo == "fused" else [("auto", 0)]
     for L in (4099, 37):
         x = workloads.all_ranks(workloads.small_spec(N, L, dtype, "normal", seed=L + 11 * N))
         scale = 0.5 if L % 2 else 1.0
         want = expected(algo, order, x, dtype, group_size=G, scale=scale, torus_dims=dims)
-        for kernel in kernels:
+        for kernel, sm_budget in kernels:
             for out_of_place in (False, True):
                 plan = g.ar_plan(N, L, dtype, algo, group_size=G, order=order, scale=scale, kernel=kernel,
-                                 torus_dims=dims or (0, 0, 0))
+                                 torus_dims=dims or (0, 0, 0), sm_budget=sm_budget)
                 ws_bytes = plan.stats["workspace_bytes"]
                 shapes = [(L, dtype)] * N + ([(L, dtype)] * N if out_of_place else [])
                 shapes += [(ws_bytes, "u8")] if ws_bytes else []
@@ -103,7 +104,8 @@ def test_allreduce_stays_inside_its_buffers(g, algo, order, G, dims, dtype, alig
                 outs = [a[N + r] for r in range(N)] if out_of_place else None
                 ws = a[len(shapes) - 1] if ws_bytes else None
                 g.ar_execute(plan, [a[r] for r in range(N)], outs=outs, workspace=ws)
-                what = f"{algo}/{order} {kernel} L={L} {'out of place' if out_of_place else 'in place'}"
+                what = (f"{algo}/{order} {kernel} sm_budget={sm_budget} L={L} "
+                        f"{'out of place' if out_of_place else 'in place'}")
                 a.check_guards(what)
                 for r in range(N):
                     got = to_host(outs[r] if out_of_place else a[r], dtype)
@@ -112,10 +114,15 @@ def test_allreduce_stays_inside_its_buffers(g, algo, order, G, dims, dtype, alig
 
 @pytest.mark.parametrize("align16", [True, False])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("algo,coll,kernel", [("ring", "reduce_scatter", "auto"), ("fused", "reduce_scatter", "auto"),
-                                              ("ring", "allgather", "auto"), ("fused", "allgather", "loads"),
-                                              ("fused", "allgather", "bulk")])
-def test_collectives_stay_inside_their_buffers(g, algo, coll, kernel, dtype, align16):
+@pytest.mark.parametrize("algo,coll,kernel,sm_budget,out_of_place",
+                         [("ring", "reduce_scatter", "auto", 0, False), ("fused", "reduce_scatter", "auto", 0, False),
+                          ("fused", "reduce_scatter", "loads", 5, False), ("ring", "allgather", "auto", 0, False),
+                          ("ring", "allgather", "auto", 0, True), ("fused", "allgather", "loads", 0, False),
+                          ("fused", "allgather", "bulk", 0, False), ("fused", "allgather", "bulk", 0, True)])
+def test_collectives_stay_inside_their_buffers(g, algo, coll, kernel, sm_budget, out_of_place, dtype, align16):
+    """Out of place the ring all-gather's first step also writes each sent
+    chunk to the sender's output; held to a few SMs the reduce-scatter runs
+    the kernel that loads ahead across tiles."""
     N, L = 5, 20011
     x = workloads.all_ranks(workloads.small_spec(N, L, dtype, "uniform", seed=3 + L))
     xf = widened(x, dtype)
@@ -129,15 +136,19 @@ def test_collectives_stay_inside_their_buffers(g, algo, coll, kernel, dtype, ali
     else:
         s = numerics.fused_sum(xf, "ring_rs")
         want = [numerics.f32_to_bf16_rne(s) if dtype == "bf16" else s] * N
-    plan = g.ar_plan(N, L, dtype, algo, collective=coll, kernel=kernel)
+    plan = g.ar_plan(N, L, dtype, algo, collective=coll, kernel=kernel, sm_budget=sm_budget)
     ws_bytes = plan.stats["workspace_bytes"]
-    a = Arena([(L, dtype)] * N + ([(ws_bytes, "u8")] if ws_bytes else []), align16)
+    shapes = [(L, dtype)] * N + ([(L, dtype)] * N if out_of_place else [])
+    a = Arena(shapes + ([(ws_bytes, "u8")] if ws_bytes else []), align16)
     for r in range(N):
         _fill(a[r], x[r], dtype)
-    g.ar_execute(plan, [a[r] for r in range(N)], workspace=a[N] if ws_bytes else None)
-    a.check_guards(f"{algo} {coll} {kernel}")
+    outs = [a[N + r] for r in range(N)] if out_of_place else None
+    g.ar_execute(plan, [a[r] for r in range(N)], outs=outs, workspace=a[len(shapes)] if ws_bytes else None)
+    a.check_guards(f"{algo} {coll} {kernel} sm_budget={sm_budget} out_of_place={out_of_place}")
     for r in range(N):
-        got = to_host(a[r], dtype)
+        got = to_host(outs[r] if out_of_place else a[r], dtype)
+        if out_of_place:
+            np.testing.assert_array_equal(to_host(a[r], dtype), x[r])
         if coll == "allgather":
             assert_bits_equal(got, want[r], f"rank {r}")
         else:
@@ -160,7 +171,7 @@ def test_bucket_calls_stay_inside_their_buffers(g, align16):
         lo, hi = min(b), max(b) + 1
         Lb = sum(counts[t] for t in b)
         want = ob.sync_bucket(grads, b, counts, scale)
-        for path in ("pack", "fused_loads", "fused_bulk"):
+        for path in ("pack", "fused_loads", "fused_bulk", "fused_loads_budget"):
             shapes = [(counts[t], "bf16") for r in range(N) for t in range(nt)]
             shapes += [(Lb, "f32")] * N if path == "pack" else []
             a = Arena(shapes, align16)
@@ -173,8 +184,9 @@ def test_bucket_calls_stay_inside_their_buffers(g, align16):
                 g.ar_bucket_pack(tensors, counts, lo, hi, "bf16", bucket)
                 g.ar_execute(g.ar_plan(N, Lb, "f32", "ring"), bucket)
                 g.ar_bucket_unpack(bucket, scale, "bf16", tensors, counts, lo, hi)
-            else:
-                g.ar_bucket_allreduce(tensors, counts, lo, hi, "bf16", scale, kernel=path.split("_")[1])
+            else:  # the budgeted launch runs the kernel that loads ahead across tiles
+                g.ar_bucket_allreduce(tensors, counts, lo, hi, "bf16", scale, kernel=path.split("_")[1],
+                                      sm_budget=5 if path.endswith("budget") else 0)
             a.check_guards(f"bucket {lo}..{hi} {path}")
             for r in range(N):
                 for t in range(nt):
@@ -185,8 +197,10 @@ def test_bucket_calls_stay_inside_their_buffers(g, align16):
 @pytest.mark.parametrize("align16", [True, False])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("ef", [False, True])
-def test_compression_stays_inside_its_buffers(g, dtype, ef, align16):
-    N, block = 5, 64
+@pytest.mark.parametrize("block", [64, 512, 1024])
+def test_compression_stays_inside_its_buffers(g, dtype, ef, block, align16):
+    """Blocks of 512 and 1024 run the kernels for blocks that span warps."""
+    N = 5
     for L in (4103, 23):
         rng = np.random.default_rng(L + 7)
         xf = (rng.standard_normal((N, L)) * 1e-2).astype(np.float32)
