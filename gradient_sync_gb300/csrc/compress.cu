@@ -239,6 +239,17 @@ __device__ __forceinline__ float rcp_approx(float s) {
   return r;
 }
 
+// Barrier over the W warps (a power of two, W <= kWarps) that hold one block:
+// named barrier 1 + warp / W of W * 32 threads, the whole CTA when W = kWarps.
+// The warps of other blocks in the CTA do not wait.
+__device__ __forceinline__ void block_group_sync(int W) {
+  if (W >= kWarps) {
+    __syncthreads();
+    return;
+  }
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + (int(threadIdx.x) >> 5) / W), "r"(W * 32) : "memory");
+}
+
 // The block's scale s = max|x| / 127 for this thread's kEPT values.
 // `wmax` is this call's shared-memory slot; callers alternate two slots, so
 // one barrier per call suffices (a warp that writes the next call's slot has
@@ -284,8 +295,10 @@ __device__ __forceinline__ float block_scale(const float (&x)[kEPT], int block, 
 // with block_scale's arithmetic. For blocks that span warps, the warps'
 // maxima of all NB ranks go to shared memory together and one barrier serves
 // the batch instead of one per rank (wm: the batch's slot of NB x kWarps
-// floats; callers alternate two slots, as for block_scale).
-template <int kEPT, int NB>
+// floats; callers alternate two slots, as for block_scale). kGroupSync: the
+// barrier holds only the block's own warps (the fused pass, fp32 block 512:
+// 0.986 of its bytes against 0.964; the compressor measured 1 % slower).
+template <int kEPT, int NB, bool kGroupSync = false>
 __device__ __forceinline__ void batch_scales(const float (&x)[NB][kEPT], int nb, int block, float* wm,
                                              float (&s)[NB]) {
   constexpr int kWarpElems = 32 * kEPT;
@@ -306,8 +319,11 @@ __device__ __forceinline__ void batch_scales(const float (&x)[NB][kEPT], int nb,
 #pragma unroll
       for (int b = 0; b < NB; ++b) wm[b * kWarps + warp] = m[b];
     }
-    __syncthreads();
     const int W = block / kWarpElems;
+    if (kGroupSync)
+      block_group_sync(W);
+    else
+      __syncthreads();
     const int w0 = warp & ~(W - 1);
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
@@ -752,11 +768,11 @@ __device__ __forceinline__ void lean_bf16_rank(const float (&x)[8], float* wm, P
 #pragma unroll
     for (int o = kLanes / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
   }
-  if constexpr (kBlock > 32 * 8) {
-    constexpr int W = kBlock / (32 * 8);
-    const int warp = threadIdx.x >> 5;
+  if constexpr (kBlock > 32 * 8) {  // the block's own warps wait, not the CTA's (block 512: 0.965
+    constexpr int W = kBlock / (32 * 8);  // of its bytes against 0.870 with a CTA barrier, 1024: 0.927
+    const int warp = threadIdx.x >> 5;     // against 0.874)
     if ((threadIdx.x & 31) == 0) wm[warp] = m;
-    __syncthreads();
+    block_group_sync(W);
     const int w0 = warp & ~(W - 1);
     m = wm[w0];
 #pragma unroll
@@ -895,7 +911,11 @@ __global__ void __launch_bounds__(kThreads) compressed_allreduce_bf16_packed_ker
 // being quantised, over two load buffers.
 
 // The message of one pair: x holds the 8 values at element e of rank r.
-template <int kLogBlock>
+// kGroupSync: blocks that span warps wait on a barrier of their own warps
+// only (the bf16 compressor: block 1024 0.813 of its bytes against 0.797
+// with a CTA barrier; fp32 measured 0.83 against 0.94 and keeps the CTA
+// barrier).
+template <int kLogBlock, bool kGroupSync>
 __device__ __forceinline__ void packed_message(const float (&x)[8], float* wm, int8_t* q, float* sc, int64_t e) {
   constexpr int kBlock = 1 << kLogBlock;
   constexpr int kLanes = kBlock >= 32 * 8 ? 32 : kBlock / 8;
@@ -920,7 +940,10 @@ __device__ __forceinline__ void packed_message(const float (&x)[8], float* wm, i
     constexpr int W = kBlock / (32 * 8);
     const int warp = threadIdx.x >> 5;
     if ((threadIdx.x & 31) == 0) wm[warp] = m;
-    __syncthreads();
+    if (kGroupSync)
+      block_group_sync(W);
+    else
+      __syncthreads();
     const int w0 = warp & ~(W - 1);
     m = wm[w0];
 #pragma unroll
@@ -998,7 +1021,7 @@ __global__ void __launch_bounds__(kThreads) compress_packed_kernel(const __grid_
     float x[kEPT];
     widen_raw<BF16, kEPT>(w, x);
     fetch(w);
-    packed_message<kLogBlock>(x, wmax[phase], p.q[c_r], p.s[c_r], c_off);
+    packed_message<kLogBlock, BF16>(x, wmax[phase], p.q[c_r], p.s[c_r], c_off);
     phase ^= 1;
     if (++c_r == n) {
       c_r = 0;
@@ -1113,7 +1136,7 @@ __global__ void __launch_bounds__(kThreads) compressed_allreduce_batch_kernel(co
           if (b < nb) add_each(x[b], x[b], xe[b]);
       }
       float s[NB];
-      batch_scales<kEPT, NB>(x, nb, p.block, wmax[phase], s);
+      batch_scales<kEPT, NB, true>(x, nb, p.block, wmax[phase], s);
       phase ^= 1;
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
