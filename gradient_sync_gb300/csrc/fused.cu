@@ -301,6 +301,39 @@ __device__ __forceinline__ void add_batch_tree(float (&slot)[kLevels][L::W], con
   }
 }
 
+// The same over VPT vectors per thread (a slot set per vector).
+template <class L, int NB, int VPT, int kLevels>
+__device__ __forceinline__ void add_batch_tree_v(float (&slot)[VPT][kLevels][L::W], const typename L::raw_t (&v)[NB][VPT],
+                                               int base, int n, const bool (&ok)[VPT]) {
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    if (base + b < n) {
+#pragma unroll
+      for (int q = 0; q < VPT; ++q) {
+        if (!ok[q]) continue;
+        float carry[L::W];
+        L::widen(v[b][q], carry);
+        int bits = base + b;
+        bool placed = false;
+#pragma unroll
+        for (int l = 0; l < kLevels; ++l) {
+          if (!placed) {
+            if (bits & 1) {
+#pragma unroll
+              for (int w = 0; w < L::W; ++w) carry[w] = fadd(slot[q][l][w], carry[w]);
+              bits >>= 1;
+            } else {
+#pragma unroll
+              for (int w = 0; w < L::W; ++w) slot[q][l][w] = carry[w];
+              placed = true;
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
 template <class L, int NB, int VPT>
 __device__ __forceinline__ void load_batch(typename L::raw_t (&v)[NB][VPT], const char* const* seq, int base, int n,
                                            const int64_t (&e)[VPT], const bool (&ok)[VPT]) {
@@ -354,11 +387,10 @@ __device__ __forceinline__ void ragged_ends(const char* const* seq, char* const*
 // 0.556 against 0.551), except 3-4 ranks (4 x 4 vectors: 0.664 against
 // 0.682); bf16, whose sums take more registers, and 64 ranks measured about
 // 1 % slower with it.
-// TREE: Rabenseifner's order (rank order, combined as fold_tree does; one
-// vector per thread, n a power of two below 2^kLevels).
+// TREE: Rabenseifner's order (rank order, combined as fold_tree does; n a
+// power of two below 2^kLevels).
 template <bool BF16, int NB, int VPT, bool kRegPtr, bool TREE = false, int kLevels = kTreeLevels>
 __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_deep_kernel(const __grid_constant__ FusedParams p) {
-  static_assert(!TREE || VPT == 1, "the tree order takes one vector per thread");
   using LV = Lane<BF16, true>;
   using LS = Lane<BF16, false>;
   constexpr int W = LV::W;
@@ -425,19 +457,37 @@ __global__ void __launch_bounds__(kThreads, AR_FUSED_MINB) fused_deep_kernel(con
     const char* const* seq = s_seq + seg_rotation(p, c.seg);
     float part[VPT][W];
     if constexpr (TREE) {
-      float slot[kLevels][W];
-      add_batch_tree<LV, NB, kLevels>(slot, v, 0, n, ok[0]);
+      if constexpr (VPT == 1) {
+        float slot[kLevels][W];
+        add_batch_tree<LV, NB, kLevels>(slot, v, 0, n, ok[0]);
 #pragma unroll 1
-      for (int base = NB; base < n; base += NB) {
-        load_batch<LV, NB, VPT>(v, seq, base, n, e, ok);
-        add_batch_tree<LV, NB, kLevels>(slot, v, base, n, ok[0]);
-      }
-#pragma unroll
-      for (int l = 0; l < kLevels; ++l)  // n = 2^K: the whole tree sits in slot K
-        if ((1 << l) == n) {
-#pragma unroll
-          for (int w = 0; w < W; ++w) part[0][w] = slot[l][w];
+        for (int base = NB; base < n; base += NB) {
+          load_batch<LV, NB, VPT>(v, seq, base, n, e, ok);
+          add_batch_tree<LV, NB, kLevels>(slot, v, base, n, ok[0]);
         }
+#pragma unroll
+        for (int l = 0; l < kLevels; ++l)  // n = 2^K: the whole tree sits in slot K
+          if ((1 << l) == n) {
+#pragma unroll
+            for (int w = 0; w < W; ++w) part[0][w] = slot[l][w];
+          }
+      } else {
+        float slot[VPT][kLevels][W];
+        add_batch_tree_v<LV, NB, VPT, kLevels>(slot, v, 0, n, ok);
+#pragma unroll 1
+        for (int base = NB; base < n; base += NB) {
+          load_batch<LV, NB, VPT>(v, seq, base, n, e, ok);
+          add_batch_tree_v<LV, NB, VPT, kLevels>(slot, v, base, n, ok);
+        }
+#pragma unroll
+        for (int l = 0; l < kLevels; ++l)
+          if ((1 << l) == n) {
+#pragma unroll
+            for (int q = 0; q < VPT; ++q)
+#pragma unroll
+              for (int w = 0; w < W; ++w) part[q][w] = slot[q][l][w];
+          }
+      }
     } else {
       add_batch<LV, NB, VPT>(part, v, 0, n, ok);
 #pragma unroll 1
@@ -737,13 +787,18 @@ int deep_nb(int n) { return n >= kDeepWideMin ? 16 : n > 4 ? 8 : n > 2 ? 4 : 2; 
 int deep_vpt(int n, bool bf16) {
   return n >= kDeepWideMin ? 1 : n > 4 ? 2 : n > 2 ? (bf16 ? 3 : 4) : (bf16 ? 4 : 5);
 }
+// The budgeted tree order keeps a slot per tree level and vector: one vector
+// per thread (above 16 bf16 ranks the full-width tree kernel runs), 2 below 8
+// fp32 ranks (wider shapes spill registers). At 32 SMs, fp32: 4 ranks 0.497
+// of HBM against 0.293 with one vector, 2 ranks 0.295 against 0.164.
+int tree_deep_vpt(int n, bool bf16) { return !bf16 && n < 8 ? 2 : 1; }
 
 // `deep` (a budgeted launch, see budgeted()): the all-reduce in ring or rank
 // order takes the deep kernel's shape; the hierarchical order over more than
 // 4 ranks takes 2 vectors per thread with 8 ranks per batch.
 int fused_vpt(int n, int order, int collective, bool bf16, bool deep) {
   if (collective == AR_ALLGATHER) return kAgVPT;
-  if (order == AR_ORDER_TREE) return 1;
+  if (order == AR_ORDER_TREE) return deep ? tree_deep_vpt(n, bf16) : 1;
   if (deep && order != AR_ORDER_HIER) return deep_vpt(n, bf16);  // all-reduce or reduce-scatter
   if (collective == AR_REDUCE_SCATTER && n > 4) return kRsVPT;
   if (deep && n > 4) return 2;
@@ -771,12 +826,15 @@ cudaError_t launch_fused_rot(const FusedParams& p, int64_t tiles, int sm_budget,
   if (p.order == AR_ORDER_TREE && p.collective != AR_ALLGATHER) {  // n is a power of two
     // budgeted: the deep kernel, 16 ranks per batch (bf16, whose wider sums
     // take twice the registers, 8, and only up to 16 ranks: 5 tree levels)
-    if (budgeted(sm_budget)) {
+    if (budgeted(sm_budget)) {  // vectors per thread: tree_deep_vpt
       if constexpr (BF16) {
-        if (p.n <= 16) return launch_persistent(fused_deep_kernel<true, 8, 1, false, true, 5>, p, tiles, sm_budget, stream);
+        if (p.n == 16) return launch_persistent(fused_deep_kernel<true, 8, 1, false, true, 5>, p, tiles, sm_budget, stream);
+        if (p.n == 8) return launch_persistent(fused_deep_kernel<true, 8, 1, false, true, 4>, p, tiles, sm_budget, stream);
+        if (p.n < 8) return launch_persistent(fused_deep_kernel<true, 4, 1, false, true, 3>, p, tiles, sm_budget, stream);
       } else {
-        return p.n >= 16 ? launch_persistent(fused_deep_kernel<false, 16, 1, false, true>, p, tiles, sm_budget, stream)
-                         : launch_persistent(fused_deep_kernel<false, 8, 1, false, true>, p, tiles, sm_budget, stream);
+        if (p.n >= 16) return launch_persistent(fused_deep_kernel<false, 16, 1, false, true>, p, tiles, sm_budget, stream);
+        if (p.n == 8) return launch_persistent(fused_deep_kernel<false, 8, 1, false, true>, p, tiles, sm_budget, stream);
+        return launch_persistent(fused_deep_kernel<false, 4, 2, false, true, 3>, p, tiles, sm_budget, stream);
       }
     }
     return launch_persistent(fused_flat_kernel<BF16, true, kSeqRotated, 8, 1>, p, tiles, sm_budget, stream);
