@@ -784,6 +784,14 @@ ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs
     if (s != AR_OK) return s;
   }
   for (const Step& st : p->steps) {
+    // A bf16 copy step whose transfers all start and end on an even element
+    // and move bf16 buffers (not the fp32 partials) runs as an fp32 copy of
+    // element pairs over the same bytes: 32-byte vectors when the buffers
+    // allow them, half the instructions per byte.
+    bool pairs = d.dtype == AR_BF16 && st.op == OP_COPY;
+    for (const Transfer& t : st.xfers)
+      pairs = pairs && t.lo % 2 == 0 && t.hi % 2 == 0 && t.xs != PART && t.ds != PART;
+    const int64_t div = pairs ? 2 : 1;
     // a step's transfers are independent (none writes what another reads), so
     // a step with more transfers than one launch holds runs as several
     for (size_t x0 = 0; x0 < st.xfers.size(); x0 += kMaxXfers) {
@@ -792,13 +800,17 @@ ar_status execute_steps(const ar_plan_t* p, void* const* bufs, void* const* outs
       for (int x = 0; x < sp.n_xfer; ++x) {
         const Transfer& t = st.xfers[x0 + size_t(x)];
         sp.x[x] = t;
+        sp.x[x].lo = t.lo / div;
+        sp.x[x].hi = t.hi / div;
         if (&st == &p->steps[0] && !pair_first.empty()) sp.x[x].pair = pair_first[x0 + size_t(x)];
         sp.tile_start[x] = tiles;
-        const int64_t body = std::max<int64_t>(rdown(t.hi, kStepVec) - rup(t.lo, kStepVec), 0);
+        const Transfer& u = sp.x[x];
+        const int64_t body = std::max<int64_t>(rdown(u.hi, kStepVec) - rup(u.lo, kStepVec), 0);
         tiles += int(std::max<int64_t>(1, (body + kStepTile - 1) / kStepTile));
       }
       sp.tile_start[sp.n_xfer] = tiles;
-      const ar_status s = from_cuda(launch_step(sp, d.dtype, st.op, tiles, true, d.sm_budget, v8, stream));
+      const ar_status s =
+          from_cuda(launch_step(sp, pairs ? AR_F32 : d.dtype, st.op, tiles, true, d.sm_budget, v8, stream));
       if (s != AR_OK) return s;
     }
   }

@@ -103,12 +103,13 @@ def test_allgather_bulk_copies(g, dtype, N, L, out_of_place):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("N,L", [(3, 1000), (8, 20003), (16, 100003), (5, 3)])
+@pytest.mark.parametrize("N,L", [(3, 1000), (8, 20003), (16, 100003), (5, 3), (16, 1 << 16), (6, 30000)])
 def test_ring_allgather_mixed_in_and_out_of_place(g, dtype, N, L):
     """Even ranks in place, odd ranks into separate outputs, in one call: the
     first ring step writes each sent chunk to the sender's own output only for
-    the ranks whose output is separate. Every output is the oracle's and every
-    separate input is left as it was."""
+    the ranks whose output is separate (bf16 chunks with even bounds move as
+    fp32 pairs). Every output is the oracle's and every separate input is left
+    as it was."""
     x = workloads.all_ranks(workloads.small_spec(N, L, dtype, "uniform", seed=N + L))
     devs = [to_device(x[r], dtype) for r in range(N)]
     outs = [d if r % 2 == 0 else torch.full_like(d, 7.0) for r, d in enumerate(devs)]

@@ -119,11 +119,13 @@ def test_allreduce_stays_inside_its_buffers(g, algo, order, G, dims, dtype, alig
                           ("fused", "reduce_scatter", "loads", 5, False), ("ring", "allgather", "auto", 0, False),
                           ("ring", "allgather", "auto", 0, True), ("fused", "allgather", "loads", 0, False),
                           ("fused", "allgather", "bulk", 0, False), ("fused", "allgather", "bulk", 0, True)])
-def test_collectives_stay_inside_their_buffers(g, algo, coll, kernel, sm_budget, out_of_place, dtype, align16):
+@pytest.mark.parametrize("L", [20011, 20010])
+def test_collectives_stay_inside_their_buffers(g, algo, coll, kernel, sm_budget, out_of_place, dtype, align16, L):
     """Out of place the ring all-gather's first step also writes each sent
     chunk to the sender's output; held to a few SMs the reduce-scatter runs
-    the kernel that loads ahead across tiles."""
-    N, L = 5, 20011
+    the kernel that loads ahead across tiles; with even chunk bounds (L =
+    20010) bf16 copy steps move fp32 pairs."""
+    N = 5
     x = workloads.all_ranks(workloads.small_spec(N, L, dtype, "uniform", seed=3 + L))
     xf = widened(x, dtype)
     b = chunk_bounds(L, N)
