@@ -189,7 +189,11 @@ typedef struct {
   int sm_budget;   /* at most this many SMs' worth of CTAs per kernel (0 = all SMs).
                       A collective that overlaps computation takes only part of
                       the GPU, as a NCCL channel takes one SM (primer §4.5).
-                      Results do not depend on it. */
+                      A budget of B launches the CTAs B SMs hold (2 B for the
+                      single pass), which the scheduler spreads one per SM; the
+                      single pass then loads the next tile while it stores
+                      this one (all orders but the hierarchical). Results do
+                      not depend on it. */
   ar_kernel kernel; /* AR_KERNEL_AUTO (0) unless set */
   int torus_dims[3]; /* AR_TORUS: {X, Y, Z}, a 0 counting as 1, product N
                         (AR_EINVAL otherwise); ignored by the others */
